@@ -1,0 +1,135 @@
+"""Seeded synthetic inputs for C = A·Bᵀ (fp16 A: M×K, fp16 B: N×K, row-major).
+
+This module holds no GEMM arithmetic. It is the one piece that both the CUDA
+path (tests, bench) and the CPU oracle are fed from, so that both see the same
+matrices.
+
+Generator. A counter-based SplitMix64 stream (Steele, Lea and Flood, "Fast
+splittable pseudorandom number generators", OOPSLA 2014; the constants are the
+ones of Vigna's public-domain splitmix64.c):
+
+    mix64(z):  z ^= z >> 30; z *= 0xBF58476D1CE4E5B9
+               z ^= z >> 27; z *= 0x94D049BB133111EB
+               z ^= z >> 31
+    key        = mix64(seed · 2^16 + tensor_id)
+    h(i)       = mix64(key + (i + 1) · 0x9E3779B97F4A7C15)     (mod 2^64)
+
+`i` is the logical row-major index row·cols + col, independent of the leading
+dimension. With key = 0, h(0) is the first output of SplitMix64 seeded with 0.
+
+Values.
+* "uniform": u = (h >> 11) · 2^-53 in [0, 1), x = 2u − 1, rounded to fp16
+  with round-to-nearest-even (numpy's float64 → float16 cast keeps fp16
+  subnormals).
+* "int": v = ((h >> 32) · 5) >> 32, x = v − 2 in {−2, …, 2} (exact in fp16).
+
+The pages measured on integers in [−3, 3] from a hash of the index
+("SASS-Level Kernel Generation for Blackwell", How we measured); the
+workloads here use uniform[−1, 1] fp16 plus a {−2..2} integer copy.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_MASK = (1 << 64) - 1
+
+# fp16 quiet NaN, used to poison padding columns so that a reader that strays
+# past K is caught.
+F16_NAN_BITS = 0x7E00
+
+
+def mix64_int(z: int) -> int:
+    """SplitMix64 finaliser on a Python int (mod 2^64)."""
+    z &= _MASK
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _MASK
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _MASK
+    return z ^ (z >> 31)
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def stream_key(seed: int, tensor_id: int) -> int:
+    return mix64_int(seed * (1 << 16) + tensor_id)
+
+
+def hash_stream(key: int, start: int, count: int) -> np.ndarray:
+    """h(i) for i in [start, start + count), as uint64."""
+    idx = np.arange(start + 1, start + 1 + count, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return _mix64(np.uint64(key) + idx * _GAMMA)
+
+
+def _values(h: np.ndarray, kind: str) -> np.ndarray:
+    if kind == "uniform":
+        u = (h >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+        return (2.0 * u - 1.0).astype(np.float16)
+    if kind == "int":
+        with np.errstate(over="ignore"):
+            v = ((h >> np.uint64(32)) * np.uint64(5)) >> np.uint64(32)
+        return (v.astype(np.int64) - 2).astype(np.float16)
+    raise ValueError(f"unknown value kind {kind!r}")
+
+
+def matrix(rows: int, cols: int, seed: int, tensor_id: int, kind: str = "uniform",
+           ld: int | None = None, pad: str = "zero",
+           chunk_elems: int = 1 << 22) -> np.ndarray:
+    """A rows×ld fp16 array whose first `cols` columns hold the seeded stream.
+
+    Columns [cols, ld) are padding: zeros (pad="zero") or fp16 NaN (pad="nan").
+    The stream index of element (r, c) is r·cols + c, so the values do not
+    depend on `ld`.
+    """
+    ld = cols if ld is None else ld
+    if ld < cols:
+        raise ValueError("ld < cols")
+    out = np.empty((rows, ld), dtype=np.float16)
+    if ld > cols:
+        if pad == "nan":
+            out[:, cols:].view(np.uint16)[...] = F16_NAN_BITS
+        else:
+            out[:, cols:] = 0
+    if rows == 0 or cols == 0:
+        return out
+    key = stream_key(seed, tensor_id)
+    rows_per_chunk = max(1, chunk_elems // cols)
+    for r0 in range(0, rows, rows_per_chunk):
+        r1 = min(rows, r0 + rows_per_chunk)
+        h = hash_stream(key, r0 * cols, (r1 - r0) * cols)
+        out[r0:r1, :cols] = _values(h, kind).reshape(r1 - r0, cols)
+    return out
+
+
+def gemm_operands(M: int, N: int, K: int, seed: int, kind: str = "uniform",
+                  lda: int | None = None, ldb: int | None = None,
+                  pad: str = "zero") -> tuple[np.ndarray, np.ndarray]:
+    """The A (M×lda) and B (N×ldb) fp16 operands of one problem: tensor ids 0 and 1."""
+    A = matrix(M, K, seed, 0, kind, lda, pad)
+    B = matrix(N, K, seed, 1, kind, ldb, pad)
+    return A, B
+
+
+def sample_indices(n: int, count: int, seed: int, tensor_id: int) -> np.ndarray:
+    """`count` distinct sorted indices in [0, n) that always include 0 and n−1.
+
+    Used to check large problems on a sampled set of rows and columns.
+    """
+    if count >= n:
+        return np.arange(n, dtype=np.int64)
+    h = hash_stream(stream_key(seed, tensor_id), 0, 4 * count + 64)
+    picked = {0, n - 1}
+    for v in (h % np.uint64(n)).astype(np.int64):
+        if len(picked) >= count:
+            break
+        picked.add(int(v))
+    j = 0
+    while len(picked) < count:  # only for pathological collisions
+        picked.add(j)
+        j += 1
+    return np.array(sorted(picked), dtype=np.int64)
