@@ -1,0 +1,416 @@
+"""Benchmark of the dense GEMM C = A·Bᵀ (fp16 in, fp32 accumulate and out).
+
+One step = one call of each shape of the workload, each call timed alone with
+CUDA events on the launching stream, an L2 flush (a 256 MiB write) between
+calls, nothing overlapping ("SASS-Level Kernel Generation for Blackwell",
+section "How we measured": every call runs alone). Inputs are seeded
+synthetic uniform[-1, 1] fp16 matrices, resident in HBM before timing starts.
+
+Default workload: the square and near-square sweep (1536³, 2048³, 4096³,
+3072×1280×2048, 4096×4096×1024, 8192×2048×4096). Other workloads: c1
+(1024³), splitk (1024×1024×65536), streamk (2048×2048×16384), large (8192³,
+16384³), all.
+
+Prints one JSON line (rank 0). `value` = Σ 2·M·N·K over the step's calls ÷
+Σ their GPU times, in TFLOP/s, over all ranks (replicas for N > 1).
+
+`--impl reference` times the CPU oracle (the plain fp64 triple loop) on the
+host cores, on a bounded row sample of the same shapes, in the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("µs/call and TFLOP/s per shape (1 GB300) + fraction of dense fp16 tensor peak")
+WORKLOADS = {
+    "c1": [(1024, 1024, 1024)],
+    "sweep": [(1536, 1536, 1536), (2048, 2048, 2048), (4096, 4096, 4096), (3072, 1280, 2048),
+              (4096, 4096, 1024), (8192, 2048, 4096)],
+    "splitk": [(1024, 1024, 65536)],
+    "streamk": [(2048, 2048, 16384)],
+    "large": [(8192, 8192, 8192), (16384, 16384, 16384)],
+}
+WORKLOADS["all"] = (WORKLOADS["c1"] + WORKLOADS["sweep"] + WORKLOADS["large"]
+                    + WORKLOADS["streamk"] + WORKLOADS["splitk"])
+FLUSH_BYTES = 256 << 20  # > the 129 MB L2
+FALLBACK_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def shape_name(s):
+    return "x".join(str(v) for v in s)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_fp16_gemm_02_gb300", "csrc")
+    for d, _, files in sorted(os.walk(csrc)):
+        for f in sorted(files):
+            if f.endswith((".cu", ".cuh", ".h")):
+                with open(os.path.join(d, f), "rb") as fh:
+                    h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(config_name: str, shape):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources for this configuration and shape."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rows = json.load(f)
+    except (OSError, ValueError):
+        return None
+    digest = kernel_source_digest()
+    for r in rows:
+        if (r.get("kernel_src") == digest and r.get("config") == config_name
+                and r.get("shape") == shape_name(shape)):
+            return r.get("dram_bytes")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample_rate(shapes, seconds_per_shape: float, nthreads: int = 0):
+    """Times the CPU oracle on a row sample of every shape; returns
+    (TFLOP/s over the sample, threads, description)."""
+    import numpy as np
+
+    import oracle
+    from dense_fp16_gemm_02_gb300 import inputs
+    total_flops, total_t, desc = 0.0, 0.0, []
+    threads = nthreads or oracle.hardware_threads()
+    for (M, N, K) in shapes:
+        # Calibrate on a few rows, then size the sample to the time budget.
+        rows = 4
+        A = inputs.matrix(rows, K, 1000, 0)
+        B = inputs.matrix(N, K, 1000, 1)
+        t0 = time.perf_counter()
+        oracle.gemm_f64(A, B, nthreads=threads)
+        dt = max(time.perf_counter() - t0, 1e-4)
+        rows = int(max(threads, min(M, rows * seconds_per_shape / dt)))
+        rows = max(threads, (rows // threads) * threads) if rows >= threads else rows
+        A = inputs.matrix(rows, K, 1000, 0)
+        t0 = time.perf_counter()
+        oracle.gemm_f64(A, B, nthreads=threads)
+        dt = time.perf_counter() - t0
+        total_flops += 2.0 * rows * N * K
+        total_t += dt
+        desc.append(f"{rows} of {M} rows of {shape_name((M, N, K))}")
+        del A, B
+        _ = np
+    return total_flops / total_t / 1e12, threads, "; ".join(desc), total_t
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    shapes = WORKLOADS[args.workload]
+    budget = max(0.5, min(20.0, 60.0 / (len(shapes) * max(1, args.steps + args.warmup))))
+    for _ in range(args.warmup):
+        oracle_sample_rate(shapes, budget / 4)
+    vals, last = [], None
+    for _ in range(args.steps):
+        last = oracle_sample_rate(shapes, budget)
+        vals.append(last[0])
+    value = statistics.median(vals)
+    tflop_per_step = sum(2.0 * M * N * K for (M, N, K) in shapes) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tflop_per_step / value * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload + ": " + ", ".join(shape_name(s) for s in shapes),
+                   "oracle": "plain fp64 triple loop in C (oracle/wgemm_oracle.c)",
+                   "sample": "row sample per shape, extrapolated per call"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last[1], "kind": "oracle",
+                         "sample": last[2]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
+
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    build.build()
+    wgemm.load()
+    shapes = WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream()
+    h = stream.cuda_stream
+
+    # Inputs: generated on the host once, uploaded before timing.
+    data = []
+    for i, (M, N, K) in enumerate(shapes):
+        A, B = inputs.gemm_operands(M, N, K, seed=1000 + i, kind="uniform")
+        dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
+        data.append((A, B, dA, dB, C))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    names = wgemm.config_names()
+
+    def call(i):
+        (M, N, K) = shapes[i]
+        _, _, dA, dB, C = data[i]
+        rc = wgemm.wgemm_f16f32(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, K, K, N, h)
+        if rc != 0:
+            raise RuntimeError(f"wgemm_f16f32 failed: {rc}")
+
+    def one_step(events):
+        for i in range(len(shapes)):
+            flush.fill_(float(i))  # evict L2; the GPU is busy while the call is enqueued
+            e0, e1 = events[i]
+            e0.record(stream)
+            call(i)
+            e1.record(stream)
+
+    mk = lambda: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in shapes]
+    for _ in range(args.warmup):
+        one_step(mk())
+    rc = wgemm.wgemm_check(h)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc}: {wgemm.wgemm_last_device_error()}")
+
+    per_step_events = [mk() for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for s in range(args.steps):
+            one_step(per_step_events[s])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    rc = wgemm.wgemm_check(h)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc}: {wgemm.wgemm_last_device_error()}")
+    gpu_launches = args.steps * len(shapes)
+
+    times = np.array([[e0.elapsed_time(e1) for (e0, e1) in ev] for ev in per_step_events])  # ms
+    step_ms = float(np.median(times.sum(axis=1)))
+    flops = np.array([2.0 * M * N * K for (M, N, K) in shapes])
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = world * flops.sum() / (step_ms * 1e-3) / 1e12
+    peak_tflops, peak_hbm, peak_src = peaks()
+
+    # Per-shape report, and the configuration each call ran.
+    per_shape = []
+    by_config = {}
+    for i, (M, N, K) in enumerate(shapes):
+        us = times[:, i] * 1e3
+        cfg, mode, splits = wgemm.wgemm_select(M, N, K)
+        med = float(np.median(us))
+        tf = flops[i] / (med * 1e-6) / 1e12
+        bytes_min = 2.0 * (M * K + N * K) + 4.0 * M * N
+        per_shape.append({
+            "shape": shape_name((M, N, K)), "us_median": round(med, 3),
+            "us_min": round(float(us.min()), 3), "us_max": round(float(us.max()), 3),
+            "tflops": round(tf, 1), "tensor_frac": round(tf / peak_tflops, 4),
+            "hbm_gbs": round(bytes_min / (med * 1e-6) / 1e9, 1),
+            "hbm_frac": round(bytes_min / (med * 1e-6) / 1e9 / peak_hbm, 4),
+            "config": names[cfg], "mode": ["data-parallel", "split-K", "stream-K"][mode],
+            "splits": splits})
+        agg = by_config.setdefault(names[cfg], {"flops": 0.0, "ms": 0.0, "launches": 0,
+                                                "shape": (M, N, K), "shape_ms": 0.0})
+        agg["flops"] += flops[i] * args.steps
+        agg["ms"] += float(times[:, i].sum())
+        agg["launches"] += args.steps
+        if float(times[:, i].sum()) > agg["shape_ms"]:
+            agg["shape"], agg["shape_ms"] = (M, N, K), float(times[:, i].sum())
+    dom_name, dom = max(by_config.items(), key=lambda kv: kv[1]["ms"])
+    achieved = dom["flops"] / (dom["ms"] * 1e-3) / 1e12
+
+    # End to end through the public API with host buffers: H2D of A and B from
+    # pinned memory, the call, D2H of C, all inside the timed region.
+    pinned = []
+    for (A, B, _, _, C) in data:
+        hA = torch.from_numpy(A).pin_memory()
+        hB = torch.from_numpy(B).pin_memory()
+        hC = torch.empty(C.shape, dtype=torch.float32).pin_memory()
+        pinned.append((hA, hB, hC))
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_ms = []
+    for s in range(e2e_steps + 1):
+        tot = 0.0
+        for i, (M, N, K) in enumerate(shapes):
+            hA, hB, hC = pinned[i]
+            _, _, dA, dB, C = data[i]
+            flush.fill_(0.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            call(i)
+            hC.copy_(C, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+        if s > 0:  # the first pass warms the copy engines
+            e2e_ms.append(tot)
+    e2e_step_ms = statistics.median(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_step_ms = float(t.item())
+    h2d = sum(2 * (M * K + N * K) for (M, N, K) in shapes)
+    d2h = sum(4 * M * N for (M, N, K) in shapes)
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            rate, cores, sample, secs = oracle_sample_rate(shapes, args.cpu_seconds / len(shapes))
+            cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{sample} ({secs:.1f} s of oracle work)"}
+        line = {
+            "metric": METRIC, "value": round(float(value), 2), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {
+                "workload": args.workload + ": " + ", ".join(shape_name(s) for s in shapes),
+                "inputs": "uniform[-1,1] rounded to fp16, seeded SplitMix64, resident in HBM",
+                "accumulate": "f32", "output": "f32",
+                "l2": "flushed between calls (256 MiB write), each call timed alone",
+                "timing": "CUDA events on the launching stream around each call",
+                "parallelism": "replicas" if world > 1 else "single GPU",
+            },
+            "shapes": per_shape,
+            "roofline": {
+                "bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 1),
+                "peak": peak_tflops, "unit": "TFLOP/s", "frac": round(achieved / peak_tflops, 4),
+                "peak_source": f"{peak_src}: bf16 cuBLAS burst x fp16/bf16 nominal ratio 1",
+                "traffic": committed_traffic(dom_name, dom["shape"]),
+                "traffic_shape": shape_name(dom["shape"]),
+            },
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(world * float(flops.sum()) / (e2e_step_ms * 1e-3) / 1e12, 2),
+                    "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": gpu_launches,
+            "clocks": clocks.summary(),
+            "wall_s_timed": round(t_wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="sweep")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="oracle time budget of the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

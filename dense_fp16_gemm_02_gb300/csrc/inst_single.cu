@@ -1,0 +1,15 @@
+// Kernel configurations with one CTA per MMA (tcgen05.mma.cta_group::1, M = 128).
+#include "wgemm_configs.h"
+#include "wgemm_kernel.cuh"
+
+namespace wg {
+
+const KernelEntry kEntriesSingle[] = {
+    WG_ENTRY("g1_128x256_s4_a2_tma", 1, 1, 256, 4, 2, kEpiTma),
+    WG_ENTRY("g1_128x256_s4_a2_direct", 1, 1, 256, 4, 2, kEpiDirect),
+    WG_ENTRY("g1_128x128_s6_a2_tma", 1, 1, 128, 6, 2, kEpiTma),
+    WG_ENTRY("g1_128x64_s8_a2_direct", 1, 1, 64, 8, 2, kEpiDirect),
+};
+const int kNumEntriesSingle = sizeof(kEntriesSingle) / sizeof(kEntriesSingle[0]);
+
+}  // namespace wg

@@ -1,0 +1,514 @@
+// Host side of the C-ABI library: argument checks, per-shape configuration
+// choice, tensor-map encoding, the split-K / stream-K flag workspace, and the
+// launch. Declarations and their contracts are in include/wgemm.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "wgemm.h"
+#include "wgemm_configs.h"
+#include "wgemm_kernel.cuh"
+#include "wgemm_plan.h"
+
+namespace wg {
+
+// The per-device status word the kernels write on a failed wait.
+__device__ DeviceStatus g_device_status;
+
+__global__ void wgemm_zero_kernel(float* C, int32_t M, int32_t N, int64_t ldc) {
+  const int64_t total = (int64_t)M * N;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / N, c = i - r * N;
+    C[r * ldc + c] = 0.f;
+  }
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct Registry {
+  std::vector<const KernelEntry*> entries;
+  Registry() {
+    for (int i = 0; i < kNumEntriesSingle; ++i) entries.push_back(&kEntriesSingle[i]);
+    for (int i = 0; i < kNumEntriesPair; ++i) entries.push_back(&kEntriesPair[i]);
+  }
+};
+
+const Registry& registry() {
+  static Registry r;
+  return r;
+}
+
+struct DeviceState {
+  bool init = false;
+  bool supported = false;
+  int sm_count = 0;
+  DeviceStatus* status = nullptr;      // device address of g_device_status
+  std::vector<int> max_workers;        // per config: co-resident clusters (0 = not queried)
+  DeviceStatus last_error{};
+};
+
+struct Workspace {
+  uint32_t* flags = nullptr;
+  size_t bytes = 0;
+  uint32_t epoch = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool env_log() {
+  static const bool on = [] {
+    const char* v = std::getenv("WGEMM_LOG");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+
+// Requires g_mu.
+int device_state(int* dev_out, DeviceState** st_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return WGEMM_ERR_NO_DEVICE;
+  }
+  DeviceState& st = g_dev[dev];
+  if (!st.init) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return WGEMM_ERR_NO_DEVICE;
+    }
+    st.supported = prop.major == 10 && prop.minor == 3;
+    st.sm_count = prop.multiProcessorCount;
+    if (st.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) {
+        cudaGetLastError();
+        return WGEMM_ERR_LAUNCH;
+      }
+      st.status = static_cast<DeviceStatus*>(p);
+      if (cudaMemset(st.status, 0, sizeof(DeviceStatus)) != cudaSuccess) return WGEMM_ERR_LAUNCH;
+    }
+    st.max_workers.assign(registry().entries.size(), 0);
+    st.init = true;
+  }
+  if (!st.supported) return WGEMM_ERR_NO_DEVICE;
+  *dev_out = dev;
+  *st_out = &st;
+  return WGEMM_OK;
+}
+
+int encoder() {
+  if (g_encode) return WGEMM_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    cudaGetLastError();
+    return WGEMM_ERR_LAUNCH;
+  }
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return WGEMM_OK;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t elem_strides[2] = {1, 1};
+  return g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, elem_strides,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaLaunchConfig_t launch_config(const KernelEntry& e, int workers, cudaStream_t stream,
+                                 cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(workers * e.cg), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = e.smem_bytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)e.cg;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Requires g_mu. Co-resident workers (clusters) of a configuration on this
+// device; sets the kernel's shared-memory attribute on first use.
+int max_workers(DeviceState& st, int id) {
+  if (st.max_workers[id] > 0) return st.max_workers[id];
+  const KernelEntry& e = *registry().entries[id];
+  if (cudaFuncSetAttribute(e.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)e.smem_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return WGEMM_ERR_LAUNCH;
+  }
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(e, st.sm_count / e.cg, nullptr, attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, e.func, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return WGEMM_ERR_LAUNCH;
+  }
+  st.max_workers[id] = n;
+  return n;
+}
+
+int find_config(const char* name) {
+  const auto& es = registry().entries;
+  for (size_t i = 0; i < es.size(); ++i)
+    if (std::strcmp(es[i]->name, name) == 0) return (int)i;
+  return -1;
+}
+
+// The per-shape choice. A measured table of winners first, then a rule.
+struct Choice {
+  int config, mode, splits;
+};
+
+Choice choose(int M, int N, int K, int workers_hint) {
+  const int64_t mn = (int64_t)M * N;
+  const int kblocks = (K + kBK - 1) / kBK;
+  // Few output tiles and a long K: split K (tiles far fewer than workers) or
+  // stream-K (tiles below one wave).
+  const int big = find_config("g2_512x256_s4_a1_tma");
+  const int64_t tiles_big = (int64_t)((M + 255) / 256) * ((N + 511) / 512);
+  if (kblocks >= 64 && tiles_big * 4 <= workers_hint) {
+    int s = (int)std::max<int64_t>(1, workers_hint / std::max<int64_t>(1, tiles_big));
+    s = std::min(s, kblocks / 8);
+    if (s >= 2) return {big, kSplitK, s};
+  }
+  const int sk = find_config("g2_512x128_s4_a2_tma");
+  const int64_t tiles_sk = (int64_t)((M + 127) / 128) * ((N + 511) / 512);
+  if (kblocks >= 64 && tiles_sk < workers_hint) return {sk, kStreamK, 1};
+  if (mn >= (int64_t)4096 * 4096) return {big, kDataParallel, 1};
+  if (mn >= (int64_t)1536 * 1536) return {find_config("g2_256x256_s6_a2_tma"), kDataParallel, 1};
+  return {find_config("g2_256x64_s10_a2_direct"), kDataParallel, 1};
+}
+
+int check_args(const void* A, const void* B, const void* C, int M, int N, int K, int lda, int ldb,
+               int ldc) {
+  if (M < 0 || N < 0 || K < 0) return WGEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return WGEMM_OK;
+  if (!C) return WGEMM_ERR_INVALID_ARG;
+  if (ldc < N) return WGEMM_ERR_INVALID_ARG;
+  if (K > 0) {
+    if (!A || !B || lda < K || ldb < K) return WGEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) ||
+        (lda % 8) || (ldb % 8))
+      return WGEMM_ERR_ALIGNMENT;
+  }
+  if ((reinterpret_cast<uintptr_t>(C) & 15) || (ldc % 4)) return WGEMM_ERR_ALIGNMENT;
+  return WGEMM_OK;
+}
+
+// Fills the plan for a configuration; WGEMM_ERR_CONFIG if the mode cannot run.
+int make_plan(const KernelEntry& e, int M, int N, int K, int mode, int splits, int max_w,
+              Plan* p) {
+  std::memset(p, 0, sizeof(*p));
+  p->M = M;
+  p->N = N;
+  p->K = K;
+  p->tile_rows = e.tile_rows;
+  p->tile_cols = e.tile_cols;
+  p->tiles_m = (M + e.tile_rows - 1) / e.tile_rows;
+  p->tiles_n = (N + e.tile_cols - 1) / e.tile_cols;
+  p->num_tiles = p->tiles_m * p->tiles_n;
+  p->kblocks = (K + kBK - 1) / kBK;
+  p->mode = mode;
+  p->splits = 1;
+  p->group = 8;
+  if (mode != kDataParallel && e.epi != kEpiTma) return WGEMM_ERR_CONFIG;
+  if (mode == kDataParallel) {
+    p->workers = std::min(p->num_tiles, max_w);
+  } else if (mode == kSplitK) {
+    if (splits < 1) return WGEMM_ERR_CONFIG;
+    p->splits = std::min(splits, p->kblocks);
+    p->workers = (int32_t)std::min<int64_t>((int64_t)p->num_tiles * p->splits, max_w);
+  } else if (mode == kStreamK) {
+    p->total_iters = (int64_t)p->num_tiles * p->kblocks;
+    p->workers = (int32_t)std::min<int64_t>(p->total_iters, max_w);
+  } else {
+    return WGEMM_ERR_CONFIG;
+  }
+  return p->workers > 0 ? WGEMM_OK : WGEMM_ERR_CONFIG;
+}
+
+// Requires g_mu. Flags for a call on (dev, stream): at least `words` words.
+int workspace(int dev, cudaStream_t stream, size_t words, Workspace** out) {
+  Workspace& ws = g_ws[{dev, stream}];
+  const size_t bytes = std::max<size_t>(words * sizeof(uint32_t), 4096);
+  if (ws.bytes < bytes) {
+    if (ws.flags) {
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return WGEMM_ERR_LAUNCH;
+      cudaFree(ws.flags);
+      ws.flags = nullptr;
+      ws.bytes = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return WGEMM_ERR_WORKSPACE;
+    }
+    if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+      cudaFree(p);
+      return WGEMM_ERR_WORKSPACE;
+    }
+    ws.flags = static_cast<uint32_t*>(p);
+    ws.bytes = bytes;
+    ws.epoch = 0;
+  }
+  *out = &ws;
+  return WGEMM_OK;
+}
+
+int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int lda, int ldb,
+        int ldc, int config_id, int mode, int splits, cudaStream_t stream) {
+  int rc = check_args(A, B, C, M, N, K, lda, ldb, ldc);
+  if (rc != WGEMM_OK) return rc;
+  if (M == 0 || N == 0) return WGEMM_OK;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  DeviceState* st;
+  if ((rc = device_state(&dev, &st)) != WGEMM_OK) return rc;
+  if (K == 0) {
+    const int64_t total = (int64_t)M * N;
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)st->sm_count * 8);
+    wgemm_zero_kernel<<<blocks, 256, 0, stream>>>(C, M, N, ldc);
+    return cudaGetLastError() == cudaSuccess ? WGEMM_OK : WGEMM_ERR_LAUNCH;
+  }
+  const auto& es = registry().entries;
+  if (config_id < 0) {
+    // Workers of the pair configurations bound the split / stream-K choice.
+    const int hint = st->sm_count / 2;
+    Choice c = choose(M, N, K, hint);
+    config_id = c.config;
+    mode = c.mode;
+    splits = c.splits;
+  }
+  if (config_id < 0 || config_id >= (int)es.size()) return WGEMM_ERR_CONFIG;
+  const KernelEntry& e = *es[config_id];
+  if (mode < 0) {
+    Choice c = choose(M, N, K, st->sm_count / 2);
+    mode = c.mode;
+    splits = c.splits;
+    if (mode != kDataParallel && e.epi != kEpiTma) mode = kDataParallel;
+  }
+  const int mw = max_workers(*st, config_id);
+  if (mw < 0) return mw;
+  if ((rc = encoder()) != WGEMM_OK) return rc;
+
+  KParams params;
+  std::memset(&params, 0, sizeof(params));
+  if ((rc = make_plan(e, M, N, K, mode, splits, mw, &params.plan)) != WGEMM_OK) return rc;
+  const int brows_a = e.bn / e.cg, rows_b = 128 * e.reps;
+  if (!encode_2d(&params.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
+                 (uint64_t)lda * 2, kBK, (uint32_t)brows_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&params.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)K, (uint64_t)N,
+                 (uint64_t)ldb * 2, kBK, (uint32_t)rows_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&params.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, (uint64_t)N, (uint64_t)M,
+                 (uint64_t)ldc * 4, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return WGEMM_ERR_LAUNCH;
+  params.C = C;
+  params.ldc = ldc;
+  params.status = st->status;
+  if (params.plan.mode != kDataParallel) {
+    Workspace* ws;
+    const size_t words = (size_t)params.plan.num_tiles * e.cg * params.plan.splits;
+    if ((rc = workspace(dev, stream, words, &ws)) != WGEMM_OK) return rc;
+    params.flags = ws->flags;
+    params.epoch = ++ws->epoch;
+  }
+  if (env_log())
+    std::fprintf(stderr, "wgemm: %dx%dx%d config %s mode %d splits %d workers %d tiles %d\n", M, N,
+                 K, e.name, params.plan.mode, params.plan.splits, params.plan.workers,
+                 params.plan.num_tiles);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(e, params.plan.workers, stream, attr);
+  void* args[] = {&params};
+  if (cudaLaunchKernelExC(&cfg, e.func, args) != cudaSuccess) {
+    cudaGetLastError();
+    return WGEMM_ERR_LAUNCH;
+  }
+  return WGEMM_OK;
+}
+
+}  // namespace
+}  // namespace wg
+
+using namespace wg;
+
+extern "C" {
+
+int wgemm_f16f32(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C, int M, int N, int K,
+                 int lda, int ldb, int ldc, wgemm_stream_t stream) {
+  return run(A, B, C, M, N, K, lda, ldb, ldc, -1, -1, 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int wgemm_f16f32_config(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C, int M, int N, int K,
+                        int lda, int ldb, int ldc, int config_id, int mode, int splits,
+                        wgemm_stream_t stream) {
+  if (config_id < 0 || config_id >= (int)registry().entries.size()) return WGEMM_ERR_CONFIG;
+  if (mode < -1 || mode > 2) return WGEMM_ERR_CONFIG;
+  return run(A, B, C, M, N, K, lda, ldb, ldc, config_id, mode, splits,
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int wgemm_num_configs(void) { return (int)registry().entries.size(); }
+
+const char* wgemm_config_name(int id) {
+  const auto& es = registry().entries;
+  return (id >= 0 && id < (int)es.size()) ? es[id]->name : "";
+}
+
+int wgemm_select(int M, int N, int K, int* config_id, int* mode, int* splits) {
+  if (M < 0 || N < 0 || K < 0) return WGEMM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  DeviceState* st;
+  const int rc = device_state(&dev, &st);
+  if (rc != WGEMM_OK) return rc;
+  Choice c = choose(M, N, K, st->sm_count / 2);
+  if (config_id) *config_id = c.config;
+  if (mode) *mode = c.mode;
+  if (splits) *splits = c.splits;
+  return WGEMM_OK;
+}
+
+int wgemm_check(wgemm_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return WGEMM_ERR_LAUNCH;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  DeviceState* st;
+  int rc = device_state(&dev, &st);
+  if (rc != WGEMM_OK) return rc;
+  DeviceStatus s;
+  if (cudaMemcpy(&s, st->status, sizeof(s), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return WGEMM_ERR_LAUNCH;
+  if (s.code != 0) {
+    st->last_error = s;
+    if (cudaMemset(st->status, 0, sizeof(DeviceStatus)) != cudaSuccess) return WGEMM_ERR_LAUNCH;
+    return s.code;
+  }
+  return WGEMM_OK;
+}
+
+int wgemm_last_device_error(int* block, int* warp, int* site, int* parity) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return WGEMM_ERR_NO_DEVICE;
+  }
+  const DeviceStatus& s = g_dev[dev].last_error;
+  if (block) *block = s.block;
+  if (warp) *warp = s.warp;
+  if (site) *site = s.site;
+  if (parity) *parity = s.parity;
+  return s.code;
+}
+
+const char* wgemm_status_string(int status) {
+  switch (status) {
+    case WGEMM_OK: return "ok";
+    case WGEMM_ERR_INVALID_ARG: return "invalid argument";
+    case WGEMM_ERR_ALIGNMENT: return "misaligned pointer or leading dimension";
+    case WGEMM_ERR_LAUNCH: return "CUDA error while preparing or launching";
+    case WGEMM_ERR_NO_DEVICE: return "no current device of compute capability 10.3";
+    case WGEMM_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel expired";
+    case WGEMM_ERR_CONFIG: return "configuration cannot run this shape or mode";
+    case WGEMM_ERR_WORKSPACE: return "flag workspace allocation failed";
+    default: return "unknown status";
+  }
+}
+
+size_t wgemm_workspace_bytes(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  size_t total = 0;
+  for (const auto& kv : g_ws)
+    if (kv.first.first == dev) total += kv.second.bytes;
+  return total;
+}
+
+int wgemm_release_workspace(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return WGEMM_ERR_NO_DEVICE;
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) return WGEMM_ERR_LAUNCH;
+  for (auto it = g_ws.begin(); it != g_ws.end();) {
+    if (it->first.first == dev) {
+      if (it->second.flags) cudaFree(it->second.flags);
+      it = g_ws.erase(it);
+    } else {
+      ++it;
+    }
+  }
+  return WGEMM_OK;
+}
+
+uint64_t wgemm_debug_smem_desc(uint32_t smem_addr) { return umma_smem_desc_sw128(smem_addr); }
+
+uint32_t wgemm_debug_idesc(int M, int N) { return umma_idesc_f16((uint32_t)M, (uint32_t)N); }
+
+uint32_t wgemm_debug_sw128_offset(uint32_t row, uint32_t k) { return sw128_offset_f16(row, k); }
+
+int wgemm_debug_plan(int M, int N, int K, int config_id, int mode, int splits, int workers,
+                     int32_t* out, int max_units, int* tile_rows, int* tile_cols) {
+  const auto& es = registry().entries;
+  if (config_id < 0 || config_id >= (int)es.size() || M <= 0 || N <= 0 || K <= 0 || workers <= 0)
+    return WGEMM_ERR_INVALID_ARG;
+  const KernelEntry& e = *es[config_id];
+  Plan p;
+  const int rc = make_plan(e, M, N, K, mode, splits, workers, &p);
+  if (rc != WGEMM_OK) return rc;
+  if (tile_rows) *tile_rows = e.tile_rows;
+  if (tile_cols) *tile_cols = e.tile_cols;
+  int n = 0;
+  for (int w = 0; w < p.workers; ++w) {
+    for (int i = 0;; ++i) {
+      Unit u;
+      if (!plan_unit(p, w, i, u)) break;
+      if (out && n < max_units) {
+        int32_t* o = out + 7 * n;
+        o[0] = u.tile; o[1] = u.tm; o[2] = u.tn; o[3] = u.kb_begin; o[4] = u.kb_end;
+        o[5] = u.kind; o[6] = u.split;
+      }
+      ++n;
+    }
+  }
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,543 @@
+// The GEMM kernel family: one warp-specialised persistent kernel, templated on
+// its tile, pair mode, ring depth, accumulator count and epilogue.
+//
+// Roles ("SASS-Level Kernel Generation for Blackwell", sections "What a
+// Blackwell GEMM is" and "Writing a kernel"), 256 threads per CTA:
+//   warp 0     TMA producer: fills the stage ring with tiles of B and A.
+//   warp 1     MMA issuer (the pair leader's, for pair MMAs): one thread
+//              issues tcgen05.mma into a TMEM accumulator and frees stages
+//              with tcgen05.commit. Warp 1 also owns the TMEM allocation.
+//   warps 2-3  idle.
+//   warps 4-7  epilogue: TMEM → registers → C (direct stores, or a shared-
+//              memory staging tile written out by TMA store / reduce-add).
+// Hand-offs are mbarrier pipes: stage full / stage empty between producer and
+// MMA, accumulator full / accumulator empty between MMA and epilogue.
+//
+// Operand orientation is "SwapAB" (same page, section "Inside the kernels"):
+// the tile of B (rows = columns of C) is the MMA's A operand and the tile of A
+// (rows = rows of C) is its B operand. The accumulator is the C block
+// transposed: TMEM lane = column of C, TMEM column = row of C, so one warp's
+// tcgen05.ld row of 32 lanes is 32 consecutive floats of one row of C.
+//
+// With CG == 2 one MMA of M = 256 spans the two CTAs of a cluster pair: each
+// CTA holds 128 rows of the MMA's A operand (128·REPS columns of C) and half
+// of its B operand (BN/2 rows of C); each CTA's TMEM holds its 128 lanes of
+// the accumulator for all BN rows of C. The leader (cluster rank 0) issues.
+//
+// Every wait is bounded: after kWaitTimeoutNs the waiting role records the
+// site in the device status word, raises the CTA's abort flag, and returns;
+// the CTA then tears down normally (TMEM freed) and exits.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sm103/ptx.cuh"
+#include "sm103/umma_desc.h"
+#include "wgemm_plan.h"
+
+namespace wg {
+
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr int kThreads = 256;
+constexpr int kBK = 64;  // K per stage: one 128-byte swizzle row of fp16
+
+enum EpilogueMode : int { kEpiDirect = 0, kEpiTma = 1 };
+
+// Device status word (one per device, written by the first failing wait).
+struct DeviceStatus {
+  int32_t code;    // 0 = fine, else a negative WGEMM_ERR_* value
+  int32_t block;
+  int32_t warp;
+  int32_t site;    // role · 16 + barrier kind
+  int32_t parity;
+  int32_t pad[3];
+};
+
+enum WaitSite : int32_t {
+  kSiteProducerEmpty = 0x01,
+  kSiteProducerTail = 0x02,
+  kSiteMmaFull = 0x11,
+  kSiteMmaAccEmpty = 0x12,
+  kSiteMmaDrain = 0x13,
+  kSiteEpiAccFull = 0x21,
+  kSiteEpiFlagOwner = 0x22,
+  kSiteEpiFlagZero = 0x23,
+  kSiteEpiSync = 0x24,
+};
+
+struct KParams {
+  CUtensorMap tmA;  // A (M×K fp16): the MMA's B operand, box {64, BN/CG}
+  CUtensorMap tmB;  // B (N×K fp16): the MMA's A operand, box {64, 128·REPS}
+  CUtensorMap tmC;  // C (M×N fp32): box {32, 32}, for the TMA epilogue
+  Plan plan;
+  float* C;
+  int64_t ldc;
+  uint32_t* flags;  // split-K / stream-K flags (monotone epochs)
+  uint32_t epoch;
+  int32_t pad_;
+  DeviceStatus* status;
+};
+
+constexpr uint32_t pow2_at_least_32(uint32_t x) {
+  uint32_t p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+template <int CG_, int REPS_, int BN_, int STAGES_, int ACC_, int EPI_>
+struct Cfg {
+  static constexpr int CG = CG_;          // CTAs per MMA: 1, or 2 (pair)
+  static constexpr int REPS = REPS_;      // stacked MMA atoms per CTA (C columns 128·REPS)
+  static constexpr int BN = BN_;          // MMA N = C rows of a tile
+  static constexpr int STAGES = STAGES_;  // ring depth
+  static constexpr int ACC = ACC_;        // TMEM accumulators
+  static constexpr int EPI = EPI_;        // EpilogueMode
+
+  static constexpr int kCtaCols = 128 * REPS;       // C columns per CTA
+  static constexpr int kTileCols = kCtaCols * CG;   // C columns per worker tile
+  static constexpr int kTileRows = BN;              // C rows per worker tile
+  static constexpr int kArows = 128 * REPS;         // MMA-A rows (of B) per CTA stage
+  static constexpr int kBrows = BN / CG;            // MMA-B rows (of A) per CTA stage
+  static constexpr uint32_t kAbytes = kArows * 128;
+  static constexpr uint32_t kBbytes = kBrows * 128;
+  static constexpr uint32_t kStageBytes = kAbytes + kBbytes;
+  static constexpr uint32_t kAccCols = REPS * BN;   // TMEM columns per accumulator
+  static constexpr uint32_t kTmemCols = pow2_at_least_32(kAccCols * ACC);
+  static constexpr uint32_t kEpiSlotBytes = 32 * 32 * 4;  // one 32×32 fp32 staging tile
+  static constexpr uint32_t kEpiBytes = EPI == kEpiTma ? 4 * 2 * kEpiSlotBytes : 0;
+  static constexpr uint32_t kIdesc = umma_idesc_f16(128 * CG, BN);
+
+  // Shared-memory layout (offsets from a 1024-byte-aligned base).
+  static constexpr uint32_t kOffStages = 0;
+  static constexpr uint32_t kOffEpi = STAGES * kStageBytes;
+  static constexpr uint32_t kOffBars = kOffEpi + kEpiBytes;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 2;
+  static constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+
+  static_assert(CG == 1 || CG == 2, "CG");
+  static_assert(REPS == 1 || REPS == 2, "REPS");
+  static_assert(BN % (16 * CG) == 0 && BN >= 32 && BN <= 256, "MMA N");
+  static_assert(kBrows % 8 == 0, "operand rows in 8-row groups");
+  static_assert(kAccCols * ACC <= 512, "TMEM capacity");
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+};
+
+struct Shared {
+  uint32_t base;  // shared address of the aligned base
+  uint8_t* ptr;
+};
+
+__device__ __forceinline__ void record_error(DeviceStatus* st, int32_t code, int32_t site,
+                                             uint32_t parity) {
+  if (atomicCAS(&st->code, 0, code) == 0) {
+    st->block = (int32_t)blockIdx.x;
+    st->warp = (int32_t)(threadIdx.x / 32);
+    st->site = site;
+    st->parity = (int32_t)parity;
+    __threadfence();
+  }
+}
+
+// Bounded wait for the phase of parity `parity` of `bar`. False on timeout or
+// when another role of the CTA has aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
+                                         volatile uint32_t* abort_flag, DeviceStatus* st,
+                                         int32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        *abort_flag = 1;
+        record_error(st, -5, site, parity);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait until the flag word has reached `epoch` (monotone, wrap-safe).
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch,
+                                          volatile uint32_t* abort_flag, DeviceStatus* st,
+                                          int32_t site) {
+  if ((int32_t)(ld_acquire_gpu(flag) - epoch) >= 0) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(64);
+    if ((int32_t)(ld_acquire_gpu(flag) - epoch) >= 0) return true;
+    if ((n & 63) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        *abort_flag = 1;
+        record_error(st, -5, site, epoch);
+        return false;
+      }
+    }
+  }
+}
+
+template <class K>
+struct Kernel {
+  // Barrier addresses.
+  __device__ static uint32_t bar_full(uint32_t base, int s) { return base + K::kOffBars + 8 * s; }
+  __device__ static uint32_t bar_empty(uint32_t base, int s) {
+    return base + K::kOffBars + 8 * (K::STAGES + s);
+  }
+  __device__ static uint32_t bar_accf(uint32_t base, int a) {
+    return base + K::kOffBars + 8 * (2 * K::STAGES + a);
+  }
+  __device__ static uint32_t bar_acce(uint32_t base, int a) {
+    return base + K::kOffBars + 8 * (2 * K::STAGES + K::ACC + a);
+  }
+  __device__ static uint32_t bar_drain(uint32_t base) {
+    return base + K::kOffBars + 8 * (2 * K::STAGES + 2 * K::ACC);
+  }
+  // Rendezvous of the four epilogue warps (arrival count 4).
+  __device__ static uint32_t bar_epi(uint32_t base) {
+    return base + K::kOffBars + 8 * (2 * K::STAGES + 2 * K::ACC + 1);
+  }
+  __device__ static uint32_t stage_a(uint32_t base, int s) {
+    return base + K::kOffStages + s * K::kStageBytes;
+  }
+  __device__ static uint32_t stage_b(uint32_t base, int s) {
+    return stage_a(base, s) + K::kAbytes;
+  }
+
+  // ------------------------------------------------------------ producer
+  __device__ static void producer(const KParams& p, uint32_t base, uint32_t rank,
+                                  int32_t worker, volatile uint32_t* abort_flag) {
+    uint32_t s = 0, ph = 0;
+    bool ok = true;
+    for (int32_t i = 0; ok; ++i) {
+      Unit u;
+      if (!plan_unit(p.plan, worker, i, u)) break;
+      const int32_t b_row0 = u.tn * K::kTileCols + (int32_t)rank * K::kCtaCols;  // rows of B
+      const int32_t a_row0 = u.tm * K::kTileRows + (int32_t)rank * K::kBrows;    // rows of A
+      for (int32_t kb = u.kb_begin; kb < u.kb_end; ++kb) {
+        if (!wait_bar(bar_empty(base, s), ph ^ 1, abort_flag, p.status, kSiteProducerEmpty)) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = bar_full(base, s);
+        if constexpr (K::CG == 1) {
+          mbar_arrive_expect_tx(full, K::kStageBytes);
+          tma_load_2d(stage_a(base, s), &p.tmB, full, kb * kBK, b_row0);
+          tma_load_2d(stage_b(base, s), &p.tmA, full, kb * kBK, a_row0);
+        } else {
+          if (rank == 0) mbar_arrive_expect_tx(full, 2 * K::kStageBytes);
+          const uint32_t full_leader = mapa_shared(full, 0);
+          tma_load_2d_pair(stage_a(base, s), &p.tmB, full_leader, kb * kBK, b_row0);
+          tma_load_2d_pair(stage_b(base, s), &p.tmA, full_leader, kb * kBK, a_row0);
+        }
+        if (++s == (uint32_t)K::STAGES) { s = 0; ph ^= 1; }
+      }
+    }
+    // Tail: wait until the MMA has released every stage this CTA filled, so
+    // that no commit aimed at this CTA's barriers is still in flight at exit.
+    if (ok) {
+      for (int j = 0; j < K::STAGES; ++j) {
+        if (!wait_bar(bar_empty(base, s), ph ^ 1, abort_flag, p.status, kSiteProducerTail)) break;
+        if (++s == (uint32_t)K::STAGES) { s = 0; ph ^= 1; }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ MMA issuer
+  __device__ static void mma(const KParams& p, uint32_t base, uint32_t tmem, int32_t worker,
+                             volatile uint32_t* abort_flag) {
+    uint32_t s = 0, ph = 0, ab = 0, aph = 0;
+    bool ok = true;
+    for (int32_t i = 0; ok; ++i) {
+      Unit u;
+      if (!plan_unit(p.plan, worker, i, u)) break;
+      if (!wait_bar(bar_acce(base, ab), aph ^ 1, abort_flag, p.status, kSiteMmaAccEmpty)) {
+        ok = false;
+        break;
+      }
+      tcgen05_fence_after();
+      const uint32_t d = tmem + ab * K::kAccCols;
+      for (int32_t kb = u.kb_begin; kb < u.kb_end; ++kb) {
+        if (!wait_bar(bar_full(base, s), ph, abort_flag, p.status, kSiteMmaFull)) {
+          ok = false;
+          break;
+        }
+        tcgen05_fence_after();
+        const uint32_t sa = stage_a(base, s), sb = stage_b(base, s);
+#pragma unroll
+        for (int r = 0; r < K::REPS; ++r) {
+#pragma unroll
+          for (int j = 0; j < kBK / 16; ++j) {
+            const uint64_t adesc = umma_smem_desc_sw128(sa + r * 128 * 128 + j * 32);
+            const uint64_t bdesc = umma_smem_desc_sw128(sb + j * 32);
+            umma_f16<K::CG>(d + r * K::BN, adesc, bdesc, K::kIdesc,
+                            (kb > u.kb_begin || j > 0) ? 1u : 0u);
+          }
+        }
+        if constexpr (K::CG == 1) umma_commit(bar_empty(base, s));
+        else umma_commit_pair_multicast(bar_empty(base, s), 0x3);
+        if (++s == (uint32_t)K::STAGES) { s = 0; ph ^= 1; }
+      }
+      if (!ok) break;
+      if constexpr (K::CG == 1) umma_commit(bar_accf(base, ab));
+      else umma_commit_pair_multicast(bar_accf(base, ab), 0x3);
+      if (++ab == (uint32_t)K::ACC) { ab = 0; aph ^= 1; }
+    }
+    if (!ok) {
+      // Let the MMAs already issued finish before TMEM is freed.
+      if constexpr (K::CG == 1) umma_commit(bar_drain(base));
+      else umma_commit_pair_multicast(bar_drain(base), 0x3);
+      wait_bar(bar_drain(base), 0, abort_flag, p.status, kSiteMmaDrain);
+    }
+  }
+
+  // Bounded rendezvous of the four epilogue warps: every lane's earlier
+  // memory operations happen before every lane's later ones.
+  __device__ static bool epi_sync(uint32_t base, uint32_t& phase, volatile uint32_t* abort_flag,
+                                  DeviceStatus* st) {
+    __syncwarp();
+    if (lane_id() == 0) mbar_arrive(bar_epi(base));
+    const bool ok = wait_bar(bar_epi(base), phase, abort_flag, st, kSiteEpiSync);
+    phase ^= 1;
+    __syncwarp();
+    return ok;
+  }
+
+  // ------------------------------------------------------------ epilogue
+  // 128 threads (warps 4..7); warp q = warp % 4 reads TMEM lanes 32q..32q+31.
+  __device__ static void epilogue(const KParams& p, uint32_t base, uint8_t* smem, uint32_t tmem,
+                                  uint32_t rank, int32_t worker, volatile uint32_t* abort_flag) {
+    const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t q = warp & 3;
+    const int32_t M = p.plan.M, N = p.plan.N;
+    const int64_t ldc = p.ldc;
+    bool ok = true;
+    uint32_t sync_phase = 0;
+
+    if constexpr (K::EPI == kEpiTma) {
+      if (p.plan.mode == kSplitK) ok = zero_slices(p, base, rank, worker, sync_phase, abort_flag);
+    }
+
+    uint32_t ab = 0, aph = 0, slot = 0;
+    const uint32_t stage_base = base + K::kOffEpi + q * 2 * K::kEpiSlotBytes;
+    for (int32_t i = 0; ok; ++i) {
+      Unit u;
+      if (!plan_unit(p.plan, worker, i, u)) break;
+      if (!wait_bar(bar_accf(base, ab), aph, abort_flag, p.status, kSiteEpiAccFull)) {
+        ok = false;
+        break;
+      }
+      __syncwarp();
+      tcgen05_fence_after();
+      const int32_t col_cta = u.tn * K::kTileCols + (int32_t)rank * K::kCtaCols;
+      const int32_t row0 = u.tm * K::kTileRows;
+      const bool add = u.kind == kUnitAddAfterOwner || u.kind == kUnitAddAfterZero;
+      if constexpr (K::EPI == kEpiTma) {
+        if (add && lane == 0) {
+          if (u.kind == kUnitAddAfterOwner) {
+            ok = wait_flag(p.flags + (u.tile * K::CG + rank), p.epoch, abort_flag, p.status,
+                           kSiteEpiFlagOwner);
+          } else {
+            for (int32_t s = 0; s < p.plan.splits && ok; ++s)
+              ok = wait_flag(p.flags + ((u.tile * K::CG + rank) * p.plan.splits + s), p.epoch,
+                             abort_flag, p.status, kSiteEpiFlagZero);
+          }
+          // The flag's acquire covers generic writes; order them before the
+          // async-proxy reduce-add that follows.
+          fence_proxy_async_global();
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      constexpr int kChunks = K::BN / 32;
+#pragma unroll 1
+      for (int r = 0; r < K::REPS; ++r) {
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+          uint32_t v[32];
+          const uint32_t taddr = tmem + ((q * 32u) << 16) + ab * K::kAccCols + r * K::BN + c * 32;
+          tmem_ld_32x32b_x32(taddr, v);
+          tmem_ld_wait();
+          if (r == K::REPS - 1 && c == kChunks - 1) {
+            // Accumulator fully read: hand it back to the MMA warp.
+            tcgen05_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (K::CG == 1) mbar_arrive(bar_acce(base, ab));
+              else mbar_arrive_cluster(mapa_shared(bar_acce(base, ab), 0));
+            }
+          }
+          const int32_t col_warp = col_cta + r * 128 + (int32_t)q * 32;
+          const int32_t row_c = row0 + c * 32;
+          if constexpr (K::EPI == kEpiDirect) {
+            const int32_t col = col_warp + (int32_t)lane;
+            if (col < N) {
+              float* dst = p.C + (int64_t)row_c * ldc + col;
+              if (row_c + 32 <= M) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) dst[e * ldc] = __uint_as_float(v[e]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  if (row_c + e < M) dst[e * ldc] = __uint_as_float(v[e]);
+              }
+            }
+          } else {
+            // Stage the 32 rows × 32 columns block row-major, then one lane
+            // writes it out with a TMA store (or reduce-add); TMA clips the
+            // parts outside M × N.
+            const uint32_t sbuf = stage_base + slot * K::kEpiSlotBytes;
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            float* sp = reinterpret_cast<float*>(smem + (sbuf - base));
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sp[e * 32 + lane] = __uint_as_float(v[e]);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              if (add) tma_reduce_add_2d(&p.tmC, sbuf, col_warp, row_c);
+              else tma_store_2d(&p.tmC, sbuf, col_warp, row_c);
+              bulk_commit_group();
+            }
+            slot ^= 1;
+          }
+        }
+      }
+      if constexpr (K::EPI == kEpiTma) {
+        if (u.kind == kUnitStoreRaise) {
+          // Owner of the tile's first k-block: make the stores complete and
+          // visible, then raise the flag for the CTAs that add to this tile.
+          if (lane == 0) {
+            bulk_wait_group<0>();
+            fence_proxy_async_global();
+          }
+          if (!epi_sync(base, sync_phase, abort_flag, p.status)) { ok = false; break; }
+          if (threadIdx.x == 128) {
+            fence_acq_rel_gpu();
+            st_release_gpu(p.flags + (u.tile * K::CG + rank), p.epoch);
+          }
+        }
+      }
+      if (++ab == (uint32_t)K::ACC) { ab = 0; aph ^= 1; }
+    }
+    if constexpr (K::EPI == kEpiTma) {
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
+    }
+  }
+
+  // Split-K: before any unit of this worker runs, zero this CTA's share of
+  // every tile slice it owns and raise the slice's flag.
+  __device__ static bool zero_slices(const KParams& p, uint32_t base, uint32_t rank,
+                                     int32_t worker, uint32_t& sync_phase,
+                                     volatile uint32_t* abort_flag) {
+    const int32_t M = p.plan.M, N = p.plan.N;
+    const int64_t ldc = p.ldc;
+    const int32_t t = (int32_t)threadIdx.x - 128;  // 0..127
+    for (int32_t i = 0;; ++i) {
+      Unit u;
+      if (!plan_unit(p.plan, worker, i, u)) break;
+      int32_t r0, r1;
+      plan_zero_rows(K::kTileRows, p.plan.splits, u.split, r0, r1);
+      const int32_t row_begin = u.tm * K::kTileRows + r0;
+      int32_t row_end = u.tm * K::kTileRows + r1;
+      if (row_end > M) row_end = M;
+      const int32_t col_begin = u.tn * K::kTileCols + (int32_t)rank * K::kCtaCols;
+      int32_t col_end = col_begin + K::kCtaCols;
+      if (col_end > N) col_end = N;
+      if (row_begin >= row_end || col_begin >= col_end) continue;
+      const int32_t ncols = col_end - col_begin;
+      const int32_t nvec = ncols / 4;  // ldc % 4 == 0 and C is 16-byte aligned
+      for (int32_t r = row_begin; r < row_end; ++r) {
+        float* row = p.C + (int64_t)r * ldc + col_begin;
+        for (int32_t v = t; v < nvec; v += 128)
+          reinterpret_cast<float4*>(row)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int32_t c = nvec * 4 + t; c < ncols; c += 128) row[c] = 0.f;
+      }
+    }
+    fence_proxy_async_global();
+    if (!epi_sync(base, sync_phase, abort_flag, p.status)) return false;
+    if (t == 0) {
+      fence_acq_rel_gpu();
+      for (int32_t i = 0;; ++i) {
+        Unit u;
+        if (!plan_unit(p.plan, worker, i, u)) break;
+        st_release_gpu(p.flags + ((u.tile * K::CG + rank) * p.plan.splits + u.split), p.epoch);
+      }
+    }
+    return true;
+  }
+};
+
+template <class K>
+__global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constant__ KParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t warp = threadIdx.x / 32;
+  const uint32_t rank = K::CG == 2 ? (cluster_ctarank() & 1u) : 0u;
+  const int32_t worker = (int32_t)(blockIdx.x / K::CG);
+
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + K::kOffMisc);
+  volatile uint32_t* tmem_slot = misc;
+  volatile uint32_t* abort_flag = misc + 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < K::STAGES; ++s) {
+      mbar_init(Kernel<K>::bar_full(base, s), 1);
+      mbar_init(Kernel<K>::bar_empty(base, s), 1);
+    }
+    for (int a = 0; a < K::ACC; ++a) {
+      mbar_init(Kernel<K>::bar_accf(base, a), 1);
+      mbar_init(Kernel<K>::bar_acce(base, a), 4 * K::CG);
+    }
+    mbar_init(Kernel<K>::bar_drain(base), 1);
+    mbar_init(Kernel<K>::bar_epi(base), 4);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane_id() == 0) {
+    prefetch_tensormap(&p.tmA);
+    prefetch_tensormap(&p.tmB);
+    if (K::EPI == kEpiTma) prefetch_tensormap(&p.tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc<K::CG>(smem_addr(misc), K::kTmemCols);
+    tmem_relinquish<K::CG>();
+  }
+  tcgen05_fence_before();
+  if constexpr (K::CG == 2) cluster_sync();
+  else __syncthreads();
+  tcgen05_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (elect_one()) Kernel<K>::producer(p, base, rank, worker, abort_flag);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (rank == 0) {
+      if (elect_one()) Kernel<K>::mma(p, base, tmem, worker, abort_flag);
+      __syncwarp();
+    }
+  } else if (warp >= 4) {
+    Kernel<K>::epilogue(p, base, smem, tmem, rank, worker, abort_flag);
+  }
+
+  tcgen05_fence_before();
+  if constexpr (K::CG == 2) cluster_sync();
+  else __syncthreads();
+  if (warp == 1) {
+    tcgen05_fence_after();
+    tmem_dealloc<K::CG>(tmem, K::kTmemCols);
+  }
+}
+
+// K == 0: C := 0 (the empty sum).
+__global__ void wgemm_zero_kernel(float* C, int32_t M, int32_t N, int64_t ldc);
+
+}  // namespace wg

@@ -29,6 +29,9 @@ workloads here use uniform[−1, 1] fp16 plus a {−2..2} integer copy.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+import os
+
 import numpy as np
 
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -99,10 +102,18 @@ def matrix(rows: int, cols: int, seed: int, tensor_id: int, kind: str = "uniform
         return out
     key = stream_key(seed, tensor_id)
     rows_per_chunk = max(1, chunk_elems // cols)
-    for r0 in range(0, rows, rows_per_chunk):
+
+    def fill(r0: int) -> None:
         r1 = min(rows, r0 + rows_per_chunk)
         h = hash_stream(key, r0 * cols, (r1 - r0) * cols)
         out[r0:r1, :cols] = _values(h, kind).reshape(r1 - r0, cols)
+
+    starts = range(0, rows, rows_per_chunk)
+    if len(starts) == 1:
+        fill(0)
+    else:  # chunks are independent; numpy releases the GIL inside them
+        with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, starts))
     return out
 
 

@@ -1,0 +1,200 @@
+"""Python binding of libwgemm.so (ctypes): argument marshalling only.
+
+Every name mirrors a C entry point declared in include/wgemm.h. The GEMM runs
+entirely in the library's CUDA kernels; there is no fallback path: if the
+library is not built, or the GPU is not an sm_103 part, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+WGEMM_OK = 0
+STATUS_NAMES = {
+    0: "WGEMM_OK", -1: "WGEMM_ERR_INVALID_ARG", -2: "WGEMM_ERR_ALIGNMENT", -3: "WGEMM_ERR_LAUNCH",
+    -4: "WGEMM_ERR_NO_DEVICE", -5: "WGEMM_ERR_DEVICE_TIMEOUT", -6: "WGEMM_ERR_CONFIG",
+    -7: "WGEMM_ERR_WORKSPACE",
+}
+MODE_DATA_PARALLEL, MODE_SPLIT_K, MODE_STREAM_K = 0, 1, 2
+
+
+class WgemmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)} ({status_string(code)})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libwgemm.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "dense_fp16_gemm_02_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        i, p, u32, u64 = ctypes.c_int, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64
+        lib.wgemm_f16f32.argtypes = [p, p, p, i, i, i, i, i, i, p]
+        lib.wgemm_f16f32.restype = i
+        lib.wgemm_f16f32_config.argtypes = [p, p, p, i, i, i, i, i, i, i, i, i, p]
+        lib.wgemm_f16f32_config.restype = i
+        lib.wgemm_num_configs.argtypes = []
+        lib.wgemm_num_configs.restype = i
+        lib.wgemm_config_name.argtypes = [i]
+        lib.wgemm_config_name.restype = ctypes.c_char_p
+        lib.wgemm_select.argtypes = [i, i, i, ctypes.POINTER(i), ctypes.POINTER(i),
+                                     ctypes.POINTER(i)]
+        lib.wgemm_select.restype = i
+        lib.wgemm_check.argtypes = [p]
+        lib.wgemm_check.restype = i
+        lib.wgemm_last_device_error.argtypes = [ctypes.POINTER(i)] * 4
+        lib.wgemm_last_device_error.restype = i
+        lib.wgemm_status_string.argtypes = [i]
+        lib.wgemm_status_string.restype = ctypes.c_char_p
+        lib.wgemm_workspace_bytes.argtypes = []
+        lib.wgemm_workspace_bytes.restype = ctypes.c_size_t
+        lib.wgemm_release_workspace.argtypes = []
+        lib.wgemm_release_workspace.restype = i
+        lib.wgemm_debug_smem_desc.argtypes = [u32]
+        lib.wgemm_debug_smem_desc.restype = u64
+        lib.wgemm_debug_idesc.argtypes = [i, i]
+        lib.wgemm_debug_idesc.restype = u32
+        lib.wgemm_debug_sw128_offset.argtypes = [u32, u32]
+        lib.wgemm_debug_sw128_offset.restype = u32
+        lib.wgemm_debug_plan.argtypes = [i, i, i, i, i, i, i, p, i, ctypes.POINTER(i),
+                                         ctypes.POINTER(i)]
+        lib.wgemm_debug_plan.restype = i
+        _lib = lib
+        return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/wgemm.h declares."""
+    hdr = os.path.join(os.path.dirname(_build.HERE), "include", "wgemm.h")
+    text = open(hdr).read()
+    return sorted(set(re.findall(r"^\s*[\w\s\*]*?\b(wgemm_\w+)\s*\(", text, re.M)))
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().wgemm_status_string(code).decode()
+    except RuntimeError:
+        return STATUS_NAMES.get(code, "unknown")
+
+
+def num_configs() -> int:
+    return load().wgemm_num_configs()
+
+
+def config_name(config_id: int) -> str:
+    return load().wgemm_config_name(config_id).decode()
+
+
+def config_names() -> list[str]:
+    return [config_name(i) for i in range(num_configs())]
+
+
+def config_id(name: str) -> int:
+    names = config_names()
+    if name not in names:
+        raise KeyError(name)
+    return names.index(name)
+
+
+def wgemm_f16f32(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                 stream: int | None) -> int:
+    """The raw C call on device pointers; returns the status code."""
+    return load().wgemm_f16f32(A, B, C, M, N, K, lda, ldb, ldc, stream)
+
+
+def wgemm_f16f32_config(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                        ldc: int, config: int, mode: int, splits: int,
+                        stream: int | None) -> int:
+    return load().wgemm_f16f32_config(A, B, C, M, N, K, lda, ldb, ldc, config, mode, splits,
+                                      stream)
+
+
+def wgemm_select(M: int, N: int, K: int) -> tuple[int, int, int]:
+    c, m, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = load().wgemm_select(M, N, K, ctypes.byref(c), ctypes.byref(m), ctypes.byref(s))
+    if rc != WGEMM_OK:
+        raise WgemmError(rc, "wgemm_select")
+    return c.value, m.value, s.value
+
+
+def wgemm_check(stream: int | None = None) -> int:
+    return load().wgemm_check(stream)
+
+
+def wgemm_last_device_error() -> dict:
+    vals = [ctypes.c_int() for _ in range(4)]
+    code = load().wgemm_last_device_error(*[ctypes.byref(v) for v in vals])
+    return {"code": code, "block": vals[0].value, "warp": vals[1].value,
+            "site": vals[2].value, "parity": vals[3].value}
+
+
+def wgemm_workspace_bytes() -> int:
+    return load().wgemm_workspace_bytes()
+
+
+def wgemm_release_workspace() -> int:
+    return load().wgemm_release_workspace()
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def gemm(A, B, C=None, *, config: int | str | None = None, mode: int = -1, splits: int = 1,
+         stream=None):
+    """C = A·Bᵀ for torch tensors: A (M×K fp16), B (N×K fp16), C (M×N fp32).
+
+    A and B may have a row stride larger than K (a column slice of a wider
+    tensor); their last dimension must be contiguous. C is allocated when not
+    given. The work is enqueued on `stream` (default: torch's current stream).
+    """
+    import torch
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("A and B must be float16")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError("A must be M×K and B N×K")
+    if A.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("A and B need a contiguous last dimension")
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    M, K = A.shape
+    N = B.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if C.dtype != torch.float32 or C.shape != (M, N) or C.stride(1) != 1:
+        raise ValueError("C must be an M×N float32 tensor with a contiguous last dimension")
+    lda, ldb, ldc = A.stride(0), B.stride(0), C.stride(0)
+    if M == 0 or N == 0:
+        return C
+    h = _stream_handle(stream)
+    if config is None:
+        rc = wgemm_f16f32(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, max(lda, K),
+                          max(ldb, K), ldc, h)
+    else:
+        cid = config_id(config) if isinstance(config, str) else int(config)
+        rc = wgemm_f16f32_config(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, max(lda, K),
+                                 max(ldb, K), ldc, cid, mode, splits, h)
+    if rc != WGEMM_OK:
+        raise WgemmError(rc, "wgemm_f16f32")
+    return C

@@ -1,0 +1,149 @@
+/*
+ * wgemm — dense GEMM C = A·Bᵀ for NVIDIA GB300 (sm_103a): fp16 A and B,
+ * fp32 accumulation, fp32 C.
+ *
+ * The operation is the one "SASS-Level Kernel Generation for Blackwell"
+ * measures (section "The numbers", Setup paragraph: fp16 inputs, fp32
+ * accumulation and output, C = A·Bᵀ), with its M × N × K shape convention
+ * (table of section "The numbers"):
+ *
+ *     C[i·ldc + j] = Σ_{k<K} A[i·lda + k] · B[j·ldb + k]
+ *     for 0 ≤ i < M, 0 ≤ j < N.
+ *
+ * A is M×K and B is N×K, both row-major (K contiguous); C is M×N row-major.
+ * C is overwritten (no alpha/beta). The sum is accumulated in fp32 on the
+ * tensor cores; its rounding order is unspecified.
+ *
+ * Memory. Every matrix pointer is a DEVICE pointer into the current CUDA
+ * device's memory, owned by the caller. The library never frees or keeps a
+ * caller pointer past the call's completion on `stream`.
+ *
+ * Asynchrony. Calls enqueue work on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream) and return without synchronising. Argument errors are
+ * reported before anything is enqueued. A kernel that fails at run time (a
+ * bounded wait that expired) records it in a per-device status word that
+ * wgemm_check() reads.
+ *
+ * No CPU fallback, no vendor BLAS: an unsupported argument is an error.
+ *
+ * Library state. The library keeps, per device: the kernel attributes and
+ * occupancy it queried, and, per (device, stream), a small flag workspace for
+ * the split-K and stream-K paths (allocated on first need with cudaMalloc,
+ * grown when needed, freed by wgemm_release_workspace()). Calls on different
+ * streams may run concurrently; the split-K and stream-K paths assume their
+ * kernel's CTAs are all resident at once, which holds when no other kernel
+ * shares the GPU.
+ */
+#ifndef WGEMM_H
+#define WGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the same struct tag as CUDA's runtime and driver headers). */
+typedef struct CUstream_st* wgemm_stream_t;
+
+/* An fp16 (IEEE binary16) value, passed as its bit pattern. */
+typedef uint16_t wgemm_f16_t;
+
+/* Status codes. */
+#define WGEMM_OK 0
+#define WGEMM_ERR_INVALID_ARG -1      /* M/N/K < 0, NULL with a non-empty operand, lda < K, ldb < K, ldc < N */
+#define WGEMM_ERR_ALIGNMENT -2        /* A, B, C not 16-byte aligned, lda or ldb not a multiple of 8, ldc not a multiple of 4 */
+#define WGEMM_ERR_LAUNCH -3           /* a CUDA call failed while preparing or launching */
+#define WGEMM_ERR_NO_DEVICE -4        /* no current device, or it is not compute capability 10.3 */
+#define WGEMM_ERR_DEVICE_TIMEOUT -5   /* a bounded wait inside a kernel expired (see wgemm_last_device_error) */
+#define WGEMM_ERR_CONFIG -6           /* the forced configuration id does not exist or cannot run this shape */
+#define WGEMM_ERR_WORKSPACE -7        /* the flag workspace could not be allocated */
+
+/*
+ * C = A·Bᵀ on `stream`.
+ *   A: M×K fp16, row stride lda elements (lda ≥ K, lda % 8 == 0, 16-byte aligned)
+ *   B: N×K fp16, row stride ldb elements (ldb ≥ K, ldb % 8 == 0, 16-byte aligned)
+ *   C: M×N fp32, row stride ldc elements (ldc ≥ N, ldc % 4 == 0, 16-byte aligned)
+ * M == 0 or N == 0: nothing to do, returns WGEMM_OK. K == 0: C := 0 (the empty
+ * sum). C must not overlap A or B. The kernel configuration (tile shape, pair
+ * MMA, depth, scheduler, split-K or stream-K) is chosen per shape from a
+ * measured table, else by a rule. Returns WGEMM_OK once the work is enqueued,
+ * else a negative WGEMM_ERR_* code (nothing enqueued).
+ */
+int wgemm_f16f32(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
+                 int M, int N, int K, int lda, int ldb, int ldc,
+                 wgemm_stream_t stream);
+
+/*
+ * As wgemm_f16f32, but with the kernel configuration `config_id`
+ * (0 ≤ config_id < wgemm_num_configs()) and the K-decomposition forced:
+ * mode 0 = data parallel, 1 = split-K into `splits` ways (splits ≥ 1),
+ * 2 = stream-K, -1 = what the configuration table picks. Used by the tests
+ * and the per-shape sweep. WGEMM_ERR_CONFIG if the combination cannot run.
+ */
+int wgemm_f16f32_config(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
+                        int M, int N, int K, int lda, int ldb, int ldc,
+                        int config_id, int mode, int splits,
+                        wgemm_stream_t stream);
+
+/* Number of compiled kernel configurations, and the name of one ("" if out of range). */
+int wgemm_num_configs(void);
+const char* wgemm_config_name(int config_id);
+
+/*
+ * The choice wgemm_f16f32 makes for a shape on the current device:
+ * writes the configuration id, mode and splits. Returns WGEMM_OK or an error.
+ */
+int wgemm_select(int M, int N, int K, int* config_id, int* mode, int* splits);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns WGEMM_OK, WGEMM_ERR_DEVICE_TIMEOUT, or WGEMM_ERR_LAUNCH if a
+ * CUDA error is pending.
+ */
+int wgemm_check(wgemm_stream_t stream);
+
+/*
+ * Details of the last device error wgemm_check saw on the current device:
+ * the block, the warp, the wait site (role·16 + barrier kind) and the phase
+ * parity it waited for. Any pointer may be NULL. Returns the error code.
+ */
+int wgemm_last_device_error(int* block, int* warp, int* site, int* parity);
+
+/* A short English description of a status code. Never NULL. */
+const char* wgemm_status_string(int status);
+
+/* Bytes of flag workspace currently held for the current device (all streams). */
+size_t wgemm_workspace_bytes(void);
+
+/* Frees the current device's flag workspaces after synchronising the device. */
+int wgemm_release_workspace(void);
+
+/*
+ * Host-side introspection, no GPU needed (used by the host tests).
+ *
+ * wgemm_debug_smem_desc: the 64-bit tcgen05 shared-memory descriptor the
+ * kernels build for a K-major fp16 operand tile with the 128-byte swizzle,
+ * starting at shared byte address `smem_addr`.
+ * wgemm_debug_idesc: the 32-bit instruction descriptor of a kind::f16 MMA of
+ * shape M×N×16 with an f32 accumulator.
+ * wgemm_debug_sw128_offset: byte offset of fp16 element (row, k) inside a
+ * 1024-byte-aligned 128-byte-swizzled K-major tile.
+ * wgemm_debug_plan: fills `out` (7 int32 per unit: tile, tm, tn, kb_begin,
+ * kb_end, kind, split) with every unit of the plan the library would run
+ * for this shape, configuration, mode and worker count, in worker-major
+ * order; returns the number of units (or a negative error), writing at most
+ * `max_units`. Also writes the tile shape (rows, cols) of the configuration.
+ */
+uint64_t wgemm_debug_smem_desc(uint32_t smem_addr);
+uint32_t wgemm_debug_idesc(int M, int N);
+uint32_t wgemm_debug_sw128_offset(uint32_t row, uint32_t k);
+int wgemm_debug_plan(int M, int N, int K, int config_id, int mode, int splits, int workers,
+                     int32_t* out, int max_units, int* tile_rows, int* tile_cols);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WGEMM_H */

@@ -1,0 +1,279 @@
+"""GPU parity: the CUDA path through the C-ABI against the CPU oracle.
+
+Acceptance (for C = A·Bᵀ, fp16 in, fp32 accumulation and output, "SASS-Level
+Kernel Generation for Blackwell", section "The numbers"):
+* integer-valued inputs in {-2..2}: exact. Every product is exact and every
+  partial sum is an integer of magnitude ≤ 4K ≤ 2^18 < 2^24, so any fp32
+  accumulation order, on the tensor cores or in L2 reduce-adds, is exact.
+  Compared as values (+0 == -0).
+* uniform[-1, 1] fp16 inputs: |C − C_ref| ≤ 2e-3·(|A|·|B|ᵀ)_ij + 1e-6 elementwise.
+
+Small cases run every configuration and every K-decomposition at sizes that
+span several tiles with ragged edges; the full-size cases of the workloads run
+the default per-shape choice (the launch the bench times) and are checked on
+sampled rows and columns the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
+
+pytestmark = pytest.mark.gpu
+
+RTOL, ATOL = 2e-3, 1e-6
+DP, SPLIT, STREAM = 0, 1, 2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    oracle.build_oracle()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    return wgemm.load()
+
+
+def upload(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(x).cuda()
+
+
+def run(A, B, K, config=None, mode=-1, splits=1, C=None):
+    """C = A[:, :K]·B[:, :K]ᵀ on the GPU; A, B numpy fp16 with ld ≥ K."""
+    dA, dB = upload(A), upload(B)
+    out = wgemm.gemm(dA[:, :K], dB[:, :K], C, config=config, mode=mode, splits=splits)
+    status = wgemm.wgemm_check(torch.cuda.current_stream().cuda_stream)
+    assert status == 0, (status, wgemm.wgemm_last_device_error())
+    return out
+
+
+def assert_exact(got: np.ndarray, ref: np.ndarray, what=""):
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{what}: {len(bad)} mismatches, first {bad[:5].tolist()}"
+
+
+def assert_tol(got: np.ndarray, ref: np.ndarray, ref_abs: np.ndarray, what=""):
+    err = np.abs(got - ref)
+    bound = RTOL * ref_abs + ATOL
+    ok = err <= bound
+    rel = float((err / np.maximum(np.abs(ref), 1e-30)).max()) if ref.size else 0.0
+    assert ok.all(), f"{what}: {(~ok).sum()} outside tolerance, max excess {(err - bound).max()}"
+    return rel
+
+
+def check_full(A, B, K, kind, what, **kw):
+    C = run(A, B, K, **kw).cpu().numpy().astype(np.float64)
+    if kind == "int":
+        assert_exact(C, oracle.gemm_f64(A, B, K=K), what)
+    else:
+        ref, ref_abs = oracle.gemm_f64(A, B, K=K, with_abs=True)
+        assert_tol(C, ref, ref_abs, what)
+
+
+ALL_CONFIGS = None
+
+
+def configs(suffix=""):
+    return [n for n in wgemm.config_names() if n.endswith(suffix)]
+
+
+# ---------------------------------------------------------------- every configuration
+
+
+@pytest.mark.parametrize("kind", ["int", "uniform"])
+@pytest.mark.parametrize("cfg", range(10))
+def test_every_config_ragged(cfg, kind):
+    names = wgemm.config_names()
+    if cfg >= len(names):
+        pytest.skip("fewer configurations compiled")
+    # 3 tile rows and 3 tile columns for the largest tiles, all edges ragged,
+    # K a non-multiple of the 64-wide k-block.
+    M, N, K = 600, 1100, 300
+    A, B = inputs.gemm_operands(M, N, K, seed=100 + cfg, kind=kind)
+    check_full(A, B, K, kind, f"{names[cfg]} {kind}", config=names[cfg], mode=DP)
+
+
+@pytest.mark.parametrize("splits", [2, 3, 7])
+def test_split_k_every_tma_config(splits):
+    M, N, K = 300, 700, 2000
+    for kind in ("int", "uniform"):
+        A, B = inputs.gemm_operands(M, N, K, seed=7 + splits, kind=kind)
+        for name in configs("_tma"):
+            check_full(A, B, K, kind, f"{name} split {splits} {kind}", config=name, mode=SPLIT,
+                       splits=splits)
+
+
+def test_stream_k_every_tma_config():
+    M, N, K = 520, 1100, 3000
+    for kind in ("int", "uniform"):
+        A, B = inputs.gemm_operands(M, N, K, seed=21, kind=kind)
+        for name in configs("_tma"):
+            check_full(A, B, K, kind, f"{name} stream-K {kind}", config=name, mode=STREAM)
+
+
+def test_split_and_stream_equal_data_parallel_on_integers():
+    # Exact arithmetic: every decomposition of K gives the same C, bit for bit.
+    M, N, K = 256, 512, 4096
+    A, B = inputs.gemm_operands(M, N, K, seed=5, kind="int")
+    name = "g2_512x256_s4_a1_tma"
+    base = run(A, B, K, config=name, mode=DP).cpu().numpy()
+    for mode, s in ((SPLIT, 2), (SPLIT, 9), (STREAM, 1)):
+        other = run(A, B, K, config=name, mode=mode, splits=s).cpu().numpy()
+        assert np.array_equal(base, other), (mode, s)
+
+
+def test_repeated_calls_share_flag_workspace():
+    # Monotone epochs: flags are never reset between calls; alternate modes and
+    # shapes on one stream and check every result.
+    shapes = [(300, 700, 2000, SPLIT, 3), (520, 1100, 3000, STREAM, 1),
+              (256, 512, 4096, SPLIT, 9), (300, 700, 2000, STREAM, 1)]
+    for rep in range(3):
+        for M, N, K, mode, s in shapes:
+            A, B = inputs.gemm_operands(M, N, K, seed=rep, kind="int")
+            C = run(A, B, K, config="g2_512x128_s4_a2_tma", mode=mode, splits=s)
+            assert_exact(C.cpu().numpy().astype(np.float64), oracle.gemm_f64(A, B), "repeat")
+    assert wgemm.wgemm_workspace_bytes() > 0
+
+
+# ---------------------------------------------------------------- edge cases
+
+
+def test_k_zero_writes_zeros():
+    C = torch.full((37, 53), float("nan"), device="cuda")
+    A = torch.zeros((37, 8), dtype=torch.float16, device="cuda")
+    B = torch.zeros((53, 8), dtype=torch.float16, device="cuda")
+    wgemm.gemm(A[:, :0], B[:, :0], C)
+    assert wgemm.wgemm_check(torch.cuda.current_stream().cuda_stream) == 0
+    assert torch.all(C == 0)
+
+
+def test_empty_m_or_n_is_noop():
+    A = torch.ones((0, 64), dtype=torch.float16, device="cuda")
+    B = torch.ones((5, 64), dtype=torch.float16, device="cuda")
+    C = wgemm.gemm(A, B)
+    assert C.shape == (0, 5)
+    rc = wgemm.wgemm_f16f32(0, 0, 0, 4, 0, 64, 64, 64, 4, None)
+    assert rc == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 300, 7), (300, 1, 64), (17, 33, 65),
+                                   (128, 256, 64), (256, 512, 128)])
+def test_tiny_and_exact_tile_shapes(M, N, K):
+    lda = ldb = ((K + 7) // 8) * 8
+    for name in ("g1_128x64_s8_a2_direct", "g1_128x256_s4_a2_tma", "g2_256x256_s6_a2_tma",
+                 "g2_512x256_s4_a1_tma", None):
+        A, B = inputs.gemm_operands(M, N, K, seed=3, kind="int", lda=lda, ldb=ldb)
+        check_full(A, B, K, "int", f"{name} {M}x{N}x{K}", config=name,
+                   mode=DP if name else -1)
+
+
+def test_padding_past_k_never_read():
+    # lda, ldb > K with fp16 NaN in the padding: TMA must stop at K.
+    M, N, K = 200, 300, 100
+    A, B = inputs.gemm_operands(M, N, K, seed=9, kind="uniform", lda=136, ldb=112, pad="nan")
+    for name in ("g1_128x256_s4_a2_tma", "g2_256x256_s6_a2_direct", "g2_512x128_s4_a2_tma"):
+        check_full(A, B, K, "uniform", name, config=name, mode=DP)
+
+
+def test_ldc_padding_untouched():
+    M, N, K = 130, 260, 96
+    A, B = inputs.gemm_operands(M, N, K, seed=4, kind="int")
+    for name in ("g1_128x256_s4_a2_direct", "g2_256x256_s6_a2_tma"):
+        Cfull = torch.full((M, 300), -7.0, device="cuda")
+        run(A, B, K, config=name, mode=DP, C=Cfull[:, :N])
+        got = Cfull.cpu().numpy()
+        assert np.all(got[:, N:] == -7.0)
+        assert_exact(got[:, :N].astype(np.float64), oracle.gemm_f64(A, B), name)
+
+
+def test_side_stream():
+    M, N, K = 300, 400, 500
+    A, B = inputs.gemm_operands(M, N, K, seed=12, kind="int")
+    s = torch.cuda.Stream()
+    dA, dB = upload(A), upload(B)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        C = wgemm.gemm(dA, dB)
+        assert wgemm.wgemm_check(s.cuda_stream) == 0
+    assert_exact(C.cpu().numpy().astype(np.float64), oracle.gemm_f64(A, B), "side stream")
+
+
+def test_argument_errors_on_gpu():
+    A = torch.zeros((64, 64), dtype=torch.float16, device="cuda")
+    C = torch.zeros((64, 64), dtype=torch.float32, device="cuda")
+    assert wgemm.wgemm_f16f32(A.data_ptr() + 2, A.data_ptr(), C.data_ptr(), 8, 8, 8, 64, 64, 64,
+                              None) == -2
+    assert wgemm.wgemm_f16f32(A.data_ptr(), A.data_ptr(), C.data_ptr(), 8, 8, 8, 4, 64, 64,
+                              None) == -1
+    assert wgemm.wgemm_f16f32_config(A.data_ptr(), A.data_ptr(), C.data_ptr(), 8, 8, 8, 64, 64,
+                                     64, 999, 0, 1, None) == -6
+    direct = wgemm.config_id("g2_256x256_s6_a2_direct")
+    assert wgemm.wgemm_f16f32_config(A.data_ptr(), A.data_ptr(), C.data_ptr(), 64, 64, 640, 64,
+                                     64, 64, direct, SPLIT, 2, None) == -6
+
+
+# ---------------------------------------------------------------- the workloads at full size
+
+WORKLOADS = [
+    # (M, N, K, kinds, sampled rows/cols or None for the full matrix)
+    (1024, 1024, 1024, ("int", "uniform"), None),
+    (1536, 1536, 1536, ("uniform",), 64),
+    (2048, 2048, 2048, ("uniform",), 64),
+    (3072, 1280, 2048, ("uniform",), 64),
+    (4096, 4096, 1024, ("uniform",), 64),
+    (4096, 4096, 4096, ("uniform",), 64),
+    (8192, 2048, 4096, ("uniform",), 64),
+    (1024, 1024, 65536, ("int", "uniform"), 32),
+    (2048, 2048, 16384, ("int", "uniform"), 32),
+]
+
+
+def check_sampled(A, B, C: torch.Tensor, M, N, K, kind, n_sample, seed, what):
+    rows = inputs.sample_indices(M, n_sample, seed, 2)
+    cols = inputs.sample_indices(N, n_sample, seed, 3)
+    Ch = C.cpu().numpy().astype(np.float64)
+    # Full rows R (every column) and full columns J (every row).
+    for sel_rows, sel_cols, got in ((rows, None, Ch[rows, :]), (None, cols, Ch[:, cols])):
+        if kind == "int":
+            ref = oracle.gemm_f64_select(A, B, sel_rows, sel_cols)
+            assert_exact(got, ref, what)
+        else:
+            ref, ref_abs = oracle.gemm_f64_select(A, B, sel_rows, sel_cols, with_abs=True)
+            assert_tol(got, ref, ref_abs, what)
+
+
+@pytest.mark.parametrize("M,N,K,kinds,sample", WORKLOADS)
+def test_workload_default_path(M, N, K, kinds, sample):
+    for kind in kinds:
+        A, B = inputs.gemm_operands(M, N, K, seed=1000 + M + N + K, kind=kind)
+        C = run(A, B, K)
+        if sample is None:
+            got = C.cpu().numpy().astype(np.float64)
+            if kind == "int":
+                assert_exact(got, oracle.gemm_f64(A, B), f"{M}x{N}x{K} int")
+            else:
+                ref, ref_abs = oracle.gemm_f64(A, B, with_abs=True)
+                assert_tol(got, ref, ref_abs, f"{M}x{N}x{K}")
+        else:
+            check_sampled(A, B, C, M, N, K, kind, sample, 77, f"{M}x{N}x{K} {kind}")
+        del C
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n", [8192, 16384])
+def test_large_compute_bound_sampled(n):
+    # 256 sampled rows and 256 sampled columns: the full 256×256 block C[R, J],
+    # plus, at 8192, the full rows R.
+    A, B = inputs.gemm_operands(n, n, n, seed=2000 + n, kind="uniform")
+    C = run(A, B, n)
+    rows = inputs.sample_indices(n, 256, 5, 2)
+    cols = inputs.sample_indices(n, 256, 5, 3)
+    Ch = C.cpu().numpy()
+    ref, ref_abs = oracle.gemm_f64_select(A, B, rows, cols, with_abs=True)
+    assert_tol(Ch[np.ix_(rows, cols)].astype(np.float64), ref, ref_abs, f"{n}^3 block")
+    if n == 8192:
+        ref, ref_abs = oracle.gemm_f64_select(A, B, rows[:64], None, with_abs=True)
+        assert_tol(Ch[rows[:64], :].astype(np.float64), ref, ref_abs, f"{n}^3 rows")
+    del C
+    torch.cuda.empty_cache()

@@ -1,0 +1,199 @@
+"""Host model of the work decomposition (no GPU).
+
+For every configuration and mode the units the library would run must cover
+each (tile, k-block) of the problem exactly once; the split-K zero slices must
+cover every tile row exactly once; and the stream-K / split-K flag protocol,
+simulated worker by worker with each worker taking its units in order, must
+finish without a worker waiting forever ("SASS-Level Kernel Generation for
+Blackwell", paragraph "Stream-K and split-K, added in the L2").
+"""
+import ctypes
+from collections import defaultdict
+
+import numpy as np
+import pytest
+
+from dense_fp16_gemm_02_gb300 import build, wgemm
+
+KIND_STORE, KIND_RAISE, KIND_ADD_OWNER, KIND_ADD_ZERO = 0, 1, 2, 3
+DP, SPLIT, STREAM = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return wgemm.load()
+
+
+def plan(lib, M, N, K, cfg, mode, splits, workers):
+    tr, tc = ctypes.c_int(), ctypes.c_int()
+    n = lib.wgemm_debug_plan(M, N, K, cfg, mode, splits, workers, None, 0, ctypes.byref(tr),
+                             ctypes.byref(tc))
+    assert n >= 0, n
+    buf = np.zeros(7 * max(n, 1), dtype=np.int32)
+    n2 = lib.wgemm_debug_plan(M, N, K, cfg, mode, splits, workers, buf.ctypes.data, n,
+                              ctypes.byref(tr), ctypes.byref(tc))
+    assert n2 == n
+    return buf[:7 * n].reshape(n, 7), tr.value, tc.value
+
+
+
+
+SHAPES = [(1, 1, 1), (300, 520, 200), (1024, 1024, 1024), (1000, 3000, 65),
+          (2048, 2048, 16384), (1024, 1024, 65536), (4096, 4096, 1024), (257, 513, 4097)]
+
+
+def tile_grid(M, N, tr, tc):
+    return -(-M // tr), -(-N // tc)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("workers", [1, 7, 76, 152])
+def test_data_parallel_covers_each_tile_once(lib, M, N, K, workers):
+    for cfg in range(lib.wgemm_num_configs()):
+        units, tr, tc = plan(lib, M, N, K, cfg, DP, 1, workers)
+        tm, tn = tile_grid(M, N, tr, tc)
+        kb = -(-K // 64)
+        assert len(units) == tm * tn
+        seen = {(int(u[1]), int(u[2])) for u in units}
+        assert seen == {(i, j) for i in range(tm) for j in range(tn)}
+        assert np.all(units[:, 3] == 0) and np.all(units[:, 4] == kb)
+        assert np.all(units[:, 5] == KIND_STORE)
+
+
+def tma_configs(lib):
+    return [i for i, n in enumerate(wgemm.config_names()) if n.endswith("_tma")]
+
+
+def direct_configs(lib):
+    return [i for i, n in enumerate(wgemm.config_names()) if n.endswith("_direct")]
+
+
+def coverage(units, tm, tn, kb):
+    hits = defaultdict(int)
+    for u in units:
+        assert 0 <= u[1] < tm and 0 <= u[2] < tn and u[0] == u[0]
+        assert 0 <= u[3] < u[4] <= kb
+        for k in range(int(u[3]), int(u[4])):
+            hits[(int(u[1]), int(u[2]), k)] += 1
+    return hits
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("splits", [1, 2, 3, 9, 64])
+def test_split_k_covers_each_kblock_once(lib, M, N, K, splits):
+    for cfg in tma_configs(lib):
+        units, tr, tc = plan(lib, M, N, K, cfg, SPLIT, splits, 76)
+        tm, tn = tile_grid(M, N, tr, tc)
+        kb = -(-K // 64)
+        s_eff = min(splits, kb)
+        hits = coverage(units, tm, tn, kb)
+        assert len(hits) == tm * tn * kb and set(hits.values()) == {1}
+        assert np.all(units[:, 5] == KIND_ADD_ZERO)
+        sizes = units[:, 4] - units[:, 3]
+        assert sizes.max() - sizes.min() <= 1  # near-equal contiguous ranges
+        # Each tile's splits are 0..S-1 once each.
+        per_tile = defaultdict(list)
+        for u in units:
+            per_tile[int(u[0])].append(int(u[6]))
+        assert all(sorted(v) == list(range(s_eff)) for v in per_tile.values())
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("workers", [1, 5, 76, 300])
+def test_stream_k_covers_each_kblock_once(lib, M, N, K, workers):
+    for cfg in tma_configs(lib):
+        units, tr, tc = plan(lib, M, N, K, cfg, STREAM, 1, workers)
+        tm, tn = tile_grid(M, N, tr, tc)
+        kb = -(-K // 64)
+        hits = coverage(units, tm, tn, kb)
+        assert len(hits) == tm * tn * kb and set(hits.values()) == {1}
+        # Exactly one unit per tile starts at k-block 0, and it stores.
+        starts = defaultdict(int)
+        for u in units:
+            if u[3] == 0:
+                starts[int(u[0])] += 1
+                assert u[5] in (KIND_STORE, KIND_RAISE)
+            else:
+                assert u[5] == KIND_ADD_OWNER
+        assert len(starts) == tm * tn and set(starts.values()) == {1}
+
+
+
+
+def simulate_stream_k(per_worker):
+    """Each worker runs its units in order; an add-after-owner unit can finish
+    only after its tile's owner unit finished. Returns True if every worker
+    finishes (no deadlock)."""
+    pos = [0] * len(per_worker)
+    owner_done = set()
+    progress = True
+    while progress:
+        progress = False
+        for w, units in enumerate(per_worker):
+            while pos[w] < len(units):
+                u = units[pos[w]]
+                if u[5] == KIND_ADD_OWNER and int(u[0]) not in owner_done:
+                    break
+                if u[5] in (KIND_RAISE, KIND_STORE):
+                    owner_done.add(int(u[0]))
+                pos[w] += 1
+                progress = True
+    return all(p == len(u) for p, u in zip(pos, per_worker))
+
+
+def split_by_worker(lib, M, N, K, cfg, mode, splits, workers):
+    """Per-worker lists: ask the library for each single worker count prefix.
+    The worker-major listing is cut where the worker id changes, which we
+    recover from the data-independent rule: stream-K ranges are contiguous in
+    (tile, k) order and each worker walks its range downwards."""
+    units, tr, tc = plan(lib, M, N, K, cfg, mode, splits, workers)
+    kb = -(-K // 64)
+    lists, cur, last_key = [], [], None
+    for u in units:
+        key = int(u[0]) * kb + int(u[3])
+        # Within one worker the global iteration index strictly decreases.
+        if cur and key > last_key:
+            lists.append(cur)
+            cur = []
+        cur.append(u)
+        last_key = key
+    if cur:
+        lists.append(cur)
+    return lists
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 16384), (257, 513, 4097), (1024, 1024, 65536),
+                                   (300, 520, 200)])
+@pytest.mark.parametrize("workers", [3, 76, 74])
+def test_stream_k_protocol_finishes(lib, M, N, K, workers):
+    for cfg in tma_configs(lib):
+        lists = split_by_worker(lib, M, N, K, cfg, STREAM, 1, workers)
+        # A worker's first unit waits only when it is the worker's only unit
+        # (a range inside one tile); every owner unit is its worker's first.
+        for lst in lists:
+            assert lst[0][5] != KIND_ADD_OWNER or len(lst) == 1
+            assert all(u[5] != KIND_RAISE for u in lst[1:])
+        assert simulate_stream_k(lists)
+
+
+@pytest.mark.parametrize("M,N,K,S", [(1024, 1024, 65536, 9), (300, 520, 200, 3),
+                                     (257, 513, 4097, 5)])
+def test_split_k_zero_slices_partition_rows(lib, M, N, K, S):
+    # plan_zero_rows: the S slices of a tile's rows are disjoint and cover it.
+    for tile_rows in (64, 128, 256):
+        for s_eff in range(1, S + 1):
+            per = -(-tile_rows // s_eff)
+            covered = []
+            for s in range(s_eff):
+                r0, r1 = min(s * per, tile_rows), min((s + 1) * per, tile_rows)
+                covered += list(range(r0, r1))
+            assert covered == list(range(tile_rows))
+
+
+def test_direct_epilogue_configs_reject_split_modes(lib):
+    for cfg in direct_configs(lib):
+        n = lib.wgemm_debug_plan(1024, 1024, 4096, cfg, SPLIT, 4, 76, None, 0, None, None)
+        assert n == -6
+        n = lib.wgemm_debug_plan(1024, 1024, 4096, cfg, STREAM, 1, 76, None, 0, None, None)
+        assert n == -6
