@@ -187,7 +187,15 @@ struct Choice {
   int config, mode, splits;
 };
 
-Choice choose(int M, int N, int K, int workers_hint) {
+Choice choose(int M, int N, int K, int workers_hint, bool c_tma_ok) {
+  if (!c_tma_ok) {
+    // C rows not 16-byte aligned: no TMA on C, so a direct-store epilogue
+    // and no K decomposition.
+    const int64_t mn = (int64_t)M * N;
+    if (mn >= (int64_t)1536 * 1536)
+      return {find_config("g2_256x256_s6_a2_direct"), kDataParallel, 1};
+    return {find_config("g2_256x64_s10_a2_direct"), kDataParallel, 1};
+  }
   const int64_t mn = (int64_t)M * N;
   const int kblocks = (K + kBK - 1) / kBK;
   // Few output tiles and a long K: split K (tiles far fewer than workers) or
@@ -219,8 +227,13 @@ int check_args(const void* A, const void* B, const void* C, int M, int N, int K,
         (lda % 8) || (ldb % 8))
       return WGEMM_ERR_ALIGNMENT;
   }
-  if ((reinterpret_cast<uintptr_t>(C) & 15) || (ldc % 4)) return WGEMM_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(C) & 3) return WGEMM_ERR_ALIGNMENT;
   return WGEMM_OK;
+}
+
+// C can be written by TMA (16-byte aligned base and row stride).
+bool c_tma_ok(const void* C, int ldc) {
+  return !(reinterpret_cast<uintptr_t>(C) & 15) && !(ldc % 4);
 }
 
 // Fills the plan for a configuration; WGEMM_ERR_CONFIG if the mode cannot run.
@@ -299,18 +312,20 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
     return cudaGetLastError() == cudaSuccess ? WGEMM_OK : WGEMM_ERR_LAUNCH;
   }
   const auto& es = registry().entries;
+  const bool c_ok = c_tma_ok(C, ldc);
   if (config_id < 0) {
     // Workers of the pair configurations bound the split / stream-K choice.
     const int hint = st->sm_count / 2;
-    Choice c = choose(M, N, K, hint);
+    Choice c = choose(M, N, K, hint, c_ok);
     config_id = c.config;
     mode = c.mode;
     splits = c.splits;
   }
   if (config_id < 0 || config_id >= (int)es.size()) return WGEMM_ERR_CONFIG;
   const KernelEntry& e = *es[config_id];
+  if (e.epi == kEpiTma && !c_ok) return WGEMM_ERR_ALIGNMENT;
   if (mode < 0) {
-    Choice c = choose(M, N, K, st->sm_count / 2);
+    Choice c = choose(M, N, K, st->sm_count / 2, c_ok);
     mode = c.mode;
     splits = c.splits;
     if (mode != kDataParallel && e.epi != kEpiTma) mode = kDataParallel;
@@ -327,8 +342,9 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
                  (uint64_t)lda * 2, kBK, (uint32_t)brows_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&params.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)K, (uint64_t)N,
                  (uint64_t)ldb * 2, kBK, (uint32_t)rows_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&params.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, (uint64_t)N, (uint64_t)M,
-                 (uint64_t)ldc * 4, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+      (e.epi == kEpiTma &&
+       !encode_2d(&params.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, (uint64_t)N, (uint64_t)M,
+                  (uint64_t)ldc * 4, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE)))
     return WGEMM_ERR_LAUNCH;
   params.C = C;
   params.ldc = ldc;
@@ -389,7 +405,7 @@ int wgemm_select(int M, int N, int K, int* config_id, int* mode, int* splits) {
   DeviceState* st;
   const int rc = device_state(&dev, &st);
   if (rc != WGEMM_OK) return rc;
-  Choice c = choose(M, N, K, st->sm_count / 2);
+  Choice c = choose(M, N, K, st->sm_count / 2, true);
   if (config_id) *config_id = c.config;
   if (mode) *mode = c.mode;
   if (splits) *splits = c.splits;

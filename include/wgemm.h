@@ -53,7 +53,7 @@ typedef uint16_t wgemm_f16_t;
 /* Status codes. */
 #define WGEMM_OK 0
 #define WGEMM_ERR_INVALID_ARG -1      /* M/N/K < 0, NULL with a non-empty operand, lda < K, ldb < K, ldc < N */
-#define WGEMM_ERR_ALIGNMENT -2        /* A, B, C not 16-byte aligned, lda or ldb not a multiple of 8, ldc not a multiple of 4 */
+#define WGEMM_ERR_ALIGNMENT -2        /* A or B not 16-byte aligned, lda or ldb not a multiple of 8, C not 4-byte aligned, or a TMA-epilogue configuration forced on a C that is not 16-byte aligned with ldc % 4 == 0 */
 #define WGEMM_ERR_LAUNCH -3           /* a CUDA call failed while preparing or launching */
 #define WGEMM_ERR_NO_DEVICE -4        /* no current device, or it is not compute capability 10.3 */
 #define WGEMM_ERR_DEVICE_TIMEOUT -5   /* a bounded wait inside a kernel expired (see wgemm_last_device_error) */
@@ -64,7 +64,10 @@ typedef uint16_t wgemm_f16_t;
  * C = A·Bᵀ on `stream`.
  *   A: M×K fp16, row stride lda elements (lda ≥ K, lda % 8 == 0, 16-byte aligned)
  *   B: N×K fp16, row stride ldb elements (ldb ≥ K, ldb % 8 == 0, 16-byte aligned)
- *   C: M×N fp32, row stride ldc elements (ldc ≥ N, ldc % 4 == 0, 16-byte aligned)
+ *   C: M×N fp32, row stride ldc elements (ldc ≥ N, 4-byte aligned). When C is
+ *      16-byte aligned and ldc % 4 == 0 the epilogue may write C with TMA
+ *      stores or reduce-adds (needed by split-K and stream-K); otherwise a
+ *      configuration that stores from registers is chosen.
  * M == 0 or N == 0: nothing to do, returns WGEMM_OK. K == 0: C := 0 (the empty
  * sum). C must not overlap A or B. The kernel configuration (tile shape, pair
  * MMA, depth, scheduler, split-K or stream-K) is chosen per shape from a

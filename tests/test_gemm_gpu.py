@@ -35,6 +35,17 @@ def lib():
     return wgemm.load()
 
 
+def ceil8(k: int) -> int:
+    return (k + 7) // 8 * 8
+
+
+def operands(M, N, K, seed, kind):
+    """Seeded operands with leading dimensions padded to a multiple of 8
+    (the TMA row-stride rule); the padding columns hold fp16 NaN."""
+    return inputs.gemm_operands(M, N, K, seed=seed, kind=kind, lda=ceil8(K), ldb=ceil8(K),
+                                pad="nan")
+
+
 def upload(x: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(x).cuda()
 
@@ -71,9 +82,6 @@ def check_full(A, B, K, kind, what, **kw):
         assert_tol(C, ref, ref_abs, what)
 
 
-ALL_CONFIGS = None
-
-
 def configs(suffix=""):
     return [n for n in wgemm.config_names() if n.endswith(suffix)]
 
@@ -90,7 +98,7 @@ def test_every_config_ragged(cfg, kind):
     # 3 tile rows and 3 tile columns for the largest tiles, all edges ragged,
     # K a non-multiple of the 64-wide k-block.
     M, N, K = 600, 1100, 300
-    A, B = inputs.gemm_operands(M, N, K, seed=100 + cfg, kind=kind)
+    A, B = operands(M, N, K, 100 + cfg, kind)
     check_full(A, B, K, kind, f"{names[cfg]} {kind}", config=names[cfg], mode=DP)
 
 
@@ -161,8 +169,10 @@ def test_empty_m_or_n_is_noop():
                                    (128, 256, 64), (256, 512, 128)])
 def test_tiny_and_exact_tile_shapes(M, N, K):
     lda = ldb = ((K + 7) // 8) * 8
-    for name in ("g1_128x64_s8_a2_direct", "g1_128x256_s4_a2_tma", "g2_256x256_s6_a2_tma",
-                 "g2_512x256_s4_a1_tma", None):
+    names = ["g1_128x64_s8_a2_direct", "g2_256x256_s6_a2_direct", None]
+    if N % 4 == 0:  # a contiguous C allows the TMA epilogue
+        names += ["g1_128x256_s4_a2_tma", "g2_256x256_s6_a2_tma", "g2_512x256_s4_a1_tma"]
+    for name in names:
         A, B = inputs.gemm_operands(M, N, K, seed=3, kind="int", lda=lda, ldb=ldb)
         check_full(A, B, K, "int", f"{name} {M}x{N}x{K}", config=name,
                    mode=DP if name else -1)
@@ -174,6 +184,14 @@ def test_padding_past_k_never_read():
     A, B = inputs.gemm_operands(M, N, K, seed=9, kind="uniform", lda=136, ldb=112, pad="nan")
     for name in ("g1_128x256_s4_a2_tma", "g2_256x256_s6_a2_direct", "g2_512x128_s4_a2_tma"):
         check_full(A, B, K, "uniform", name, config=name, mode=DP)
+
+
+def test_unaligned_c_rows_use_register_stores():
+    # N = 53: rows of a contiguous C are not 16-byte aligned; the default
+    # choice stores from registers and the result is still exact.
+    for M, N, K in ((37, 53, 72), (700, 1531, 200), (1600, 1999, 64)):
+        A, B = operands(M, N, K, 31, "int")
+        check_full(A, B, K, "int", f"unaligned C {M}x{N}x{K}")
 
 
 def test_ldc_padding_untouched():
@@ -189,14 +207,14 @@ def test_ldc_padding_untouched():
 
 def test_side_stream():
     M, N, K = 300, 400, 500
-    A, B = inputs.gemm_operands(M, N, K, seed=12, kind="int")
+    A, B = operands(M, N, K, 12, "int")
     s = torch.cuda.Stream()
     dA, dB = upload(A), upload(B)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
-        C = wgemm.gemm(dA, dB)
+        C = wgemm.gemm(dA[:, :K], dB[:, :K])
         assert wgemm.wgemm_check(s.cuda_stream) == 0
-    assert_exact(C.cpu().numpy().astype(np.float64), oracle.gemm_f64(A, B), "side stream")
+    assert_exact(C.cpu().numpy().astype(np.float64), oracle.gemm_f64(A, B, K=K), "side stream")
 
 
 def test_argument_errors_on_gpu():
@@ -209,8 +227,14 @@ def test_argument_errors_on_gpu():
     assert wgemm.wgemm_f16f32_config(A.data_ptr(), A.data_ptr(), C.data_ptr(), 8, 8, 8, 64, 64,
                                      64, 999, 0, 1, None) == -6
     direct = wgemm.config_id("g2_256x256_s6_a2_direct")
-    assert wgemm.wgemm_f16f32_config(A.data_ptr(), A.data_ptr(), C.data_ptr(), 64, 64, 640, 64,
+    assert wgemm.wgemm_f16f32_config(A.data_ptr(), A.data_ptr(), C.data_ptr(), 64, 64, 64, 64,
                                      64, 64, direct, SPLIT, 2, None) == -6
+    # A TMA epilogue forced on a C whose rows are not 16-byte aligned.
+    tma = wgemm.config_id("g2_256x256_s6_a2_tma")
+    assert wgemm.wgemm_f16f32_config(A.data_ptr(), A.data_ptr(), C.data_ptr() + 4, 8, 8, 8, 64,
+                                     64, 64, tma, 0, 1, None) == -2
+    assert wgemm.wgemm_f16f32_config(A.data_ptr(), A.data_ptr(), C.data_ptr(), 8, 6, 8, 64,
+                                     64, 6, tma, 0, 1, None) == -2
 
 
 # ---------------------------------------------------------------- the workloads at full size
