@@ -528,3 +528,102 @@ int wgemm_debug_plan(int M, int N, int K, int config_id, int mode, int splits, i
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free split-K entry point (wgemm_f16f32_splitk_noalloc).
+//
+// Its split-K flags live in a fixed array in device memory that belongs to the
+// library image itself: every device that loads the library holds these
+// 64 KiB until the process exits. Host code must not use the array's name as
+// a device address (on the host it names a stand-in); the device address is
+// taken once per device with cudaGetSymbolAddress, with that device current.
+namespace wg {
+
+constexpr uint32_t kNoAllocFlagWords = 16384;  // 64 KiB of split-K flags
+static __device__ __align__(256) uint32_t g_noalloc_flags[kNoAllocFlagWords];
+
+namespace {
+
+struct NoAllocState {
+  uint32_t* flags = nullptr;  // device address of g_noalloc_flags on this device
+  uint32_t epoch = 0;         // flags only grow, so nothing is ever cleared
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+// Requires g_mu. First call on a device: look up the array's device address.
+int noalloc_flags(int dev, NoAllocState** out) {
+  NoAllocState& s = g_noalloc[dev];
+  if (!s.flags) {
+    uint32_t* ptr = nullptr;
+    if (cudaGetSymbolAddress((void**)&ptr, g_noalloc_flags) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return WGEMM_ERR_LAUNCH;
+    }
+    s.flags = ptr;
+  }
+  *out = &s;
+  return WGEMM_OK;
+}
+
+int run_noalloc(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int lda,
+                int ldb, int ldc, int splits, cudaStream_t stream) {
+  int rc = check_args(A, B, C, M, N, K, lda, ldb, ldc);
+  if (rc != WGEMM_OK) return rc;
+  if (splits < 1) return WGEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return WGEMM_OK;
+  if (!c_tma_ok(C, ldc)) return WGEMM_ERR_ALIGNMENT;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  DeviceState* st;
+  if ((rc = device_state(&dev, &st)) != WGEMM_OK) return rc;
+  NoAllocState* na;
+  if ((rc = noalloc_flags(dev, &na)) != WGEMM_OK) return rc;
+  if (K == 0) {
+    const int64_t total = (int64_t)M * N;
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)st->sm_count * 8);
+    wgemm_zero_kernel<<<blocks, 256, 0, stream>>>(C, M, N, ldc);
+    return cudaGetLastError() == cudaSuccess ? WGEMM_OK : WGEMM_ERR_LAUNCH;
+  }
+  const int config_id = find_config("g2_512x256_s4_a1_tma");
+  if (config_id < 0) return WGEMM_ERR_CONFIG;
+  const KernelEntry& e = *registry().entries[config_id];
+  const int mw = max_workers(*st, config_id);
+  if (mw < 0) return mw;
+  if ((rc = encoder()) != WGEMM_OK) return rc;
+  KParams params;
+  std::memset(&params, 0, sizeof(params));
+  if ((rc = make_plan(e, M, N, K, kSplitK, splits, mw, &params.plan)) != WGEMM_OK) return rc;
+  const size_t words = (size_t)params.plan.num_tiles * e.cg * params.plan.splits;
+  if (words > kNoAllocFlagWords) return WGEMM_ERR_NOALLOC_TOO_LARGE;
+  const int brows_a = e.bn / e.cg, rows_b = 128 * e.reps;
+  if (!encode_2d(&params.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
+                 (uint64_t)lda * 2, kBK, (uint32_t)brows_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&params.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)K, (uint64_t)N,
+                 (uint64_t)ldb * 2, kBK, (uint32_t)rows_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&params.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, (uint64_t)N, (uint64_t)M,
+                 (uint64_t)ldc * 4, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return WGEMM_ERR_LAUNCH;
+  params.C = C;
+  params.ldc = ldc;
+  params.status = st->status;
+  params.flags = na->flags;
+  params.epoch = ++na->epoch;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(e, params.plan.workers, stream, attr);
+  void* args[] = {&params};
+  if (cudaLaunchKernelExC(&cfg, e.func, args) != cudaSuccess) {
+    cudaGetLastError();
+    return WGEMM_ERR_LAUNCH;
+  }
+  return WGEMM_OK;
+}
+
+}  // namespace
+}  // namespace wg
+
+extern "C" int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
+                                           int M, int N, int K, int lda, int ldb, int ldc,
+                                           int splits, wgemm_stream_t stream) {
+  return wg::run_noalloc(A, B, C, M, N, K, lda, ldb, ldc, splits,
+                         reinterpret_cast<cudaStream_t>(stream));
+}

@@ -20,7 +20,7 @@ WGEMM_OK = 0
 STATUS_NAMES = {
     0: "WGEMM_OK", -1: "WGEMM_ERR_INVALID_ARG", -2: "WGEMM_ERR_ALIGNMENT", -3: "WGEMM_ERR_LAUNCH",
     -4: "WGEMM_ERR_NO_DEVICE", -5: "WGEMM_ERR_DEVICE_TIMEOUT", -6: "WGEMM_ERR_CONFIG",
-    -7: "WGEMM_ERR_WORKSPACE",
+    -7: "WGEMM_ERR_WORKSPACE", -8: "WGEMM_ERR_NOALLOC_TOO_LARGE",
 }
 MODE_DATA_PARALLEL, MODE_SPLIT_K, MODE_STREAM_K = 0, 1, 2
 
@@ -51,6 +51,8 @@ def load():
         lib.wgemm_f16f32.restype = i
         lib.wgemm_f16f32_config.argtypes = [p, p, p, i, i, i, i, i, i, i, i, i, p]
         lib.wgemm_f16f32_config.restype = i
+        lib.wgemm_f16f32_splitk_noalloc.argtypes = [p, p, p, i, i, i, i, i, i, i, p]
+        lib.wgemm_f16f32_splitk_noalloc.restype = i
         lib.wgemm_num_configs.argtypes = []
         lib.wgemm_num_configs.restype = i
         lib.wgemm_config_name.argtypes = [i]
@@ -125,6 +127,13 @@ def wgemm_f16f32_config(A: int, B: int, C: int, M: int, N: int, K: int, lda: int
                         stream: int | None) -> int:
     return load().wgemm_f16f32_config(A, B, C, M, N, K, lda, ldb, ldc, config, mode, splits,
                                       stream)
+
+
+def wgemm_f16f32_splitk_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int,
+                                ldb: int, ldc: int, splits: int, stream: int | None) -> int:
+    """Split-K on device pointers with the library's fixed scratch array (no
+    allocation); returns the status code."""
+    return load().wgemm_f16f32_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, splits, stream)
 
 
 def wgemm_select(M: int, N: int, K: int) -> tuple[int, int, int]:

@@ -59,6 +59,7 @@ typedef uint16_t wgemm_f16_t;
 #define WGEMM_ERR_DEVICE_TIMEOUT -5   /* a bounded wait inside a kernel expired (see wgemm_last_device_error) */
 #define WGEMM_ERR_CONFIG -6           /* the forced configuration id does not exist or cannot run this shape */
 #define WGEMM_ERR_WORKSPACE -7        /* the flag workspace could not be allocated */
+#define WGEMM_ERR_NOALLOC_TOO_LARGE -8 /* the problem needs more split-K flags than wgemm_f16f32_splitk_noalloc's fixed array holds */
 
 /*
  * C = A·Bᵀ on `stream`.
@@ -122,6 +123,41 @@ size_t wgemm_workspace_bytes(void);
 
 /* Frees the current device's flag workspaces after synchronising the device. */
 int wgemm_release_workspace(void);
+
+/*
+ * Split-K C = A·Bᵀ that allocates nothing. The paper has no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc or cudaFree
+ * while they run, for example a process whose framework allocator has
+ * reserved the device memory for itself (a new allocation can fail), a
+ * latency-bound serving loop that cannot afford the device-wide
+ * synchronisation cudaFree implies when a workspace grows, or a host
+ * application that forbids plug-in libraries from owning device allocations.
+ *
+ * Same arguments and result as wgemm_f16f32 (A, B, C device pointers owned by
+ * the caller), computed by the pair-MMA configuration g2_512x256_s4_a1_tma
+ * with K split `splits` ways (splits >= 1, clamped to ceil(K / 64)). C must
+ * be 16-byte aligned with ldc % 4 == 0 (the partial sums are added into C
+ * with TMA reduce-adds), else WGEMM_ERR_ALIGNMENT.
+ *
+ * Scratch: the split-K flags live in a fixed array of 16384 32-bit words
+ * (64 KiB) of device memory inside the library image, which every device that
+ * loads the library holds until the process exits. A call needs
+ * ceil(M / 256) · ceil(N / 512) · 2 · splits words; a larger problem is
+ * rejected with WGEMM_ERR_NOALLOC_TOO_LARGE before anything is enqueued.
+ * The array keeps the previous call's contents; the flags hold a per-device
+ * call counter that only grows, so nothing needs clearing between calls.
+ * Every call on a device shares the one array: calls that overlap on the GPU
+ * (for example on two streams at once) race on it and give wrong results;
+ * order them on one stream or with events.
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and the kernel's attributes
+ * and occupancy; make that first call before any stream capture. The call
+ * never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
+                                int M, int N, int K, int lda, int ldb, int ldc,
+                                int splits, wgemm_stream_t stream);
 
 /*
  * Host-side introspection, no GPU needed (used by the host tests).
