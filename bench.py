@@ -44,6 +44,7 @@ WORKLOADS = {
 WORKLOADS["all"] = (WORKLOADS["c1"] + WORKLOADS["sweep"] + WORKLOADS["large"]
                     + WORKLOADS["streamk"] + WORKLOADS["splitk"])
 FLUSH_BYTES = 256 << 20  # > the 129 MB L2
+GATE_CYCLES = 400_000    # ≈ 0.2 ms of GPU spin ahead of each timed call
 FALLBACK_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -62,14 +63,17 @@ def peaks():
         return FALLBACK_TFLOPS, FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ["wgemm_kernel.cuh", "wgemm_plan.h", "wgemm_configs.h", "inst_single.cu",
+                  "inst_pair.cu", "sm103/ptx.cuh", "sm103/umma_desc.h"]
+
+
 def kernel_source_digest() -> str:
+    """Digest of the files that define the GEMM kernels (not the host code)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp16_gemm_02_gb300", "csrc")
-    for d, _, files in sorted(os.walk(csrc)):
-        for f in sorted(files):
-            if f.endswith((".cu", ".cuh", ".h")):
-                with open(os.path.join(d, f), "rb") as fh:
-                    h.update(f.encode() + fh.read())
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -250,7 +254,10 @@ def run_ours(args):
 
     def one_step(events):
         for i in range(len(shapes)):
-            flush.fill_(float(i))  # evict L2; the GPU is busy while the call is enqueued
+            flush.fill_(float(i))  # evict L2
+            # Keep the GPU busy while the host enqueues the start event and the
+            # call, so the event pair brackets the kernel, not host latency.
+            torch.cuda._sleep(GATE_CYCLES)
             e0, e1 = events[i]
             e0.record(stream)
             call(i)
@@ -370,7 +377,8 @@ def run_ours(args):
                 "inputs": "uniform[-1,1] rounded to fp16, seeded SplitMix64, resident in HBM",
                 "accumulate": "f32", "output": "f32",
                 "l2": "flushed between calls (256 MiB write), each call timed alone",
-                "timing": "CUDA events on the launching stream around each call",
+                "timing": ("CUDA events on the launching stream around each call; a GPU-side "
+                       "spin ahead of the start event hides host enqueue latency"),
                 "parallelism": "replicas" if world > 1 else "single GPU",
             },
             "shapes": per_shape,
@@ -402,11 +410,19 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="sweep")
+    ap.add_argument("--shape", metavar="MxNxK",
+                    help="time this one shape instead of a named workload")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="oracle time budget of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.shape:
+        dims = tuple(int(v) for v in args.shape.lower().split("x"))
+        if len(dims) != 3 or min(dims) <= 0:
+            ap.error("--shape wants MxNxK")
+        WORKLOADS["shape"] = [dims]
+        args.workload = "shape"
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

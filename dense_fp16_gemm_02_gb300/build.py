@@ -26,7 +26,7 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-DNDEBUG", "-Xcompiler", "-fPIC",
 def _headers() -> list[str]:
     out = []
     for d, _, files in os.walk(CSRC):
-        out += [os.path.join(d, f) for f in files if f.endswith((".h", ".cuh"))]
+        out += [os.path.join(d, f) for f in files if f.endswith((".h", ".cuh", ".inc"))]
     out.append(os.path.join(ROOT, "include", "wgemm.h"))
     return out
 

@@ -187,7 +187,25 @@ struct Choice {
   int config, mode, splits;
 };
 
+struct TunedRow {
+  int M, N, K;
+  const char* config;
+  int mode, splits;
+  double us;
+};
+
+const TunedRow kTuned[] = {
+#include "wgemm_tuned.inc"
+};
+
 Choice choose(int M, int N, int K, int workers_hint, bool c_tma_ok) {
+  for (const TunedRow& r : kTuned) {
+    if (r.M == M && r.N == N && r.K == K) {
+      const int id = find_config(r.config);
+      const bool tma = std::strstr(r.config, "_tma") != nullptr;
+      if (id >= 0 && (c_tma_ok || !tma)) return {id, r.mode, r.splits};
+    }
+  }
   if (!c_tma_ok) {
     // C rows not 16-byte aligned: no TMA on C, so a direct-store epilogue
     // and no K decomposition.
