@@ -16,11 +16,17 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libwgemm.so")
-SOURCES = ["wgemm_host.cu", "inst_single.cu", "inst_pair.cu"]
+SOURCES = ["wgemm_host.cu", "inst_single.cu", "inst_pair.cu", "inst_pair2.cu"]
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-DNDEBUG", "-Xcompiler", "-fPIC",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), "-I", CSRC]
+# WGEMM_CHECKED=1 in the environment builds the index-checking debug variant
+# into a separate directory (dense_fp16_gemm_02_gb300/_build_checked).
+if os.environ.get("WGEMM_CHECKED") == "1":
+    FLAGS.append("-DWGEMM_CHECKED=1")
+    BUILD = os.path.join(HERE, "_build_checked")
+    LIB = os.path.join(BUILD, "libwgemm.so")
 
 
 def _headers() -> list[str]:

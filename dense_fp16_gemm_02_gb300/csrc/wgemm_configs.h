@@ -19,6 +19,8 @@ extern const KernelEntry kEntriesPair[];
 extern const int kNumEntriesPair;
 extern const KernelEntry kEntriesSingle[];
 extern const int kNumEntriesSingle;
+extern const KernelEntry kEntriesPair2[];
+extern const int kNumEntriesPair2;
 
 }  // namespace wg
 

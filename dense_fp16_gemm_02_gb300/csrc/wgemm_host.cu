@@ -42,6 +42,7 @@ struct Registry {
   Registry() {
     for (int i = 0; i < kNumEntriesSingle; ++i) entries.push_back(&kEntriesSingle[i]);
     for (int i = 0; i < kNumEntriesPair; ++i) entries.push_back(&kEntriesPair[i]);
+    for (int i = 0; i < kNumEntriesPair2; ++i) entries.push_back(&kEntriesPair2[i]);
   }
 };
 
@@ -372,6 +373,7 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
     const size_t words = (size_t)params.plan.num_tiles * e.cg * params.plan.splits;
     if ((rc = workspace(dev, stream, words, &ws)) != WGEMM_OK) return rc;
     params.flags = ws->flags;
+    params.flag_words = (int32_t)(ws->bytes / sizeof(uint32_t));
     params.epoch = ++ws->epoch;
   }
   if (env_log())
@@ -625,6 +627,7 @@ int run_noalloc(const uint16_t* A, const uint16_t* B, float* C, int M, int N, in
   params.ldc = ldc;
   params.status = st->status;
   params.flags = na->flags;
+  params.flag_words = (int32_t)kNoAllocFlagWords;
   params.epoch = ++na->epoch;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(e, params.plan.workers, stream, attr);

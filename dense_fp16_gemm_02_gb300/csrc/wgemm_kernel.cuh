@@ -64,6 +64,14 @@ enum WaitSite : int32_t {
   kSiteEpiFlagOwner = 0x22,
   kSiteEpiFlagZero = 0x23,
   kSiteEpiSync = 0x24,
+  // index checks of debug builds
+  kCheckPlan = 0x31,
+  kCheckTmemMma = 0x32,
+  kCheckTmemLd = 0x33,
+  kCheckStore = 0x34,
+  kCheckStaging = 0x35,
+  kCheckFlag = 0x36,
+  kCheckZero = 0x37,
 };
 
 struct KParams {
@@ -75,7 +83,7 @@ struct KParams {
   int64_t ldc;
   uint32_t* flags;  // split-K / stream-K flags (monotone epochs)
   uint32_t epoch;
-  int32_t pad_;
+  int32_t flag_words;  // words the flag array holds
   DeviceStatus* status;
 };
 
@@ -105,7 +113,11 @@ struct Cfg {
   static constexpr uint32_t kAccCols = REPS * BN;   // TMEM columns per accumulator
   static constexpr uint32_t kTmemCols = pow2_at_least_32(kAccCols * ACC);
   static constexpr uint32_t kEpiSlotBytes = 32 * 32 * 4;  // one 32×32 fp32 staging tile
-  static constexpr uint32_t kEpiBytes = EPI == kEpiTma ? 4 * 2 * kEpiSlotBytes : 0;
+  // TMEM chunks (32 columns each) drained per wait: 4 when storing from
+  // registers, 2 when staging through shared memory (one slot per chunk).
+  static constexpr int kEpiBatch = EPI == kEpiTma ? (BN / 32 >= 2 ? 2 : 1)
+                                                  : (BN / 32 >= 4 ? 4 : BN / 32);
+  static constexpr uint32_t kEpiBytes = EPI == kEpiTma ? 4 * kEpiBatch * kEpiSlotBytes : 0;
   static constexpr uint32_t kIdesc = umma_idesc_f16(128 * CG, BN);
 
   // Shared-memory layout (offsets from a 1024-byte-aligned base).
@@ -118,16 +130,11 @@ struct Cfg {
 
   static_assert(CG == 1 || CG == 2, "CG");
   static_assert(REPS == 1 || REPS == 2, "REPS");
-  static_assert(BN % (16 * CG) == 0 && BN >= 32 && BN <= 256, "MMA N");
+  static_assert(BN % 32 == 0 && BN % (16 * CG) == 0 && BN >= 32 && BN <= 256, "MMA N");
   static_assert(kBrows % 8 == 0, "operand rows in 8-row groups");
   static_assert(kAccCols * ACC <= 512, "TMEM capacity");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
-};
-
-struct Shared {
-  uint32_t base;  // shared address of the aligned base
-  uint8_t* ptr;
 };
 
 __device__ __forceinline__ void record_error(DeviceStatus* st, int32_t code, int32_t site,
@@ -140,6 +147,17 @@ __device__ __forceinline__ void record_error(DeviceStatus* st, int32_t code, int
     __threadfence();
   }
 }
+
+// Debug builds (-DWGEMM_CHECKED=1) verify every index the kernel derives
+// (plan coordinates, TMEM columns, shared-memory offsets, global addresses,
+// flag indices) before use; a violation is recorded in the device status word
+// (code -9, the site, and the offending value) and the access is skipped.
+#ifndef WGEMM_CHECKED
+#define WGEMM_CHECKED 0
+#endif
+#define WG_CHECK(st, cond, site, value)                            \
+  (!WGEMM_CHECKED || (cond) ||                                     \
+   (record_error((st), -9, (site), (uint32_t)(value)), false))
 
 // Bounded wait for the phase of parity `parity` of `bar`. False on timeout or
 // when another role of the CTA has aborted.
@@ -208,6 +226,14 @@ struct Kernel {
     return stage_a(base, s) + K::kAbytes;
   }
 
+  __device__ static bool unit_ok(const KParams& p, const Unit& u) {
+    return WG_CHECK(p.status, u.tm >= 0 && u.tm < p.plan.tiles_m, kCheckPlan, u.tm) &&
+           WG_CHECK(p.status, u.tn >= 0 && u.tn < p.plan.tiles_n, kCheckPlan, u.tn) &&
+           WG_CHECK(p.status, u.kb_begin >= 0 && u.kb_begin < u.kb_end && u.kb_end <= p.plan.kblocks,
+                    kCheckPlan, u.kb_end) &&
+           WG_CHECK(p.status, u.tile >= 0 && u.tile < p.plan.num_tiles, kCheckPlan, u.tile);
+  }
+
   // ------------------------------------------------------------ producer
   __device__ static void producer(const KParams& p, uint32_t base, uint32_t rank,
                                   int32_t worker, volatile uint32_t* abort_flag) {
@@ -216,6 +242,7 @@ struct Kernel {
     for (int32_t i = 0; ok; ++i) {
       Unit u;
       if (!plan_unit(p.plan, worker, i, u)) break;
+      if (!unit_ok(p, u)) { ok = false; break; }
       const int32_t b_row0 = u.tn * K::kTileCols + (int32_t)rank * K::kCtaCols;  // rows of B
       const int32_t a_row0 = u.tm * K::kTileRows + (int32_t)rank * K::kBrows;    // rows of A
       for (int32_t kb = u.kb_begin; kb < u.kb_end; ++kb) {
@@ -261,6 +288,11 @@ struct Kernel {
       }
       tcgen05_fence_after();
       const uint32_t d = tmem + ab * K::kAccCols;
+      if (!unit_ok(p, u) ||
+          !WG_CHECK(p.status, (ab + 1) * K::kAccCols <= K::kTmemCols, kCheckTmemMma, ab)) {
+        ok = false;
+        break;
+      }
       for (int32_t kb = u.kb_begin; kb < u.kb_end; ++kb) {
         if (!wait_bar(bar_full(base, s), ph, abort_flag, p.status, kSiteMmaFull)) {
           ok = false;
@@ -307,14 +339,105 @@ struct Kernel {
     return ok;
   }
 
+  // One batch of the epilogue: chunks [c0, c0 + NBB) of one atom of the
+  // accumulator (TMEM columns from `tatom`) go to C rows row0 + 32·c0 ...,
+  // columns col_warp + lane. Chunks wholly outside C are skipped. When
+  // `release` is set the accumulator is handed back to the MMA warp once the
+  // batch's TMEM reads are complete.
+  template <int NBB>
+  __device__ static void drain(const KParams& p, uint32_t base, uint8_t* smem, uint32_t tmem,
+                               uint32_t tatom, int c0, int32_t col_warp, int32_t row0, bool add,
+                               uint32_t stage_base, bool release, uint32_t ab) {
+    const uint32_t lane = threadIdx.x % 32;
+    const int32_t M = p.plan.M, N = p.plan.N;
+    const int64_t ldc = p.ldc;
+    bool live = col_warp < N && row0 + c0 * 32 < M;  // warp-uniform
+    live = live && WG_CHECK(p.status,
+                            (tatom & 0xFFFFu) - (tmem & 0xFFFFu) + (c0 + NBB) * 32u <= K::kTmemCols,
+                            kCheckTmemLd, tatom);
+    uint32_t v[NBB][32];
+    // tcgen05.ld / wait::ld are .sync.aligned: the whole warp must execute
+    // them together, so reconverge after any lane-divergent stores before.
+    __syncwarp();
+    if (live) {
+#pragma unroll
+      for (int b = 0; b < NBB; ++b) tmem_ld_32x32b_x32(tatom + (c0 + b) * 32, v[b]);
+      tmem_ld_wait();
+    }
+    if (release) {
+      tcgen05_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (K::CG == 1) mbar_arrive(bar_acce(base, ab));
+        else mbar_arrive_cluster(mapa_shared(bar_acce(base, ab), 0));
+      }
+    }
+    if (!live) return;
+    if constexpr (K::EPI == kEpiDirect) {
+      const int32_t col = col_warp + (int32_t)lane;
+      if (col < N) {
+#pragma unroll
+        for (int b = 0; b < NBB; ++b) {
+          const int32_t row_c = row0 + (c0 + b) * 32;
+          float* dst = p.C + (int64_t)row_c * ldc + col;
+          if (WGEMM_CHECKED) {
+            for (int e = 0; e < 32; ++e) {
+              const int64_t off = (int64_t)(row_c + e) * ldc + col;
+              if (row_c + e < M &&
+                  WG_CHECK(p.status, col >= 0 && off >= 0 && off < (int64_t)(M - 1) * ldc + N,
+                           kCheckStore, off))
+                dst[e * ldc] = __uint_as_float(v[b][e]);
+            }
+          } else if (row_c + 32 <= M) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dst[e * ldc] = __uint_as_float(v[b][e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (row_c + e < M) dst[e * ldc] = __uint_as_float(v[b][e]);
+          }
+        }
+      }
+      __syncwarp();
+    } else {
+      // Stage each 32 rows × 32 columns block row-major (one slot per chunk,
+      // reused once the previous batch's stores have read it), then one lane
+      // writes them out with TMA stores or reduce-adds; TMA clips what lies
+      // outside M × N.
+      if (!WG_CHECK(p.status,
+                    stage_base - base + NBB * K::kEpiSlotBytes <= K::kOffBars &&
+                        stage_base - base >= K::kOffEpi,
+                    kCheckStaging, stage_base - base))
+        return;
+      if (lane == 0) bulk_wait_group_read<0>();
+      __syncwarp();
+#pragma unroll
+      for (int b = 0; b < NBB; ++b) {
+        float* sp = reinterpret_cast<float*>(smem + (stage_base - base) + b * K::kEpiSlotBytes);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sp[e * 32 + lane] = __uint_as_float(v[b][e]);
+      }
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int b = 0; b < NBB; ++b) {
+          const uint32_t sbuf = stage_base + b * K::kEpiSlotBytes;
+          const int32_t row_c = row0 + (c0 + b) * 32;
+          if (add) tma_reduce_add_2d(&p.tmC, sbuf, col_warp, row_c);
+          else tma_store_2d(&p.tmC, sbuf, col_warp, row_c);
+        }
+        bulk_commit_group();
+      }
+    }
+  }
+
   // ------------------------------------------------------------ epilogue
   // 128 threads (warps 4..7); warp q = warp % 4 reads TMEM lanes 32q..32q+31.
   __device__ static void epilogue(const KParams& p, uint32_t base, uint8_t* smem, uint32_t tmem,
                                   uint32_t rank, int32_t worker, volatile uint32_t* abort_flag) {
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t q = warp & 3;
-    const int32_t M = p.plan.M, N = p.plan.N;
-    const int64_t ldc = p.ldc;
     bool ok = true;
     uint32_t sync_phase = 0;
 
@@ -322,7 +445,7 @@ struct Kernel {
       if (p.plan.mode == kSplitK) ok = zero_slices(p, base, rank, worker, sync_phase, abort_flag);
     }
 
-    uint32_t ab = 0, aph = 0, slot = 0;
+    uint32_t ab = 0, aph = 0;
     const uint32_t stage_base = base + K::kOffEpi + q * 2 * K::kEpiSlotBytes;
     for (int32_t i = 0; ok; ++i) {
       Unit u;
@@ -333,17 +456,23 @@ struct Kernel {
       }
       __syncwarp();
       tcgen05_fence_after();
+      if (!unit_ok(p, u)) { ok = false; break; }
       const int32_t col_cta = u.tn * K::kTileCols + (int32_t)rank * K::kCtaCols;
       const int32_t row0 = u.tm * K::kTileRows;
       const bool add = u.kind == kUnitAddAfterOwner || u.kind == kUnitAddAfterZero;
       if constexpr (K::EPI == kEpiTma) {
         if (add && lane == 0) {
           if (u.kind == kUnitAddAfterOwner) {
-            ok = wait_flag(p.flags + (u.tile * K::CG + rank), p.epoch, abort_flag, p.status,
+            ok = WG_CHECK(p.status, (int32_t)(u.tile * K::CG + rank) < p.flag_words, kCheckFlag,
+                          u.tile) &&
+                 wait_flag(p.flags + (u.tile * K::CG + rank), p.epoch, abort_flag, p.status,
                            kSiteEpiFlagOwner);
           } else {
             for (int32_t s = 0; s < p.plan.splits && ok; ++s)
-              ok = wait_flag(p.flags + ((u.tile * K::CG + rank) * p.plan.splits + s), p.epoch,
+              ok = WG_CHECK(p.status,
+                            (int32_t)((u.tile * K::CG + rank) * p.plan.splits + s) < p.flag_words,
+                            kCheckFlag, u.tile) &&
+                   wait_flag(p.flags + ((u.tile * K::CG + rank) * p.plan.splits + s), p.epoch,
                              abort_flag, p.status, kSiteEpiFlagZero);
           }
           // The flag's acquire covers generic writes; order them before the
@@ -353,59 +482,24 @@ struct Kernel {
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
       }
+      // TMEM is drained in batches of NB chunks of 32 columns (32 rows of C):
+      // all loads of a batch are issued before one wait, so their latency is
+      // paid once per batch; a shorter batch takes the remainder of an atom.
       constexpr int kChunks = K::BN / 32;
+      constexpr int NB = K::kEpiBatch;
+      constexpr int kFull = kChunks / NB, kRem = kChunks % NB;
+      const uint32_t tacc = tmem + ((q * 32u) << 16) + ab * K::kAccCols;
 #pragma unroll 1
       for (int r = 0; r < K::REPS; ++r) {
+        const int32_t col_warp = col_cta + r * 128 + (int32_t)q * 32;
+        const bool last_atom = r == K::REPS - 1;
 #pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) {
-          uint32_t v[32];
-          const uint32_t taddr = tmem + ((q * 32u) << 16) + ab * K::kAccCols + r * K::BN + c * 32;
-          tmem_ld_32x32b_x32(taddr, v);
-          tmem_ld_wait();
-          if (r == K::REPS - 1 && c == kChunks - 1) {
-            // Accumulator fully read: hand it back to the MMA warp.
-            tcgen05_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if constexpr (K::CG == 1) mbar_arrive(bar_acce(base, ab));
-              else mbar_arrive_cluster(mapa_shared(bar_acce(base, ab), 0));
-            }
-          }
-          const int32_t col_warp = col_cta + r * 128 + (int32_t)q * 32;
-          const int32_t row_c = row0 + c * 32;
-          if constexpr (K::EPI == kEpiDirect) {
-            const int32_t col = col_warp + (int32_t)lane;
-            if (col < N) {
-              float* dst = p.C + (int64_t)row_c * ldc + col;
-              if (row_c + 32 <= M) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) dst[e * ldc] = __uint_as_float(v[e]);
-              } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  if (row_c + e < M) dst[e * ldc] = __uint_as_float(v[e]);
-              }
-            }
-          } else {
-            // Stage the 32 rows × 32 columns block row-major, then one lane
-            // writes it out with a TMA store (or reduce-add); TMA clips the
-            // parts outside M × N.
-            const uint32_t sbuf = stage_base + slot * K::kEpiSlotBytes;
-            if (lane == 0) bulk_wait_group_read<1>();
-            __syncwarp();
-            float* sp = reinterpret_cast<float*>(smem + (sbuf - base));
-#pragma unroll
-            for (int e = 0; e < 32; ++e) sp[e * 32 + lane] = __uint_as_float(v[e]);
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              if (add) tma_reduce_add_2d(&p.tmC, sbuf, col_warp, row_c);
-              else tma_store_2d(&p.tmC, sbuf, col_warp, row_c);
-              bulk_commit_group();
-            }
-            slot ^= 1;
-          }
-        }
+        for (int bi = 0; bi < kFull; ++bi)
+          drain<NB>(p, base, smem, tmem, tacc + r * K::BN, bi * NB, col_warp, row0, add,
+                    stage_base, last_atom && kRem == 0 && bi == kFull - 1, ab);
+        if constexpr (kRem > 0)
+          drain<kRem>(p, base, smem, tmem, tacc + r * K::BN, kFull * NB, col_warp, row0, add,
+                      stage_base, last_atom, ab);
       }
       if constexpr (K::EPI == kEpiTma) {
         if (u.kind == kUnitStoreRaise) {
@@ -416,7 +510,9 @@ struct Kernel {
             fence_proxy_async_global();
           }
           if (!epi_sync(base, sync_phase, abort_flag, p.status)) { ok = false; break; }
-          if (threadIdx.x == 128) {
+          if (threadIdx.x == 128 &&
+              WG_CHECK(p.status, (int32_t)(u.tile * K::CG + rank) < p.flag_words, kCheckFlag,
+                       u.tile)) {
             fence_acq_rel_gpu();
             st_release_gpu(p.flags + (u.tile * K::CG + rank), p.epoch);
           }
@@ -452,6 +548,9 @@ struct Kernel {
       if (row_begin >= row_end || col_begin >= col_end) continue;
       const int32_t ncols = col_end - col_begin;
       const int32_t nvec = ncols / 4;  // ldc % 4 == 0 and C is 16-byte aligned
+      if (!WG_CHECK(p.status, row_begin >= 0 && row_end <= M && col_begin >= 0 && col_end <= N,
+                    kCheckZero, row_end))
+        continue;
       for (int32_t r = row_begin; r < row_end; ++r) {
         float* row = p.C + (int64_t)r * ldc + col_begin;
         for (int32_t v = t; v < nvec; v += 128)
@@ -466,7 +565,9 @@ struct Kernel {
       for (int32_t i = 0;; ++i) {
         Unit u;
         if (!plan_unit(p.plan, worker, i, u)) break;
-        st_release_gpu(p.flags + ((u.tile * K::CG + rank) * p.plan.splits + u.split), p.epoch);
+        const int32_t fi = (u.tile * K::CG + rank) * p.plan.splits + u.split;
+        if (WG_CHECK(p.status, fi < p.flag_words, kCheckFlag, fi))
+          st_release_gpu(p.flags + fi, p.epoch);
       }
     }
     return true;
@@ -488,6 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   volatile uint32_t* abort_flag = misc + 1;
 
   if (threadIdx.x == 0) {
+    prefetch_tensormap(&p.tmA);
+    prefetch_tensormap(&p.tmB);
+    if (K::EPI == kEpiTma) prefetch_tensormap(&p.tmC);
     for (int s = 0; s < K::STAGES; ++s) {
       mbar_init(Kernel<K>::bar_full(base, s), 1);
       mbar_init(Kernel<K>::bar_empty(base, s), 1);
@@ -500,11 +604,6 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     mbar_init(Kernel<K>::bar_epi(base), 4);
     *abort_flag = 0;
     fence_mbarrier_init();
-  }
-  if (warp == 0 && lane_id() == 0) {
-    prefetch_tensormap(&p.tmA);
-    prefetch_tensormap(&p.tmB);
-    if (K::EPI == kEpiTma) prefetch_tensormap(&p.tmC);
   }
   if (warp == 1) {
     tmem_alloc<K::CG>(smem_addr(misc), K::kTmemCols);

@@ -90,7 +90,7 @@ def configs(suffix=""):
 
 
 @pytest.mark.parametrize("kind", ["int", "uniform"])
-@pytest.mark.parametrize("cfg", range(10))
+@pytest.mark.parametrize("cfg", range(24))
 def test_every_config_ragged(cfg, kind):
     names = wgemm.config_names()
     if cfg >= len(names):
@@ -100,6 +100,24 @@ def test_every_config_ragged(cfg, kind):
     M, N, K = 600, 1100, 300
     A, B = operands(M, N, K, 100 + cfg, kind)
     check_full(A, B, K, kind, f"{names[cfg]} {kind}", config=names[cfg], mode=DP)
+
+
+@pytest.mark.parametrize("cfg", range(24))
+def test_every_config_multi_round(cfg):
+    # More tiles than co-resident workers for every configuration (≥ 2 tiles
+    # per worker even for the 512×256 pair tile: 11 × 14 = 154 tiles over at
+    # most 76 pairs), so each CTA alternates accumulators and crosses tiles;
+    # ragged last tile row and column, K not a multiple of 64. Exact on
+    # integer inputs; run twice to catch state left over between launches.
+    names = wgemm.config_names()
+    if cfg >= len(names):
+        pytest.skip("fewer configurations compiled")
+    M, N, K = 2600, 7000, 136
+    A, B = operands(M, N, K, 300 + cfg, "int")
+    ref = oracle.gemm_f64(A, B, K=K)
+    for _ in range(2):
+        C = run(A, B, K, config=names[cfg], mode=DP).cpu().numpy().astype(np.float64)
+        assert_exact(C, ref, f"{names[cfg]} multi-round")
 
 
 @pytest.mark.parametrize("splits", [2, 3, 7])
