@@ -64,7 +64,9 @@ def peaks():
 
 
 KERNEL_SOURCES = ["wgemm_kernel.cuh", "wgemm_plan.h", "wgemm_configs.h", "inst_single.cu",
-                  "inst_pair.cu", "inst_pair2.cu", "sm103/ptx.cuh", "sm103/umma_desc.h"]
+                  "inst_pair.cu", "inst_pair2.cu", "inst_multicast.cu", "inst_clc.cu",
+                  "sm103/ptx.cuh",
+                  "sm103/umma_desc.h"]
 
 
 def kernel_source_digest() -> str:

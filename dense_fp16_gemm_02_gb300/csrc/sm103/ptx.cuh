@@ -152,6 +152,18 @@ __device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const v
       : "memory");
 }
 
+// 2-D tile load delivered to the same shared-memory offset of every CTA in
+// `mask`; each destination counts the bytes on the barrier at `bar`'s offset
+// in its own shared memory (one CTA per MMA).
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* tmap, uint32_t bar,
+                                                      int32_t x, int32_t y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;"
+      :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "h"(mask)
+      : "memory");
+}
+
 // 2-D tile store / reduce-add from this CTA's shared memory (bulk group).
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
@@ -207,6 +219,39 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// Ask the hardware to cancel a cluster of this grid that has not launched yet;
+// the 16-byte response lands at `resp` (of every CTA of the cluster with the
+// multicast form) and its bytes complete on `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
+      " [%0], [%1];" :: "r"(resp), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void clc_try_cancel_multicast(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+      ".multicast::cluster::all.b128 [%0], [%1];" :: "r"(resp), "r"(bar) : "memory");
+}
+
+// Decode a response: true if a cluster was cancelled, with the x index of its
+// first CTA in `first_x`.
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t& first_x) {
+  uint32_t ok, x = 0;
+  asm volatile(
+      "{\n\t.reg .b128 rr;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 rr, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, rr;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, rr;\n\t}"
+      : "=r"(ok), "+r"(x)
+      : "r"(resp)
+      : "memory");
+  first_x = x;
+  return ok != 0;
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -271,6 +316,15 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                :: "r"(bar) : "memory");
+}
+
+// Arrive once on the barrier at offset `bar` of every CTA in `mask` when every
+// tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;"
+      :: "r"(bar), "h"(mask) : "memory");
 }
 
 // Pair form: arrive once on the barrier at offset `bar` of every CTA in

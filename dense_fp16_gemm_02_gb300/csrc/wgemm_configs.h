@@ -9,6 +9,8 @@ namespace wg {
 struct KernelEntry {
   const char* name;
   int cg, reps, bn, stages, acc, epi;
+  int mc;                    // MMA groups per cluster sharing the A tile
+  int sched;                 // 0: static persistent grid, 1: cluster launch control
   int tile_rows, tile_cols;  // C rows / columns of one worker tile
   uint32_t smem_bytes;
   const void* func;          // the __global__ function (host stub)
@@ -21,15 +23,26 @@ extern const KernelEntry kEntriesSingle[];
 extern const int kNumEntriesSingle;
 extern const KernelEntry kEntriesPair2[];
 extern const int kNumEntriesPair2;
+extern const KernelEntry kEntriesMulticast[];
+extern const int kNumEntriesMulticast;
+extern const KernelEntry kEntriesClc[];
+extern const int kNumEntriesClc;
 
 }  // namespace wg
 
 // Builds the entry of one configuration (only in .cu files that include the
-// kernel template).
-#define WG_ENTRY(NAME, CG, REPS, BN, STAGES, ACC, EPI)                                          \
+// kernel template). MC = MMA groups per cluster sharing the A tile; SCHED =
+// kSchedStatic or kSchedClc.
+#define WG_ENTRY_FULL(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED)                          \
   wg::KernelEntry {                                                                             \
-    NAME, CG, REPS, BN, STAGES, ACC, EPI, wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI>::kTileRows,   \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI>::kTileCols,                                     \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI>::kSmemBytes,                                    \
-        reinterpret_cast<const void*>(&wg::wgemm_kernel<wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI>>) \
+    NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED,                                            \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED>::kTileRows,                          \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED>::kTileCols,                          \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED>::kSmemBytes,                         \
+        reinterpret_cast<const void*>(                                                          \
+            &wg::wgemm_kernel<wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED>>)              \
   }
+#define WG_ENTRY_MC(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC) \
+  WG_ENTRY_FULL(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, wg::kSchedStatic)
+#define WG_ENTRY(NAME, CG, REPS, BN, STAGES, ACC, EPI) \
+  WG_ENTRY_FULL(NAME, CG, REPS, BN, STAGES, ACC, EPI, 1, wg::kSchedStatic)

@@ -43,6 +43,8 @@ struct Registry {
     for (int i = 0; i < kNumEntriesSingle; ++i) entries.push_back(&kEntriesSingle[i]);
     for (int i = 0; i < kNumEntriesPair; ++i) entries.push_back(&kEntriesPair[i]);
     for (int i = 0; i < kNumEntriesPair2; ++i) entries.push_back(&kEntriesPair2[i]);
+    for (int i = 0; i < kNumEntriesMulticast; ++i) entries.push_back(&kEntriesMulticast[i]);
+    for (int i = 0; i < kNumEntriesClc; ++i) entries.push_back(&kEntriesClc[i]);
   }
 };
 
@@ -142,12 +144,12 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t
 cudaLaunchConfig_t launch_config(const KernelEntry& e, int workers, cudaStream_t stream,
                                  cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(workers * e.cg), 1, 1);
+  cfg.gridDim = dim3((unsigned)(workers * e.cg * e.mc), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = e.smem_bytes;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)e.cg;
+  attr[0].val.clusterDim.x = (unsigned)(e.cg * e.mc);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -166,7 +168,7 @@ int max_workers(DeviceState& st, int id) {
     return WGEMM_ERR_LAUNCH;
   }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_config(e, st.sm_count / e.cg, nullptr, attr);
+  cudaLaunchConfig_t cfg = launch_config(e, st.sm_count / (e.cg * e.mc), nullptr, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, e.func, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
@@ -234,6 +236,16 @@ Choice choose(int M, int N, int K, int workers_hint, bool c_tma_ok) {
   return {find_config("g2_256x64_s10_a2_direct"), kDataParallel, 1};
 }
 
+// Tile rows per raster group (WGEMM_RASTER_GROUP overrides the default 8).
+int raster_group() {
+  static const int g = [] {
+    const char* v = std::getenv("WGEMM_RASTER_GROUP");
+    const int x = v ? std::atoi(v) : 0;
+    return x > 0 ? x : 8;
+  }();
+  return g;
+}
+
 int check_args(const void* A, const void* B, const void* C, int M, int N, int K, int lda, int ldb,
                int ldc) {
   if (M < 0 || N < 0 || K < 0) return WGEMM_ERR_INVALID_ARG;
@@ -270,9 +282,13 @@ int make_plan(const KernelEntry& e, int M, int N, int K, int mode, int splits, i
   p->kblocks = (K + kBK - 1) / kBK;
   p->mode = mode;
   p->splits = 1;
-  p->group = 8;
-  if (mode != kDataParallel && e.epi != kEpiTma) return WGEMM_ERR_CONFIG;
-  if (mode == kDataParallel) {
+  p->group = raster_group();
+  if (mode != kDataParallel && (e.epi != kEpiTma || e.mc != 1 || e.sched != 0))
+    return WGEMM_ERR_CONFIG;
+  p->sched = e.sched;
+  if (mode == kDataParallel && e.sched == 1) {
+    p->workers = p->num_tiles;  // one cluster per tile; running clusters take the rest
+  } else if (mode == kDataParallel) {
     p->workers = std::min(p->num_tiles, max_w);
   } else if (mode == kSplitK) {
     if (splits < 1) return WGEMM_ERR_CONFIG;
@@ -356,7 +372,7 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
   KParams params;
   std::memset(&params, 0, sizeof(params));
   if ((rc = make_plan(e, M, N, K, mode, splits, mw, &params.plan)) != WGEMM_OK) return rc;
-  const int brows_a = e.bn / e.cg, rows_b = 128 * e.reps;
+  const int brows_a = e.bn / e.cg / e.mc, rows_b = 128 * e.reps;
   if (!encode_2d(&params.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
                  (uint64_t)lda * 2, kBK, (uint32_t)brows_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&params.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)K, (uint64_t)N,
@@ -370,7 +386,7 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
   params.status = st->status;
   if (params.plan.mode != kDataParallel) {
     Workspace* ws;
-    const size_t words = (size_t)params.plan.num_tiles * e.cg * params.plan.splits;
+    const size_t words = (size_t)params.plan.num_tiles * e.cg * e.mc * params.plan.splits;
     if ((rc = workspace(dev, stream, words, &ws)) != WGEMM_OK) return rc;
     params.flags = ws->flags;
     params.flag_words = (int32_t)(ws->bytes / sizeof(uint32_t));
@@ -615,7 +631,7 @@ int run_noalloc(const uint16_t* A, const uint16_t* B, float* C, int M, int N, in
   if ((rc = make_plan(e, M, N, K, kSplitK, splits, mw, &params.plan)) != WGEMM_OK) return rc;
   const size_t words = (size_t)params.plan.num_tiles * e.cg * params.plan.splits;
   if (words > kNoAllocFlagWords) return WGEMM_ERR_NOALLOC_TOO_LARGE;
-  const int brows_a = e.bn / e.cg, rows_b = 128 * e.reps;
+  const int brows_a = e.bn / e.cg / e.mc, rows_b = 128 * e.reps;
   if (!encode_2d(&params.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
                  (uint64_t)lda * 2, kBK, (uint32_t)brows_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&params.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)K, (uint64_t)N,

@@ -72,6 +72,8 @@ enum WaitSite : int32_t {
   kCheckStaging = 0x35,
   kCheckFlag = 0x36,
   kCheckZero = 0x37,
+  kSiteClcEmpty = 0x41,
+  kSiteClcFull = 0x42,
 };
 
 struct KParams {
@@ -93,9 +95,14 @@ constexpr uint32_t pow2_at_least_32(uint32_t x) {
   return p;
 }
 
-template <int CG_, int REPS_, int BN_, int STAGES_, int ACC_, int EPI_>
+enum SchedMode : int { kSchedStatic = 0, kSchedClc = 1 };
+
+template <int CG_, int REPS_, int BN_, int STAGES_, int ACC_, int EPI_, int MC_ = 1,
+          int SCHED_ = kSchedStatic>
 struct Cfg {
+  static constexpr int SCHED = SCHED_;    // SchedMode
   static constexpr int CG = CG_;          // CTAs per MMA: 1, or 2 (pair)
+  static constexpr int MC = MC_;          // MMA groups per cluster sharing the A tile
   static constexpr int REPS = REPS_;      // stacked MMA atoms per CTA (C columns 128·REPS)
   static constexpr int BN = BN_;          // MMA N = C rows of a tile
   static constexpr int STAGES = STAGES_;  // ring depth
@@ -103,10 +110,16 @@ struct Cfg {
   static constexpr int EPI = EPI_;        // EpilogueMode
 
   static constexpr int kCtaCols = 128 * REPS;       // C columns per CTA
-  static constexpr int kTileCols = kCtaCols * CG;   // C columns per worker tile
+  static constexpr int kGroupCols = kCtaCols * CG;  // C columns per MMA group (CTA or pair)
+  static constexpr int kTileCols = kGroupCols * MC; // C columns per worker (cluster) tile
   static constexpr int kTileRows = BN;              // C rows per worker tile
+  static constexpr int kClusterSize = CG * MC;
   static constexpr int kArows = 128 * REPS;         // MMA-A rows (of B) per CTA stage
   static constexpr int kBrows = BN / CG;            // MMA-B rows (of A) per CTA stage
+  // With MC groups side by side along C's columns, the groups of a cluster
+  // need the same rows of A: each CTA loads 1/MC of its A slice and multicasts
+  // it to the CTA in the same position of every group.
+  static constexpr int kBrowsPart = kBrows / MC;
   static constexpr uint32_t kAbytes = kArows * 128;
   static constexpr uint32_t kBbytes = kBrows * 128;
   static constexpr uint32_t kStageBytes = kAbytes + kBbytes;
@@ -124,11 +137,19 @@ struct Cfg {
   static constexpr uint32_t kOffStages = 0;
   static constexpr uint32_t kOffEpi = STAGES * kStageBytes;
   static constexpr uint32_t kOffBars = kOffEpi + kEpiBytes;
-  static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 2;
+  // Cluster launch control: a ring of kClcDepth 16-byte responses, each with a
+  // full barrier (bytes of the response) and an empty barrier (releases of
+  // every consumer in the cluster, gathered in the cluster leader).
+  static constexpr int kClcDepth = SCHED == kSchedClc ? 4 : 0;
+  static constexpr uint32_t kClcConsumers = kClusterSize * 6 + MC;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 2 + 2 * kClcDepth;
   static constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t kOffResp = (kOffMisc + 16 + 15) / 16 * 16;
+  static constexpr uint32_t kSmemBytes = kOffResp + 16 * kClcDepth + 1024;  // + alignment slack
 
   static_assert(CG == 1 || CG == 2, "CG");
+  static_assert(MC == 1 || MC == 2, "MC");
+  static_assert(kBrowsPart % 8 == 0, "multicast part in 8-row groups");
   static_assert(REPS == 1 || REPS == 2, "REPS");
   static_assert(BN % 32 == 0 && BN % (16 * CG) == 0 && BN >= 32 && BN <= 256, "MMA N");
   static_assert(kBrows % 8 == 0, "operand rows in 8-row groups");
@@ -219,6 +240,80 @@ struct Kernel {
   __device__ static uint32_t bar_epi(uint32_t base) {
     return base + K::kOffBars + 8 * (2 * K::STAGES + 2 * K::ACC + 1);
   }
+  __device__ static uint32_t bar_clc_full(uint32_t base, int j) {
+    return base + K::kOffBars + 8 * (2 * K::STAGES + 2 * K::ACC + 2 + j);
+  }
+  __device__ static uint32_t bar_clc_empty(uint32_t base, int j) {
+    return base + K::kOffBars + 8 * (2 * K::STAGES + 2 * K::ACC + 2 + K::kClcDepth + j);
+  }
+  __device__ static uint32_t clc_resp(uint32_t base, int j) { return base + K::kOffResp + 16 * j; }
+
+  // Unit i of this CTA's worker (cluster). Static scheduling: the plan's
+  // order. Cluster launch control: unit 0 is the worker's own tile, unit
+  // i > 0 is the tile of the cluster that CLC response i−1 cancelled; the
+  // response is read once it has landed and then released to the cluster
+  // leader (`release`: one thread per consuming role; `warp_wide`: the whole
+  // warp reads, then its releasing lane arrives). False when there are no
+  // more units (or, with ok = false, when a wait gave up).
+  __device__ static bool next_unit(const KParams& p, uint32_t base, int32_t worker, int32_t i,
+                                   bool release, bool warp_wide, Unit& u, bool& ok,
+                                   volatile uint32_t* abort_flag, int32_t site) {
+    if constexpr (K::SCHED == kSchedStatic) {
+      return plan_unit(p.plan, worker, i, u);
+    } else {
+      if (i == 0) {
+        if (worker >= p.plan.num_tiles) return false;
+        plan_tile_unit(p.plan, worker, u);
+        return true;
+      }
+      const int32_t e = i - 1;
+      const int j = e % K::kClcDepth;
+      const uint32_t ph = (uint32_t)(e / K::kClcDepth) & 1u;
+      if (!wait_bar(bar_clc_full(base, j), ph, abort_flag, p.status, site)) {
+        ok = false;
+        return false;
+      }
+      uint32_t x = 0;
+      const bool got = clc_query(clc_resp(base, j), x);
+      if (warp_wide) __syncwarp();
+      if (release) mbar_arrive_cluster(mapa_shared(bar_clc_empty(base, j), 0));
+      if (!got) return false;
+      const int32_t t = (int32_t)(x / K::kClusterSize);
+      if (!WG_CHECK(p.status, t >= 0 && t < p.plan.num_tiles, kCheckPlan, t)) {
+        ok = false;
+        return false;
+      }
+      plan_tile_unit(p.plan, t, u);
+      return true;
+    }
+  }
+
+  // Cluster launch control scheduler (one thread of warp 2 in every CTA): the
+  // cluster leader asks for the next tile by cancelling a cluster that has not
+  // launched yet, the response is multicast to every CTA of the cluster, and
+  // each CTA's thread accounts the response bytes on its own full barrier.
+  // One request is in flight at a time, and none is issued after a failure.
+  __device__ static void scheduler(const KParams& p, uint32_t base, uint32_t crank,
+                                   volatile uint32_t* abort_flag) {
+    for (int32_t e = 0;; ++e) {
+      const int j = e % K::kClcDepth;
+      const uint32_t ph = (uint32_t)(e / K::kClcDepth) & 1u;
+      if (crank == 0) {
+        // Every consumer in the cluster has read the slot's previous response.
+        if (!wait_bar(bar_clc_empty(base, j), ph ^ 1, abort_flag, p.status, kSiteClcEmpty)) return;
+        fence_proxy_async_shared();
+        if constexpr (K::kClusterSize > 1) clc_try_cancel_multicast(clc_resp(base, j), bar_clc_full(base, j));
+        else clc_try_cancel(clc_resp(base, j), bar_clc_full(base, j));
+      }
+      mbar_arrive_expect_tx(bar_clc_full(base, j), 16);
+      if (!wait_bar(bar_clc_full(base, j), ph, abort_flag, p.status, kSiteClcFull)) return;
+      uint32_t x;
+      const bool got = clc_query(clc_resp(base, j), x);
+      mbar_arrive_cluster(mapa_shared(bar_clc_empty(base, j), 0));
+      if (!got) return;
+    }
+  }
+
   __device__ static uint32_t stage_a(uint32_t base, int s) {
     return base + K::kOffStages + s * K::kStageBytes;
   }
@@ -235,31 +330,56 @@ struct Kernel {
   }
 
   // ------------------------------------------------------------ producer
-  __device__ static void producer(const KParams& p, uint32_t base, uint32_t rank,
+  // CTA position in its cluster: `rank` within the MMA group (0 = the group's
+  // leader, which issues the MMAs), `grp` = the group's index in the cluster.
+  __device__ static uint32_t group_leader(uint32_t grp) { return grp * K::CG; }
+  __device__ static uint16_t same_rank_mask(uint32_t rank) {
+    uint16_t m = 0;
+#pragma unroll
+    for (int q = 0; q < K::MC; ++q) m |= (uint16_t)(1u << (q * K::CG + rank));
+    return m;
+  }
+  __device__ static uint16_t group_mask(uint32_t grp) {
+    return (uint16_t)(((1u << K::CG) - 1u) << (grp * K::CG));
+  }
+
+  __device__ static void producer(const KParams& p, uint32_t base, uint32_t rank, uint32_t grp,
                                   int32_t worker, volatile uint32_t* abort_flag) {
     uint32_t s = 0, ph = 0;
     bool ok = true;
     for (int32_t i = 0; ok; ++i) {
       Unit u;
-      if (!plan_unit(p.plan, worker, i, u)) break;
+      if (!next_unit(p, base, worker, i, true, false, u, ok, abort_flag, kSiteClcFull)) break;
       if (!unit_ok(p, u)) { ok = false; break; }
-      const int32_t b_row0 = u.tn * K::kTileCols + (int32_t)rank * K::kCtaCols;  // rows of B
-      const int32_t a_row0 = u.tm * K::kTileRows + (int32_t)rank * K::kBrows;    // rows of A
+      const int32_t b_row0 = u.tn * K::kTileCols + (int32_t)grp * K::kGroupCols +
+                             (int32_t)rank * K::kCtaCols;                     // rows of B
+      const int32_t a_row0 = u.tm * K::kTileRows + (int32_t)rank * K::kBrows +
+                             (int32_t)grp * K::kBrowsPart;                    // rows of A
       for (int32_t kb = u.kb_begin; kb < u.kb_end; ++kb) {
         if (!wait_bar(bar_empty(base, s), ph ^ 1, abort_flag, p.status, kSiteProducerEmpty)) {
           ok = false;
           break;
         }
         const uint32_t full = bar_full(base, s);
+        const uint32_t a_dst = stage_b(base, s) + grp * K::kBrowsPart * 128;
         if constexpr (K::CG == 1) {
           mbar_arrive_expect_tx(full, K::kStageBytes);
           tma_load_2d(stage_a(base, s), &p.tmB, full, kb * kBK, b_row0);
-          tma_load_2d(stage_b(base, s), &p.tmA, full, kb * kBK, a_row0);
+          if constexpr (K::MC == 1)
+            tma_load_2d(a_dst, &p.tmA, full, kb * kBK, a_row0);
+          else
+            tma_load_2d_multicast(a_dst, &p.tmA, full, kb * kBK, a_row0, same_rank_mask(rank));
         } else {
+          // Every byte that lands in either CTA of a pair is counted on the
+          // pair leader's full barrier.
           if (rank == 0) mbar_arrive_expect_tx(full, 2 * K::kStageBytes);
-          const uint32_t full_leader = mapa_shared(full, 0);
+          const uint32_t full_leader = mapa_shared(full, group_leader(grp));
           tma_load_2d_pair(stage_a(base, s), &p.tmB, full_leader, kb * kBK, b_row0);
-          tma_load_2d_pair(stage_b(base, s), &p.tmA, full_leader, kb * kBK, a_row0);
+          if constexpr (K::MC == 1)
+            tma_load_2d_pair(a_dst, &p.tmA, full_leader, kb * kBK, a_row0);
+          else
+            tma_load_2d_pair_multicast(a_dst, &p.tmA, full_leader, kb * kBK, a_row0,
+                                       same_rank_mask(rank));
         }
         if (++s == (uint32_t)K::STAGES) { s = 0; ph ^= 1; }
       }
@@ -275,13 +395,17 @@ struct Kernel {
   }
 
   // ------------------------------------------------------------ MMA issuer
-  __device__ static void mma(const KParams& p, uint32_t base, uint32_t tmem, int32_t worker,
-                             volatile uint32_t* abort_flag) {
+  __device__ static void mma(const KParams& p, uint32_t base, uint32_t tmem, uint32_t grp,
+                             int32_t worker, volatile uint32_t* abort_flag) {
+    // A stage is free once every group of the cluster has read it (other
+    // groups' multicasts write into it), so its release goes to all CTAs.
+    constexpr uint16_t kAllCtas = (uint16_t)((1u << K::kClusterSize) - 1u);
+    const uint16_t own = group_mask(grp);
     uint32_t s = 0, ph = 0, ab = 0, aph = 0;
     bool ok = true;
     for (int32_t i = 0; ok; ++i) {
       Unit u;
-      if (!plan_unit(p.plan, worker, i, u)) break;
+      if (!next_unit(p, base, worker, i, true, false, u, ok, abort_flag, kSiteClcFull)) break;
       if (!wait_bar(bar_acce(base, ab), aph ^ 1, abort_flag, p.status, kSiteMmaAccEmpty)) {
         ok = false;
         break;
@@ -310,19 +434,20 @@ struct Kernel {
                             (kb > u.kb_begin || j > 0) ? 1u : 0u);
           }
         }
-        if constexpr (K::CG == 1) umma_commit(bar_empty(base, s));
-        else umma_commit_pair_multicast(bar_empty(base, s), 0x3);
+        if constexpr (K::CG == 1 && K::MC == 1) umma_commit(bar_empty(base, s));
+        else if constexpr (K::CG == 1) umma_commit_multicast(bar_empty(base, s), kAllCtas);
+        else umma_commit_pair_multicast(bar_empty(base, s), kAllCtas);
         if (++s == (uint32_t)K::STAGES) { s = 0; ph ^= 1; }
       }
       if (!ok) break;
       if constexpr (K::CG == 1) umma_commit(bar_accf(base, ab));
-      else umma_commit_pair_multicast(bar_accf(base, ab), 0x3);
+      else umma_commit_pair_multicast(bar_accf(base, ab), own);
       if (++ab == (uint32_t)K::ACC) { ab = 0; aph ^= 1; }
     }
     if (!ok) {
       // Let the MMAs already issued finish before TMEM is freed.
       if constexpr (K::CG == 1) umma_commit(bar_drain(base));
-      else umma_commit_pair_multicast(bar_drain(base), 0x3);
+      else umma_commit_pair_multicast(bar_drain(base), own);
       wait_bar(bar_drain(base), 0, abort_flag, p.status, kSiteMmaDrain);
     }
   }
@@ -347,7 +472,7 @@ struct Kernel {
   template <int NBB>
   __device__ static void drain(const KParams& p, uint32_t base, uint8_t* smem, uint32_t tmem,
                                uint32_t tatom, int c0, int32_t col_warp, int32_t row0, bool add,
-                               uint32_t stage_base, bool release, uint32_t ab) {
+                               uint32_t stage_base, bool release, uint32_t ab, uint32_t grp) {
     const uint32_t lane = threadIdx.x % 32;
     const int32_t M = p.plan.M, N = p.plan.N;
     const int64_t ldc = p.ldc;
@@ -369,7 +494,7 @@ struct Kernel {
       __syncwarp();
       if (lane == 0) {
         if constexpr (K::CG == 1) mbar_arrive(bar_acce(base, ab));
-        else mbar_arrive_cluster(mapa_shared(bar_acce(base, ab), 0));
+        else mbar_arrive_cluster(mapa_shared(bar_acce(base, ab), group_leader(grp)));
       }
     }
     if (!live) return;
@@ -435,21 +560,26 @@ struct Kernel {
   // ------------------------------------------------------------ epilogue
   // 128 threads (warps 4..7); warp q = warp % 4 reads TMEM lanes 32q..32q+31.
   __device__ static void epilogue(const KParams& p, uint32_t base, uint8_t* smem, uint32_t tmem,
-                                  uint32_t rank, int32_t worker, volatile uint32_t* abort_flag) {
+                                  uint32_t rank, uint32_t grp, int32_t worker,
+                                  volatile uint32_t* abort_flag) {
+    const uint32_t crank = grp * K::CG + rank;  // rank in the cluster
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t q = warp & 3;
     bool ok = true;
     uint32_t sync_phase = 0;
 
     if constexpr (K::EPI == kEpiTma) {
-      if (p.plan.mode == kSplitK) ok = zero_slices(p, base, rank, worker, sync_phase, abort_flag);
+      if (p.plan.mode == kSplitK)
+        ok = zero_slices(p, base, rank, grp, worker, sync_phase, abort_flag);
     }
 
     uint32_t ab = 0, aph = 0;
     const uint32_t stage_base = base + K::kOffEpi + q * 2 * K::kEpiSlotBytes;
     for (int32_t i = 0; ok; ++i) {
       Unit u;
-      if (!plan_unit(p.plan, worker, i, u)) break;
+      bool got = next_unit(p, base, worker, i, lane == 0, true, u, ok, abort_flag, kSiteClcFull);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!got || !ok) break;
       if (!wait_bar(bar_accf(base, ab), aph, abort_flag, p.status, kSiteEpiAccFull)) {
         ok = false;
         break;
@@ -457,22 +587,23 @@ struct Kernel {
       __syncwarp();
       tcgen05_fence_after();
       if (!unit_ok(p, u)) { ok = false; break; }
-      const int32_t col_cta = u.tn * K::kTileCols + (int32_t)rank * K::kCtaCols;
+      const int32_t col_cta =
+          u.tn * K::kTileCols + (int32_t)grp * K::kGroupCols + (int32_t)rank * K::kCtaCols;
       const int32_t row0 = u.tm * K::kTileRows;
       const bool add = u.kind == kUnitAddAfterOwner || u.kind == kUnitAddAfterZero;
       if constexpr (K::EPI == kEpiTma) {
         if (add && lane == 0) {
           if (u.kind == kUnitAddAfterOwner) {
-            ok = WG_CHECK(p.status, (int32_t)(u.tile * K::CG + rank) < p.flag_words, kCheckFlag,
+            ok = WG_CHECK(p.status, (int32_t)(u.tile * K::kClusterSize + crank) < p.flag_words, kCheckFlag,
                           u.tile) &&
-                 wait_flag(p.flags + (u.tile * K::CG + rank), p.epoch, abort_flag, p.status,
+                 wait_flag(p.flags + (u.tile * K::kClusterSize + crank), p.epoch, abort_flag, p.status,
                            kSiteEpiFlagOwner);
           } else {
             for (int32_t s = 0; s < p.plan.splits && ok; ++s)
               ok = WG_CHECK(p.status,
-                            (int32_t)((u.tile * K::CG + rank) * p.plan.splits + s) < p.flag_words,
+                            (int32_t)((u.tile * K::kClusterSize + crank) * p.plan.splits + s) < p.flag_words,
                             kCheckFlag, u.tile) &&
-                   wait_flag(p.flags + ((u.tile * K::CG + rank) * p.plan.splits + s), p.epoch,
+                   wait_flag(p.flags + ((u.tile * K::kClusterSize + crank) * p.plan.splits + s), p.epoch,
                              abort_flag, p.status, kSiteEpiFlagZero);
           }
           // The flag's acquire covers generic writes; order them before the
@@ -496,10 +627,10 @@ struct Kernel {
 #pragma unroll 1
         for (int bi = 0; bi < kFull; ++bi)
           drain<NB>(p, base, smem, tmem, tacc + r * K::BN, bi * NB, col_warp, row0, add,
-                    stage_base, last_atom && kRem == 0 && bi == kFull - 1, ab);
+                    stage_base, last_atom && kRem == 0 && bi == kFull - 1, ab, grp);
         if constexpr (kRem > 0)
           drain<kRem>(p, base, smem, tmem, tacc + r * K::BN, kFull * NB, col_warp, row0, add,
-                      stage_base, last_atom, ab);
+                      stage_base, last_atom, ab, grp);
       }
       if constexpr (K::EPI == kEpiTma) {
         if (u.kind == kUnitStoreRaise) {
@@ -511,10 +642,10 @@ struct Kernel {
           }
           if (!epi_sync(base, sync_phase, abort_flag, p.status)) { ok = false; break; }
           if (threadIdx.x == 128 &&
-              WG_CHECK(p.status, (int32_t)(u.tile * K::CG + rank) < p.flag_words, kCheckFlag,
+              WG_CHECK(p.status, (int32_t)(u.tile * K::kClusterSize + crank) < p.flag_words, kCheckFlag,
                        u.tile)) {
             fence_acq_rel_gpu();
-            st_release_gpu(p.flags + (u.tile * K::CG + rank), p.epoch);
+            st_release_gpu(p.flags + (u.tile * K::kClusterSize + crank), p.epoch);
           }
         }
       }
@@ -528,9 +659,10 @@ struct Kernel {
 
   // Split-K: before any unit of this worker runs, zero this CTA's share of
   // every tile slice it owns and raise the slice's flag.
-  __device__ static bool zero_slices(const KParams& p, uint32_t base, uint32_t rank,
+  __device__ static bool zero_slices(const KParams& p, uint32_t base, uint32_t rank, uint32_t grp,
                                      int32_t worker, uint32_t& sync_phase,
                                      volatile uint32_t* abort_flag) {
+    const uint32_t crank = grp * K::CG + rank;  // rank in the cluster
     const int32_t M = p.plan.M, N = p.plan.N;
     const int64_t ldc = p.ldc;
     const int32_t t = (int32_t)threadIdx.x - 128;  // 0..127
@@ -542,7 +674,8 @@ struct Kernel {
       const int32_t row_begin = u.tm * K::kTileRows + r0;
       int32_t row_end = u.tm * K::kTileRows + r1;
       if (row_end > M) row_end = M;
-      const int32_t col_begin = u.tn * K::kTileCols + (int32_t)rank * K::kCtaCols;
+      const int32_t col_begin =
+          u.tn * K::kTileCols + (int32_t)grp * K::kGroupCols + (int32_t)rank * K::kCtaCols;
       int32_t col_end = col_begin + K::kCtaCols;
       if (col_end > N) col_end = N;
       if (row_begin >= row_end || col_begin >= col_end) continue;
@@ -565,7 +698,7 @@ struct Kernel {
       for (int32_t i = 0;; ++i) {
         Unit u;
         if (!plan_unit(p.plan, worker, i, u)) break;
-        const int32_t fi = (u.tile * K::CG + rank) * p.plan.splits + u.split;
+        const int32_t fi = (u.tile * K::kClusterSize + crank) * p.plan.splits + u.split;
         if (WG_CHECK(p.status, fi < p.flag_words, kCheckFlag, fi))
           st_release_gpu(p.flags + fi, p.epoch);
       }
@@ -581,8 +714,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t warp = threadIdx.x / 32;
-  const uint32_t rank = K::CG == 2 ? (cluster_ctarank() & 1u) : 0u;
-  const int32_t worker = (int32_t)(blockIdx.x / K::CG);
+  const uint32_t crank = K::kClusterSize > 1 ? cluster_ctarank() : 0u;
+  const uint32_t rank = crank % K::CG;  // position in the MMA group (0 = leader)
+  const uint32_t grp = crank / K::CG;   // MMA group in the cluster
+  const int32_t worker = (int32_t)(blockIdx.x / K::kClusterSize);
 
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + K::kOffMisc);
   volatile uint32_t* tmem_slot = misc;
@@ -594,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     if (K::EPI == kEpiTma) prefetch_tensormap(&p.tmC);
     for (int s = 0; s < K::STAGES; ++s) {
       mbar_init(Kernel<K>::bar_full(base, s), 1);
-      mbar_init(Kernel<K>::bar_empty(base, s), 1);
+      mbar_init(Kernel<K>::bar_empty(base, s), K::MC);  // one release per MMA group
     }
     for (int a = 0; a < K::ACC; ++a) {
       mbar_init(Kernel<K>::bar_accf(base, a), 1);
@@ -602,6 +737,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     }
     mbar_init(Kernel<K>::bar_drain(base), 1);
     mbar_init(Kernel<K>::bar_epi(base), 4);
+    for (int j = 0; j < K::kClcDepth; ++j) {
+      mbar_init(Kernel<K>::bar_clc_full(base, j), 1);
+      mbar_init(Kernel<K>::bar_clc_empty(base, j), K::kClcConsumers);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -610,25 +749,30 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     tmem_relinquish<K::CG>();
   }
   tcgen05_fence_before();
-  if constexpr (K::CG == 2) cluster_sync();
+  if constexpr (K::kClusterSize > 1) cluster_sync();
   else __syncthreads();
   tcgen05_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (elect_one()) Kernel<K>::producer(p, base, rank, worker, abort_flag);
+    if (elect_one()) Kernel<K>::producer(p, base, rank, grp, worker, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
     if (rank == 0) {
-      if (elect_one()) Kernel<K>::mma(p, base, tmem, worker, abort_flag);
+      if (elect_one()) Kernel<K>::mma(p, base, tmem, grp, worker, abort_flag);
+      __syncwarp();
+    }
+  } else if (warp == 2) {
+    if constexpr (K::SCHED == kSchedClc) {
+      if (elect_one()) Kernel<K>::scheduler(p, base, crank, abort_flag);
       __syncwarp();
     }
   } else if (warp >= 4) {
-    Kernel<K>::epilogue(p, base, smem, tmem, rank, worker, abort_flag);
+    Kernel<K>::epilogue(p, base, smem, tmem, rank, grp, worker, abort_flag);
   }
 
   tcgen05_fence_before();
-  if constexpr (K::CG == 2) cluster_sync();
+  if constexpr (K::kClusterSize > 1) cluster_sync();
   else __syncthreads();
   if (warp == 1) {
     tcgen05_fence_after();

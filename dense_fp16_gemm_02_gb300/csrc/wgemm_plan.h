@@ -48,8 +48,8 @@ struct Plan {
   int32_t mode;         // PlanMode
   int32_t splits;       // split-K ways (1 otherwise)
   int32_t group;        // raster group (tile rows per group)
-  int32_t workers;      // persistent workers in the grid
-  int32_t pad_;
+  int32_t workers;      // persistent workers in the grid (clusters launched, with CLC)
+  int32_t sched;        // 0: static stride; 1: cluster launch control (tiles taken at run time)
   int64_t total_iters;  // stream-K: num_tiles · kblocks
 };
 
@@ -71,10 +71,31 @@ WG_PLAN_HD void plan_tile_coords(const Plan& p, int32_t t, int32_t& tm, int32_t&
   const int32_t local = t - g * per_group;
   tm = first_m + local % gm;
   tn = local / gm;
+  // With cluster launch control the tiles of a group run in serpentine order:
+  // every other column of the group walks its rows bottom-up, so consecutive
+  // tiles stay adjacent (and share operand panels) across column boundaries.
+  if (p.sched == 1 && (tn & 1)) tm = first_m + (gm - 1 - local % gm);
 }
 
-// The i-th unit of worker w; false when w has no i-th unit.
+// The data-parallel unit of tile t (its whole K range).
+WG_PLAN_HD void plan_tile_unit(const Plan& p, int32_t t, Unit& u) {
+  u.tile = t;
+  plan_tile_coords(p, t, u.tm, u.tn);
+  u.kb_begin = 0;
+  u.kb_end = p.kblocks;
+  u.kind = kUnitStore;
+  u.split = 0;
+}
+
+// The i-th unit of worker w; false when w has no i-th unit. With cluster
+// launch control a worker's first unit is its own tile and the rest are only
+// known at run time, so this lists just the first.
 WG_PLAN_HD bool plan_unit(const Plan& p, int32_t w, int32_t i, Unit& u) {
+  if (p.sched == 1) {
+    if (i > 0 || w >= p.num_tiles) return false;
+    plan_tile_unit(p, w, u);
+    return true;
+  }
   if (p.mode == kStreamK) {
     const int64_t T = p.total_iters, P = p.workers;
     const int64_t b = (T * w) / P, e = (T * (w + 1)) / P;
@@ -107,12 +128,7 @@ WG_PLAN_HD bool plan_unit(const Plan& p, int32_t w, int32_t i, Unit& u) {
     return true;
   }
   if (idx >= p.num_tiles) return false;
-  u.tile = (int32_t)idx;
-  plan_tile_coords(p, u.tile, u.tm, u.tn);
-  u.kb_begin = 0;
-  u.kb_end = p.kblocks;
-  u.kind = kUnitStore;
-  u.split = 0;
+  plan_tile_unit(p, (int32_t)idx, u);
   return true;
 }
 

@@ -62,11 +62,16 @@ def test_data_parallel_covers_each_tile_once(lib, M, N, K, workers):
 
 
 def tma_configs(lib):
-    return [i for i, n in enumerate(wgemm.config_names()) if n.endswith("_tma")]
+    """Configurations that run split-K and stream-K (TMA epilogue, no A multicast)."""
+    return [i for i, n in enumerate(wgemm.config_names()) if n.endswith("_tma") and "m2_" not in n]
 
 
 def direct_configs(lib):
     return [i for i, n in enumerate(wgemm.config_names()) if n.endswith("_direct")]
+
+
+def multicast_configs(lib):
+    return [i for i, n in enumerate(wgemm.config_names()) if "m2_" in n]
 
 
 def coverage(units, tm, tn, kb):
@@ -189,6 +194,13 @@ def test_split_k_zero_slices_partition_rows(lib, M, N, K, S):
                 r0, r1 = min(s * per, tile_rows), min((s + 1) * per, tile_rows)
                 covered += list(range(r0, r1))
             assert covered == list(range(tile_rows))
+
+
+def test_multicast_configs_are_data_parallel_only(lib):
+    for cfg in multicast_configs(lib):
+        for mode, s in ((SPLIT, 4), (STREAM, 1)):
+            assert lib.wgemm_debug_plan(1024, 1024, 4096, cfg, mode, s, 38, None, 0, None,
+                                        None) == -6
 
 
 def test_direct_epilogue_configs_reject_split_modes(lib):
