@@ -72,6 +72,7 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+uint32_t g_debug_wait_skew = 0;  // see wgemm_debug_set_flag_wait_skew
 
 bool env_log() {
   static const bool on = [] {
@@ -391,6 +392,7 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
     params.flags = ws->flags;
     params.flag_words = (int32_t)(ws->bytes / sizeof(uint32_t));
     params.epoch = ++ws->epoch;
+    params.wait_skew = g_debug_wait_skew;
   }
   if (env_log())
     std::fprintf(stderr, "wgemm: %dx%dx%d config %s mode %d splits %d workers %d tiles %d\n", M, N,
@@ -527,6 +529,13 @@ int wgemm_release_workspace(void) {
       ++it;
     }
   }
+  return WGEMM_OK;
+}
+
+int wgemm_debug_set_flag_wait_skew(int skew) {
+  if (skew < 0) return WGEMM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_debug_wait_skew = (uint32_t)skew;
   return WGEMM_OK;
 }
 

@@ -74,6 +74,8 @@ enum WaitSite : int32_t {
   kCheckZero = 0x37,
   kSiteClcEmpty = 0x41,
   kSiteClcFull = 0x42,
+  kSiteAbortLoads = 0x51,
+  kSiteAbortClc = 0x52,
 };
 
 struct KParams {
@@ -87,6 +89,8 @@ struct KParams {
   uint32_t epoch;
   int32_t flag_words;  // words the flag array holds
   DeviceStatus* status;
+  uint32_t wait_skew;  // added to the epoch the flag waits expect (0; tests use 1)
+  int32_t pad2_;
 };
 
 constexpr uint32_t pow2_at_least_32(uint32_t x) {
@@ -200,6 +204,22 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
   }
 }
 
+// Bounded wait used after an abort: waits for this CTA's own operations in
+// flight (copies, responses) to land before the CTA exits, ignoring the
+// abort flag; gives up after the same time limit.
+__device__ __forceinline__ bool wait_bar_final(uint32_t bar, uint32_t parity, DeviceStatus* st,
+                                               int32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) {
+      record_error(st, -5, site, parity);
+      return false;
+    }
+  }
+}
+
 // Bounded wait until the flag word has reached `epoch` (monotone, wrap-safe).
 __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch,
                                           volatile uint32_t* abort_flag, DeviceStatus* st,
@@ -306,7 +326,11 @@ struct Kernel {
         else clc_try_cancel(clc_resp(base, j), bar_clc_full(base, j));
       }
       mbar_arrive_expect_tx(bar_clc_full(base, j), 16);
-      if (!wait_bar(bar_clc_full(base, j), ph, abort_flag, p.status, kSiteClcFull)) return;
+      if (!wait_bar(bar_clc_full(base, j), ph, abort_flag, p.status, kSiteClcFull)) {
+        // Aborted with a response possibly in flight: let it land here first.
+        wait_bar_final(bar_clc_full(base, j), ph, p.status, kSiteAbortClc);
+        return;
+      }
       uint32_t x;
       const bool got = clc_query(clc_resp(base, j), x);
       mbar_arrive_cluster(mapa_shared(bar_clc_empty(base, j), 0));
@@ -346,6 +370,7 @@ struct Kernel {
   __device__ static void producer(const KParams& p, uint32_t base, uint32_t rank, uint32_t grp,
                                   int32_t worker, volatile uint32_t* abort_flag) {
     uint32_t s = 0, ph = 0;
+    uint32_t fills = 0;  // stages filled so far
     bool ok = true;
     for (int32_t i = 0; ok; ++i) {
       Unit u;
@@ -381,15 +406,25 @@ struct Kernel {
             tma_load_2d_pair_multicast(a_dst, &p.tmA, full_leader, kb * kBK, a_row0,
                                        same_rank_mask(rank));
         }
+        ++fills;
         if (++s == (uint32_t)K::STAGES) { s = 0; ph ^= 1; }
       }
     }
-    // Tail: wait until the MMA has released every stage this CTA filled, so
-    // that no commit aimed at this CTA's barriers is still in flight at exit.
     if (ok) {
+      // Tail: wait until the MMA has released every stage this CTA filled, so
+      // that no commit aimed at this CTA's barriers is still in flight at exit.
       for (int j = 0; j < K::STAGES; ++j) {
         if (!wait_bar(bar_empty(base, s), ph ^ 1, abort_flag, p.status, kSiteProducerTail)) break;
         if (++s == (uint32_t)K::STAGES) { s = 0; ph ^= 1; }
+      }
+    } else if (rank == 0) {
+      // Aborted: let the loads already issued land before the CTA (and, in a
+      // pair, its peer, which waits at the final cluster barrier) can exit.
+      // The leader's full barrier counts the bytes of both CTAs of the pair.
+      for (uint32_t x = 0; x < (uint32_t)K::STAGES && x < fills; ++x) {
+        const uint32_t last = x + (uint32_t)K::STAGES * ((fills - 1 - x) / (uint32_t)K::STAGES);
+        wait_bar_final(bar_full(base, x), (last / (uint32_t)K::STAGES) & 1u, p.status,
+                       kSiteAbortLoads);
       }
     }
   }
@@ -596,14 +631,15 @@ struct Kernel {
           if (u.kind == kUnitAddAfterOwner) {
             ok = WG_CHECK(p.status, (int32_t)(u.tile * K::kClusterSize + crank) < p.flag_words, kCheckFlag,
                           u.tile) &&
-                 wait_flag(p.flags + (u.tile * K::kClusterSize + crank), p.epoch, abort_flag, p.status,
+                 wait_flag(p.flags + (u.tile * K::kClusterSize + crank), p.epoch + p.wait_skew, abort_flag, p.status,
                            kSiteEpiFlagOwner);
           } else {
             for (int32_t s = 0; s < p.plan.splits && ok; ++s)
               ok = WG_CHECK(p.status,
                             (int32_t)((u.tile * K::kClusterSize + crank) * p.plan.splits + s) < p.flag_words,
                             kCheckFlag, u.tile) &&
-                   wait_flag(p.flags + ((u.tile * K::kClusterSize + crank) * p.plan.splits + s), p.epoch,
+                   wait_flag(p.flags + ((u.tile * K::kClusterSize + crank) * p.plan.splits + s),
+                             p.epoch + p.wait_skew,
                              abort_flag, p.status, kSiteEpiFlagZero);
           }
           // The flag's acquire covers generic writes; order them before the

@@ -175,6 +175,16 @@ int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16_t* B, floa
  * order; returns the number of units (or a negative error), writing at most
  * `max_units`. Also writes the tile shape (rows, cols) of the configuration.
  */
+/*
+ * Fault-path test hook: from the next call on, the split-K and stream-K
+ * kernels wait for flags to reach their call's epoch + `skew` instead of the
+ * epoch. A skew of 1 is a value no CTA ever writes, so the flag waits run out
+ * their time limit (2 s), record WGEMM_ERR_DEVICE_TIMEOUT in the device status
+ * word and return; the kernel tears down normally. 0 (the default) restores
+ * normal operation. Returns WGEMM_OK, or WGEMM_ERR_INVALID_ARG for skew < 0.
+ */
+int wgemm_debug_set_flag_wait_skew(int skew);
+
 uint64_t wgemm_debug_smem_desc(uint32_t smem_addr);
 uint32_t wgemm_debug_idesc(int M, int N);
 uint32_t wgemm_debug_sw128_offset(uint32_t row, uint32_t k);

@@ -167,6 +167,33 @@ def test_repeated_calls_share_flag_workspace():
     assert wgemm.wgemm_workspace_bytes() > 0
 
 
+def test_device_timeout_is_reported_and_context_survives():
+    # Failure detection without a GPU fault: the split-K waiters are told to
+    # wait for a flag value that nothing writes. Their bounded waits run out
+    # (2 s), the kernel records the timeout and tears down normally; the host
+    # reads it from the status word, and the next call works.
+    lib = wgemm.load()
+    M, N, K = 256, 512, 640
+    A, B = inputs.gemm_operands(M, N, K, seed=8, kind="int")
+    dA, dB = upload(A), upload(B)
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    h = torch.cuda.current_stream().cuda_stream
+    cid = wgemm.config_id("g2_512x256_s4_a1_tma")
+    assert lib.wgemm_debug_set_flag_wait_skew(1) == 0
+    try:
+        rc = wgemm.wgemm_f16f32_config(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, K, K,
+                                       N, cid, SPLIT, 2, h)
+        assert rc == 0
+        assert wgemm.wgemm_check(h) == -5
+        err = wgemm.wgemm_last_device_error()
+        assert err["code"] == -5 and err["site"] == 0x23  # epilogue, split-K flag wait
+    finally:
+        assert lib.wgemm_debug_set_flag_wait_skew(0) == 0
+    assert lib.wgemm_debug_set_flag_wait_skew(-1) == -1
+    C = run(A, B, K, config="g2_512x256_s4_a1_tma", mode=SPLIT, splits=2)
+    assert_exact(C.cpu().numpy().astype(np.float64), oracle.gemm_f64(A, B), "after timeout")
+
+
 # ---------------------------------------------------------------- edge cases
 
 
