@@ -150,6 +150,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of a list of floats over all ranks (identity with
+    one process). Every rank's timed region is bracketed by barriers, so the
+    slowest rank's time is the job's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_value(flops_per_rank_step: float, world: int, step_ms: float) -> float:
+    """Whole-job throughput in TFLOP/s: every rank's flops over the slowest time."""
+    return world * flops_per_rank_step / (step_ms * 1e-3) / 1e12
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -295,11 +313,8 @@ def run_ours(args):
     times = np.array([[e0.elapsed_time(e1) for (e0, e1) in ev] for ev in per_step_events])  # ms
     step_ms = float(np.median(times.sum(axis=1)))
     flops = np.array([2.0 * M * N * K for (M, N, K) in shapes])
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = world * flops.sum() / (step_ms * 1e-3) / 1e12
+    step_ms = max_over_ranks([step_ms], dev)[0]
+    value = job_value(float(flops.sum()), world, step_ms)
     peak_tflops, peak_hbm, peak_src = peaks()
 
     # Per-shape report, and the configuration each call ran.
@@ -356,11 +371,7 @@ def run_ours(args):
             tot += e0.elapsed_time(e1)
         if s > 0:  # the first pass warms the copy engines
             e2e_ms.append(tot)
-    e2e_step_ms = statistics.median(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_step_ms = float(t.item())
+    e2e_step_ms = max_over_ranks([statistics.median(e2e_ms)], dev)[0]
     h2d = sum(2 * (M * K + N * K) for (M, N, K) in shapes)
     d2h = sum(4 * M * N for (M, N, K) in shapes)
 
@@ -394,7 +405,7 @@ def run_ours(args):
                 "traffic_shape": shape_name(dom["shape"]),
             },
             "cpu_baseline": cpu,
-            "e2e": {"value": round(world * float(flops.sum()) / (e2e_step_ms * 1e-3) / 1e12, 2),
+            "e2e": {"value": round(job_value(float(flops.sum()), world, e2e_step_ms), 2),
                     "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": gpu_launches,
             "clocks": clocks.summary(),
