@@ -400,6 +400,7 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
                  params.plan.num_tiles);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(e, params.plan.workers, stream, attr);
+  if (e.cg * e.mc == 1) cfg.numAttrs = 0;  // no cluster: a plain launch
   void* args[] = {&params};
   if (cudaLaunchKernelExC(&cfg, e.func, args) != cudaSuccess) {
     cudaGetLastError();

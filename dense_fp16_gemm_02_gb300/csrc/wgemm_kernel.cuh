@@ -367,10 +367,63 @@ struct Kernel {
     return (uint16_t)(((1u << K::CG) - 1u) << (grp * K::CG));
   }
 
+  // Loads k-block `kb` of a unit into stage s and accounts its bytes.
+  __device__ static void load_stage(const KParams& p, uint32_t base, uint32_t s, int32_t kb,
+                                    int32_t b_row0, int32_t a_row0, uint32_t rank, uint32_t grp) {
+    const uint32_t full = bar_full(base, s);
+    const uint32_t a_dst = stage_b(base, s) + grp * K::kBrowsPart * 128;
+    if constexpr (K::CG == 1) {
+      mbar_arrive_expect_tx(full, K::kStageBytes);
+      tma_load_2d(stage_a(base, s), &p.tmB, full, kb * kBK, b_row0);
+      if constexpr (K::MC == 1)
+        tma_load_2d(a_dst, &p.tmA, full, kb * kBK, a_row0);
+      else
+        tma_load_2d_multicast(a_dst, &p.tmA, full, kb * kBK, a_row0, same_rank_mask(rank));
+    } else {
+      // Every byte that lands in either CTA of a pair is counted on the
+      // pair leader's full barrier.
+      if (rank == 0) mbar_arrive_expect_tx(full, 2 * K::kStageBytes);
+      const uint32_t full_leader = mapa_shared(full, group_leader(grp));
+      tma_load_2d_pair(stage_a(base, s), &p.tmB, full_leader, kb * kBK, b_row0);
+      if constexpr (K::MC == 1)
+        tma_load_2d_pair(a_dst, &p.tmA, full_leader, kb * kBK, a_row0);
+      else
+        tma_load_2d_pair_multicast(a_dst, &p.tmA, full_leader, kb * kBK, a_row0,
+                                   same_rank_mask(rank));
+    }
+  }
+
+  // Kernels without a cluster start filling the ring as soon as the barriers
+  // exist, before the CTA-wide set-up barrier and the TMEM allocation: the
+  // thread that initialised the barriers loads the first unit's first
+  // min(STAGES, k-blocks) stages (all empty at that point). Returns how many.
+  __device__ static uint32_t prefill(const KParams& p, uint32_t base, int32_t worker) {
+    if constexpr (K::kClusterSize != 1) {
+      return 0;
+    } else {
+      Unit u;
+      bool have;
+      if constexpr (K::SCHED == kSchedClc) {
+        have = worker < p.plan.num_tiles;
+        if (have) plan_tile_unit(p.plan, worker, u);
+      } else {
+        have = plan_unit(p.plan, worker, 0, u);
+      }
+      if (!have || !unit_ok(p, u)) return 0;
+      const int32_t b_row0 = u.tn * K::kTileCols, a_row0 = u.tm * K::kTileRows;
+      uint32_t n = 0;
+      for (int32_t kb = u.kb_begin; kb < u.kb_end && n < (uint32_t)K::STAGES; ++kb, ++n)
+        load_stage(p, base, n, kb, b_row0, a_row0, 0, 0);
+      return n;
+    }
+  }
+
   __device__ static void producer(const KParams& p, uint32_t base, uint32_t rank, uint32_t grp,
-                                  int32_t worker, volatile uint32_t* abort_flag) {
-    uint32_t s = 0, ph = 0;
-    uint32_t fills = 0;  // stages filled so far
+                                  int32_t worker, uint32_t prefilled,
+                                  volatile uint32_t* abort_flag) {
+    // The first `prefilled` stages of unit 0 were loaded before set-up.
+    uint32_t s = prefilled % (uint32_t)K::STAGES, ph = prefilled / (uint32_t)K::STAGES;
+    uint32_t fills = prefilled;  // stages filled so far
     bool ok = true;
     for (int32_t i = 0; ok; ++i) {
       Unit u;
@@ -380,32 +433,12 @@ struct Kernel {
                              (int32_t)rank * K::kCtaCols;                     // rows of B
       const int32_t a_row0 = u.tm * K::kTileRows + (int32_t)rank * K::kBrows +
                              (int32_t)grp * K::kBrowsPart;                    // rows of A
-      for (int32_t kb = u.kb_begin; kb < u.kb_end; ++kb) {
+      for (int32_t kb = u.kb_begin + (i == 0 ? (int32_t)prefilled : 0); kb < u.kb_end; ++kb) {
         if (!wait_bar(bar_empty(base, s), ph ^ 1, abort_flag, p.status, kSiteProducerEmpty)) {
           ok = false;
           break;
         }
-        const uint32_t full = bar_full(base, s);
-        const uint32_t a_dst = stage_b(base, s) + grp * K::kBrowsPart * 128;
-        if constexpr (K::CG == 1) {
-          mbar_arrive_expect_tx(full, K::kStageBytes);
-          tma_load_2d(stage_a(base, s), &p.tmB, full, kb * kBK, b_row0);
-          if constexpr (K::MC == 1)
-            tma_load_2d(a_dst, &p.tmA, full, kb * kBK, a_row0);
-          else
-            tma_load_2d_multicast(a_dst, &p.tmA, full, kb * kBK, a_row0, same_rank_mask(rank));
-        } else {
-          // Every byte that lands in either CTA of a pair is counted on the
-          // pair leader's full barrier.
-          if (rank == 0) mbar_arrive_expect_tx(full, 2 * K::kStageBytes);
-          const uint32_t full_leader = mapa_shared(full, group_leader(grp));
-          tma_load_2d_pair(stage_a(base, s), &p.tmB, full_leader, kb * kBK, b_row0);
-          if constexpr (K::MC == 1)
-            tma_load_2d_pair(a_dst, &p.tmA, full_leader, kb * kBK, a_row0);
-          else
-            tma_load_2d_pair_multicast(a_dst, &p.tmA, full_leader, kb * kBK, a_row0,
-                                       same_rank_mask(rank));
-        }
+        load_stage(p, base, s, kb, b_row0, a_row0, rank, grp);
         ++fills;
         if (++s == (uint32_t)K::STAGES) { s = 0; ph ^= 1; }
       }
@@ -759,6 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   volatile uint32_t* tmem_slot = misc;
   volatile uint32_t* abort_flag = misc + 1;
 
+  uint32_t prefilled = 0;  // meaningful in thread 0, the producer
   if (threadIdx.x == 0) {
     prefetch_tensormap(&p.tmA);
     prefetch_tensormap(&p.tmB);
@@ -779,6 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     }
     *abort_flag = 0;
     fence_mbarrier_init();
+    prefilled = Kernel<K>::prefill(p, base, worker);
   }
   if (warp == 1) {
     tmem_alloc<K::CG>(smem_addr(misc), K::kTmemCols);
@@ -791,7 +826,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (elect_one()) Kernel<K>::producer(p, base, rank, grp, worker, abort_flag);
+    // Thread 0 initialised the barriers and prefilled the ring, so it produces.
+    if (threadIdx.x == 0) Kernel<K>::producer(p, base, rank, grp, worker, prefilled, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
     if (rank == 0) {
