@@ -28,6 +28,11 @@ if os.environ.get("WGEMM_CHECKED") == "1":
     FLAGS.append("-DWGEMM_CHECKED=1")
     BUILD = os.path.join(HERE, "_build_checked")
     LIB = os.path.join(BUILD, "libwgemm.so")
+# WGEMM_TRACE=1 builds the timeline-tracing variant (dense_fp16_gemm_02_gb300/_build_trace).
+if os.environ.get("WGEMM_TRACE") == "1":
+    FLAGS.append("-DWGEMM_TRACE=1")
+    BUILD = os.path.join(HERE, "_build_trace")
+    LIB = os.path.join(BUILD, "libwgemm.so")
 
 
 def _headers() -> list[str]:

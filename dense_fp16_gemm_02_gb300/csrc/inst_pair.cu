@@ -9,6 +9,7 @@ const KernelEntry kEntriesPair[] = {
     WG_ENTRY("g2_256x256_s6_a2_tma", 2, 1, 256, 6, 2, kEpiTma),
     WG_ENTRY("g2_256x256_s6_a2_direct", 2, 1, 256, 6, 2, kEpiDirect),
     WG_ENTRY("g2_256x224_s6_a2_tma", 2, 1, 224, 6, 2, kEpiTma),
+    WG_ENTRY("g2_256x224_s7_a2_direct", 2, 1, 224, 7, 2, kEpiDirect),
     WG_ENTRY("g2_256x192_s6_a2_tma", 2, 1, 192, 6, 2, kEpiTma),
     WG_ENTRY("g2_256x192_s8_a2_direct", 2, 1, 192, 8, 2, kEpiDirect),
     WG_ENTRY("g2_256x160_s8_a2_direct", 2, 1, 160, 8, 2, kEpiDirect),

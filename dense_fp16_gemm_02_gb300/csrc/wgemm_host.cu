@@ -73,6 +73,8 @@ DeviceState g_dev[kMaxDevices];
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 uint32_t g_debug_wait_skew = 0;  // see wgemm_debug_set_flag_wait_skew
+uint64_t* g_debug_trace = nullptr;  // see wgemm_debug_set_trace
+int g_debug_trace_ctas = 0;
 
 bool env_log() {
   static const bool on = [] {
@@ -385,6 +387,8 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
   params.C = C;
   params.ldc = ldc;
   params.status = st->status;
+  params.trace = g_debug_trace;
+  params.trace_ctas = g_debug_trace_ctas;
   if (params.plan.mode != kDataParallel) {
     Workspace* ws;
     const size_t words = (size_t)params.plan.num_tiles * e.cg * e.mc * params.plan.splits;
@@ -532,6 +536,16 @@ int wgemm_release_workspace(void) {
   }
   return WGEMM_OK;
 }
+
+int wgemm_debug_set_trace(uint64_t* device_buffer, int ctas) {
+  if (ctas < 0 || (ctas > 0 && !device_buffer)) return WGEMM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_debug_trace = ctas > 0 ? device_buffer : nullptr;
+  g_debug_trace_ctas = ctas;
+  return WGEMM_OK;
+}
+
+int wgemm_debug_trace_build(void) { return WGEMM_TRACE; }
 
 int wgemm_debug_set_flag_wait_skew(int skew) {
   if (skew < 0) return WGEMM_ERR_INVALID_ARG;

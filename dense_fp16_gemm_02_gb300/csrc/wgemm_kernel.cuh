@@ -90,8 +90,33 @@ struct KParams {
   int32_t flag_words;  // words the flag array holds
   DeviceStatus* status;
   uint32_t wait_skew;  // added to the epoch the flag waits expect (0; tests use 1)
-  int32_t pad2_;
+  int32_t trace_ctas;  // CTAs the trace buffer holds (trace builds only)
+  uint64_t* trace;     // per-CTA event timestamps (trace builds only), else null
 };
+
+// Timeline trace (builds with -DWGEMM_TRACE=1): %globaltimer at fixed points
+// of each CTA's life, kTraceEvents per CTA, written by one thread per event.
+#ifndef WGEMM_TRACE
+#define WGEMM_TRACE 0
+#endif
+enum TraceEvent : int {
+  kTrEntry = 0,        // kernel entry (thread 0)
+  kTrSetUp = 1,        // after the set-up barrier (thread 0)
+  kTrFirstData = 2,    // MMA thread: first stage landed
+  kTrLastCommit = 3,   // MMA thread: last accumulator committed
+  kTrEpiFirst = 4,     // epilogue warp 4: first accumulator full
+  kTrEpiDone = 5,      // epilogue warp 4: last unit written
+  kTrExit = 6,         // after the teardown barrier (thread 0)
+  kTrUnits = 7,        // number of units this CTA ran (a count, not a time)
+  kTraceEvents = 8,
+};
+__device__ __forceinline__ void trace_event(const KParams& p, int ev, uint64_t value = 0) {
+  if (WGEMM_TRACE && p.trace != nullptr && (int32_t)blockIdx.x < p.trace_ctas) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    p.trace[(size_t)blockIdx.x * kTraceEvents + ev] = ev == kTrUnits ? value : t;
+  }
+}
 
 constexpr uint32_t pow2_at_least_32(uint32_t x) {
   uint32_t p = 32;
@@ -396,8 +421,10 @@ struct Kernel {
   // Kernels without a cluster start filling the ring as soon as the barriers
   // exist, before the CTA-wide set-up barrier and the TMEM allocation: the
   // thread that initialised the barriers loads the first unit's first
-  // min(STAGES, k-blocks) stages (all empty at that point). Returns how many.
-  __device__ static uint32_t prefill(const KParams& p, uint32_t base, int32_t worker) {
+  // min(STAGES, k-blocks) stages (all empty at that point) and returns how
+  // many. (Doing the same for a pair's leader measured no gain.)
+  __device__ static uint32_t prefill(const KParams& p, uint32_t base, int32_t worker,
+                                     uint32_t rank, uint32_t grp) {
     if constexpr (K::kClusterSize != 1) {
       return 0;
     } else {
@@ -410,10 +437,11 @@ struct Kernel {
         have = plan_unit(p.plan, worker, 0, u);
       }
       if (!have || !unit_ok(p, u)) return 0;
-      const int32_t b_row0 = u.tn * K::kTileCols, a_row0 = u.tm * K::kTileRows;
+      const int32_t b_row0 = u.tn * K::kTileCols + (int32_t)rank * K::kCtaCols;
+      const int32_t a_row0 = u.tm * K::kTileRows + (int32_t)rank * K::kBrows;
       uint32_t n = 0;
       for (int32_t kb = u.kb_begin; kb < u.kb_end && n < (uint32_t)K::STAGES; ++kb, ++n)
-        load_stage(p, base, n, kb, b_row0, a_row0, 0, 0);
+        load_stage(p, base, n, kb, b_row0, a_row0, rank, grp);
       return n;
     }
   }
@@ -490,6 +518,7 @@ struct Kernel {
           ok = false;
           break;
         }
+        if (WGEMM_TRACE && i == 0 && kb == u.kb_begin) trace_event(p, kTrFirstData);
         tcgen05_fence_after();
         const uint32_t sa = stage_a(base, s), sb = stage_b(base, s);
 #pragma unroll
@@ -510,6 +539,7 @@ struct Kernel {
       if (!ok) break;
       if constexpr (K::CG == 1) umma_commit(bar_accf(base, ab));
       else umma_commit_pair_multicast(bar_accf(base, ab), own);
+      if (WGEMM_TRACE) trace_event(p, kTrLastCommit);
       if (++ab == (uint32_t)K::ACC) { ab = 0; aph ^= 1; }
     }
     if (!ok) {
@@ -539,14 +569,15 @@ struct Kernel {
   // batch's TMEM reads are complete.
   template <int NBB>
   __device__ static void drain(const KParams& p, uint32_t base, uint8_t* smem, uint32_t tmem,
-                               uint32_t tatom, int c0, int32_t col_warp, int32_t row0, bool add,
-                               uint32_t stage_base, bool release, uint32_t ab, uint32_t grp) {
+                               uint32_t tatom, int c0, int nb, int32_t col_warp, int32_t row0,
+                               bool add, uint32_t stage_base, bool release, uint32_t ab,
+                               uint32_t grp) {
     const uint32_t lane = threadIdx.x % 32;
     const int32_t M = p.plan.M, N = p.plan.N;
     const int64_t ldc = p.ldc;
     bool live = col_warp < N && row0 + c0 * 32 < M;  // warp-uniform
     live = live && WG_CHECK(p.status,
-                            (tatom & 0xFFFFu) - (tmem & 0xFFFFu) + (c0 + NBB) * 32u <= K::kTmemCols,
+                            (tatom & 0xFFFFu) - (tmem & 0xFFFFu) + (c0 + nb) * 32u <= K::kTmemCols,
                             kCheckTmemLd, tatom);
     uint32_t v[NBB][32];
     // tcgen05.ld / wait::ld are .sync.aligned: the whole warp must execute
@@ -554,7 +585,8 @@ struct Kernel {
     __syncwarp();
     if (live) {
 #pragma unroll
-      for (int b = 0; b < NBB; ++b) tmem_ld_32x32b_x32(tatom + (c0 + b) * 32, v[b]);
+      for (int b = 0; b < NBB; ++b)
+        if (b < nb) tmem_ld_32x32b_x32(tatom + (c0 + b) * 32, v[b]);
       tmem_ld_wait();
     }
     if (release) {
@@ -571,6 +603,7 @@ struct Kernel {
       if (col < N) {
 #pragma unroll
         for (int b = 0; b < NBB; ++b) {
+          if (b >= nb) break;
           const int32_t row_c = row0 + (c0 + b) * 32;
           float* dst = p.C + (int64_t)row_c * ldc + col;
           if (WGEMM_CHECKED) {
@@ -598,7 +631,7 @@ struct Kernel {
       // writes them out with TMA stores or reduce-adds; TMA clips what lies
       // outside M × N.
       if (!WG_CHECK(p.status,
-                    stage_base - base + NBB * K::kEpiSlotBytes <= K::kOffBars &&
+                    stage_base - base + nb * K::kEpiSlotBytes <= K::kOffBars &&
                         stage_base - base >= K::kOffEpi,
                     kCheckStaging, stage_base - base))
         return;
@@ -606,6 +639,7 @@ struct Kernel {
       __syncwarp();
 #pragma unroll
       for (int b = 0; b < NBB; ++b) {
+        if (b >= nb) break;
         float* sp = reinterpret_cast<float*>(smem + (stage_base - base) + b * K::kEpiSlotBytes);
 #pragma unroll
         for (int e = 0; e < 32; ++e) sp[e * 32 + lane] = __uint_as_float(v[b][e]);
@@ -615,6 +649,7 @@ struct Kernel {
       if (lane == 0) {
 #pragma unroll
         for (int b = 0; b < NBB; ++b) {
+          if (b >= nb) break;
           const uint32_t sbuf = stage_base + b * K::kEpiSlotBytes;
           const int32_t row_c = row0 + (c0 + b) * 32;
           if (add) tma_reduce_add_2d(&p.tmC, sbuf, col_warp, row_c);
@@ -653,6 +688,7 @@ struct Kernel {
         break;
       }
       __syncwarp();
+      if (WGEMM_TRACE && i == 0 && threadIdx.x == 128) trace_event(p, kTrEpiFirst);
       tcgen05_fence_after();
       if (!unit_ok(p, u)) { ok = false; break; }
       const int32_t col_cta =
@@ -687,19 +723,19 @@ struct Kernel {
       // paid once per batch; a shorter batch takes the remainder of an atom.
       constexpr int kChunks = K::BN / 32;
       constexpr int NB = K::kEpiBatch;
-      constexpr int kFull = kChunks / NB, kRem = kChunks % NB;
       const uint32_t tacc = tmem + ((q * 32u) << 16) + ab * K::kAccCols;
 #pragma unroll 1
       for (int r = 0; r < K::REPS; ++r) {
         const int32_t col_warp = col_cta + r * 128 + (int32_t)q * 32;
         const bool last_atom = r == K::REPS - 1;
 #pragma unroll 1
-        for (int bi = 0; bi < kFull; ++bi)
-          drain<NB>(p, base, smem, tmem, tacc + r * K::BN, bi * NB, col_warp, row0, add,
-                    stage_base, last_atom && kRem == 0 && bi == kFull - 1, ab, grp);
-        if constexpr (kRem > 0)
-          drain<kRem>(p, base, smem, tmem, tacc + r * K::BN, kFull * NB, col_warp, row0, add,
-                      stage_base, last_atom, ab, grp);
+        for (int c0 = 0; c0 < kChunks; c0 += NB) {
+          // The last batch of an atom may be short (kChunks not a multiple of
+          // NB); one register array of NB chunks serves every batch.
+          const int nb = kChunks - c0 < NB ? kChunks - c0 : NB;
+          drain<NB>(p, base, smem, tmem, tacc + r * K::BN, c0, nb, col_warp, row0, add,
+                    stage_base, last_atom && c0 + nb == kChunks, ab, grp);
+        }
       }
       if constexpr (K::EPI == kEpiTma) {
         if (u.kind == kUnitStoreRaise) {
@@ -724,7 +760,9 @@ struct Kernel {
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
     }
+    if (WGEMM_TRACE && threadIdx.x == 128) trace_event(p, kTrEpiDone);
   }
+
 
   // Split-K: before any unit of this worker runs, zero this CTA's share of
   // every tile slice it owns and raise the slice's flag.
@@ -794,6 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
 
   uint32_t prefilled = 0;  // meaningful in thread 0, the producer
   if (threadIdx.x == 0) {
+    if (WGEMM_TRACE) trace_event(p, kTrEntry);
     prefetch_tensormap(&p.tmA);
     prefetch_tensormap(&p.tmB);
     if (K::EPI == kEpiTma) prefetch_tensormap(&p.tmC);
@@ -813,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     }
     *abort_flag = 0;
     fence_mbarrier_init();
-    prefilled = Kernel<K>::prefill(p, base, worker);
+    if constexpr (K::kClusterSize == 1) prefilled = Kernel<K>::prefill(p, base, worker, rank, grp);
   }
   if (warp == 1) {
     tmem_alloc<K::CG>(smem_addr(misc), K::kTmemCols);
@@ -824,6 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   else __syncthreads();
   tcgen05_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (WGEMM_TRACE && threadIdx.x == 0) trace_event(p, kTrSetUp);
 
   if (warp == 0) {
     // Thread 0 initialised the barriers and prefilled the ring, so it produces.
@@ -850,6 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     tcgen05_fence_after();
     tmem_dealloc<K::CG>(tmem, K::kTmemCols);
   }
+  if (WGEMM_TRACE && threadIdx.x == 0) trace_event(p, kTrExit);
 }
 
 // K == 0: C := 0 (the empty sum).

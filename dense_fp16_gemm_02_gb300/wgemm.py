@@ -70,6 +70,10 @@ def load():
         lib.wgemm_workspace_bytes.restype = ctypes.c_size_t
         lib.wgemm_release_workspace.argtypes = []
         lib.wgemm_release_workspace.restype = i
+        lib.wgemm_debug_set_trace.argtypes = [p, i]
+        lib.wgemm_debug_set_trace.restype = i
+        lib.wgemm_debug_trace_build.argtypes = []
+        lib.wgemm_debug_trace_build.restype = i
         lib.wgemm_debug_set_flag_wait_skew.argtypes = [i]
         lib.wgemm_debug_set_flag_wait_skew.restype = i
         lib.wgemm_debug_smem_desc.argtypes = [u32]

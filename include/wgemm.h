@@ -185,6 +185,19 @@ int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16_t* B, floa
  */
 int wgemm_debug_set_flag_wait_skew(int skew);
 
+/*
+ * Timeline tracing (a library built with WGEMM_TRACE=1 only; other builds
+ * ignore the buffer). wgemm_debug_set_trace: from the next call on, CTA b of
+ * each GEMM kernel writes %globaltimer values (ns) into
+ * device_buffer[b·8 + e] for b < ctas, at e = 0 kernel entry, 1 after the
+ * set-up barrier, 2 first stage landed (MMA thread), 3 last accumulator
+ * committed, 4 epilogue's first accumulator full, 5 epilogue done, 6 after the
+ * teardown barrier. The caller owns the device buffer; ctas = 0 turns tracing
+ * off. wgemm_debug_trace_build: 1 in a tracing build, else 0.
+ */
+int wgemm_debug_set_trace(uint64_t* device_buffer, int ctas);
+int wgemm_debug_trace_build(void);
+
 uint64_t wgemm_debug_smem_desc(uint32_t smem_addr);
 uint32_t wgemm_debug_idesc(int M, int N);
 uint32_t wgemm_debug_sw128_offset(uint32_t row, uint32_t k);
