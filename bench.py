@@ -178,14 +178,20 @@ def dist_setup(args):
 _B_CACHE = {}
 
 
-def oracle_sample_rate(shapes, seconds_per_shape: float, nthreads: int = 0):
-    """Times the CPU oracle on a row sample of every shape; returns
-    (TFLOP/s over the sample, threads, description, seconds of oracle work)."""
+def oracle_sample_rate(shapes, seconds_total: float, nthreads: int = 0):
+    """Times the CPU oracle on a row sample of every shape, about
+    `seconds_total` of oracle work in all (a shape that finishes in full hands
+    its unused share to the larger ones); returns (TFLOP/s over the sample,
+    threads, description, seconds of oracle work)."""
     import oracle
     from dense_fp16_gemm_02_gb300 import inputs
     total_flops, total_t, desc = 0.0, 0.0, []
     threads = nthreads or oracle.hardware_threads()
-    for (M, N, K) in shapes:
+    order = sorted(range(len(shapes)), key=lambda i: shapes[i][0] * shapes[i][1] * shapes[i][2])
+    left = seconds_total
+    for n_done, i in enumerate(order):
+        M, N, K = shapes[i]
+        budget = left / (len(order) - n_done)
         if (N, K) not in _B_CACHE:
             _B_CACHE[(N, K)] = inputs.matrix(N, K, 1000, 1)
         B = _B_CACHE[(N, K)]
@@ -195,13 +201,14 @@ def oracle_sample_rate(shapes, seconds_per_shape: float, nthreads: int = 0):
         t0 = time.perf_counter()
         oracle.gemm_f64(A, B, nthreads=threads)
         dt = max(time.perf_counter() - t0, 1e-4)
-        rows = int(min(M, max(rows, rows * seconds_per_shape / dt)))
+        rows = int(min(M, max(rows, rows * budget / dt)))
         if rows > threads:
             rows -= rows % threads
         A = inputs.matrix(rows, K, 1000, 0)
         t0 = time.perf_counter()
         oracle.gemm_f64(A, B, nthreads=threads)
         dt = time.perf_counter() - t0
+        left -= dt
         total_flops += 2.0 * rows * N * K
         total_t += dt
         desc.append(f"{rows} of {M} rows of {shape_name((M, N, K))}")
@@ -213,7 +220,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     shapes = WORKLOADS[args.workload]
-    budget = max(0.5, min(20.0, 60.0 / (len(shapes) * max(1, args.steps + args.warmup))))
+    budget = max(0.5 * len(shapes), min(60.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_sample_rate(shapes, budget / 4)
     vals, last = [], None
@@ -379,7 +386,7 @@ def run_ours(args):
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            rate, cores, sample, secs = oracle_sample_rate(shapes, args.cpu_seconds / len(shapes))
+            rate, cores, sample, secs = oracle_sample_rate(shapes, args.cpu_seconds)
             cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                    "sample": f"{sample} ({secs:.1f} s of oracle work)"}
         line = {
