@@ -204,39 +204,111 @@ const TunedRow kTuned[] = {
 #include "wgemm_tuned.inc"
 };
 
-Choice choose(int M, int N, int K, int workers_hint, bool c_tma_ok) {
+// Measured cost of each data-parallel configuration (tune.py --rates):
+// a call of `waves` full waves over `kblocks` k-blocks takes about
+// t0 + waves · (a + b · kblocks) microseconds. Two fits per configuration:
+// operand rows that start on 32-byte sectors, and rows 16 bytes off them
+// (every 128-byte TMA row then touches five L2 sectors instead of four,
+// which costs tiles with more operand bytes per flop up to 40%).
+struct RateRow {
+  const char* config;
+  double t0_us, a_us, b_us;     // rows on 32-byte sectors
+  double t0u_us, au_us, bu_us;  // rows 16 bytes off
+};
+
+const RateRow kRates[] = {
+#include "wgemm_rates.inc"
+    {nullptr, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0},
+};
+
+const RateRow* rate_of(const char* name) {
+  for (const RateRow& r : kRates)
+    if (r.config && std::strcmp(r.config, name) == 0) return &r;
+  return nullptr;
+}
+
+// Operand rows of both A and B start on 32-byte sectors.
+bool rows_on_sectors(int lda, int ldb) { return lda % 16 == 0 && ldb % 16 == 0; }
+
+// Predicted microseconds of a configuration and K-decomposition from the
+// measured rates, with `workers` co-resident workers; < 0 if not modelled.
+double predict_us(const KernelEntry& e, int M, int N, int K, bool aligned, int mode, int splits,
+                  int workers) {
+  const RateRow* r = rate_of(e.name);
+  if (!r || workers <= 0) return -1.0;
+  const double t0 = aligned ? r->t0_us : r->t0u_us;
+  const double a = aligned ? r->a_us : r->au_us;
+  const double b = aligned ? r->b_us : r->bu_us;
+  const int64_t tiles = (int64_t)((M + e.tile_rows - 1) / e.tile_rows) *
+                        ((N + e.tile_cols - 1) / e.tile_cols);
+  const int64_t kblocks = (K + kBK - 1) / kBK;
+  if (mode == kSplitK) {
+    const int64_t units = tiles * splits;
+    const int64_t waves = (units + workers - 1) / workers;
+    // Zeroing C and one reduce-add of every partial tile in L2 (measured
+    // ≈3 µs plus ≈0.5 µs per split on GB300).
+    return t0 + 3.0 + 0.5 * splits + waves * a +
+           waves * b * (double)((kblocks + splits - 1) / splits);
+  }
+  if (mode == kStreamK) {
+    const int64_t per_worker = (tiles * kblocks + workers - 1) / workers;
+    // The owner's store and flag, then the other units' reduce-adds, one
+    // after the other (measured ≈6 µs on GB300).
+    return t0 + 6.0 + a + b * (double)per_worker;
+  }
+  const int64_t waves = (tiles + workers - 1) / workers;
+  return t0 + waves * (a + b * (double)kblocks);
+}
+
+Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma_ok) {
+  // The table was measured with rows on 32-byte sectors.
+  const bool aligned = rows_on_sectors(lda, ldb);
   for (const TunedRow& r : kTuned) {
-    if (r.M == M && r.N == N && r.K == K) {
+    if (aligned && r.M == M && r.N == N && r.K == K) {
       const int id = find_config(r.config);
       const bool tma = std::strstr(r.config, "_tma") != nullptr;
       if (id >= 0 && (c_tma_ok || !tma)) return {id, r.mode, r.splits};
     }
   }
-  if (!c_tma_ok) {
-    // C rows not 16-byte aligned: no TMA on C, so a direct-store epilogue
-    // and no K decomposition.
-    const int64_t mn = (int64_t)M * N;
-    if (mn >= (int64_t)1536 * 1536)
-      return {find_config("g2_256x256_s6_a2_direct"), kDataParallel, 1};
-    return {find_config("g2_256x64_s10_a2_direct"), kDataParallel, 1};
+  // Not in the table: the configuration and K-decomposition with the least
+  // predicted time from the measured per-configuration rates. A K split is
+  // taken only when it predicts at least 20% less time than the best
+  // data-parallel choice: its fix-up cost (zeroing, reduce-adds in L2, flag
+  // waits) varies more from shape to shape than one fitted constant.
+  const auto& es = registry().entries;
+  Choice best{-1, kDataParallel, 1}, best_split{-1, kDataParallel, 1};
+  double best_us = 0.0, best_split_us = 0.0;
+  for (int id = 0; id < (int)es.size(); ++id) {
+    const KernelEntry& e = *es[id];
+    if (e.epi == kEpiTma && !c_tma_ok) continue;
+    const int w = max_workers(st, id);
+    if (w <= 0) continue;
+    auto consider = [&](int mode, int splits) {
+      const double us = predict_us(e, M, N, K, aligned, mode, splits, w);
+      Choice& c = mode == kDataParallel ? best : best_split;
+      double& c_us = mode == kDataParallel ? best_us : best_split_us;
+      if (us >= 0.0 && (c.config < 0 || us < c_us)) {
+        c = {id, mode, splits};
+        c_us = us;
+      }
+    };
+    consider(kDataParallel, 1);
+    const bool ksplit = e.epi == kEpiTma && e.mc == 1 && e.sched == 0;
+    const int64_t tiles = (int64_t)((M + e.tile_rows - 1) / e.tile_rows) *
+                          ((N + e.tile_cols - 1) / e.tile_cols);
+    const int kblocks = (K + kBK - 1) / kBK;
+    if (ksplit && kblocks >= 32 && tiles < w) {
+      consider(kStreamK, 1);
+      for (int sp = 2; sp <= 16 && sp <= kblocks / 8 && tiles * sp <= w; ++sp)
+        consider(kSplitK, sp);
+    }
   }
-  const int64_t mn = (int64_t)M * N;
-  const int kblocks = (K + kBK - 1) / kBK;
-  // Few output tiles and a long K: split K (tiles far fewer than workers) or
-  // stream-K (tiles below one wave).
-  const int big = find_config("g2_512x256_s4_a1_tma");
-  const int64_t tiles_big = (int64_t)((M + 255) / 256) * ((N + 511) / 512);
-  if (kblocks >= 64 && tiles_big * 4 <= workers_hint) {
-    int s = (int)std::max<int64_t>(1, workers_hint / std::max<int64_t>(1, tiles_big));
-    s = std::min(s, kblocks / 8);
-    if (s >= 2) return {big, kSplitK, s};
-  }
-  const int sk = find_config("g2_512x128_s4_a2_tma");
-  const int64_t tiles_sk = (int64_t)((M + 127) / 128) * ((N + 511) / 512);
-  if (kblocks >= 64 && tiles_sk < workers_hint) return {sk, kStreamK, 1};
-  if (mn >= (int64_t)4096 * 4096) return {big, kDataParallel, 1};
-  if (mn >= (int64_t)1536 * 1536) return {find_config("g2_256x256_s6_a2_tma"), kDataParallel, 1};
-  return {find_config("g2_256x64_s10_a2_direct"), kDataParallel, 1};
+  if (best_split.config >= 0 && (best.config < 0 || best_split_us < 0.8 * best_us))
+    return best_split;
+  if (best.config >= 0) return best;
+  // No rates compiled in: a plain fallback.
+  if (!c_tma_ok) return {find_config("g2_256x256_s6_a2_direct"), kDataParallel, 1};
+  return {find_config("g2_256x256_s6_a2_tma"), kDataParallel, 1};
 }
 
 // Tile rows per raster group (WGEMM_RASTER_GROUP overrides the default 8).
@@ -352,9 +424,7 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
   const auto& es = registry().entries;
   const bool c_ok = c_tma_ok(C, ldc);
   if (config_id < 0) {
-    // Workers of the pair configurations bound the split / stream-K choice.
-    const int hint = st->sm_count / 2;
-    Choice c = choose(M, N, K, hint, c_ok);
+    Choice c = choose(*st, M, N, K, lda, ldb, c_ok);
     config_id = c.config;
     mode = c.mode;
     splits = c.splits;
@@ -363,7 +433,7 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
   const KernelEntry& e = *es[config_id];
   if (e.epi == kEpiTma && !c_ok) return WGEMM_ERR_ALIGNMENT;
   if (mode < 0) {
-    Choice c = choose(M, N, K, st->sm_count / 2, c_ok);
+    Choice c = choose(*st, M, N, K, lda, ldb, c_ok);
     mode = c.mode;
     splits = c.splits;
     if (mode != kDataParallel && e.epi != kEpiTma) mode = kDataParallel;
@@ -441,14 +511,15 @@ const char* wgemm_config_name(int id) {
   return (id >= 0 && id < (int)es.size()) ? es[id]->name : "";
 }
 
-int wgemm_select(int M, int N, int K, int* config_id, int* mode, int* splits) {
-  if (M < 0 || N < 0 || K < 0) return WGEMM_ERR_INVALID_ARG;
+int wgemm_select(int M, int N, int K, int lda, int ldb, int* config_id, int* mode,
+                 int* splits) {
+  if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K) return WGEMM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
   int dev;
   DeviceState* st;
   const int rc = device_state(&dev, &st);
   if (rc != WGEMM_OK) return rc;
-  Choice c = choose(M, N, K, st->sm_count / 2, true);
+  Choice c = choose(*st, M, N, K, lda, ldb, true);
   if (config_id) *config_id = c.config;
   if (mode) *mode = c.mode;
   if (splits) *splits = c.splits;
@@ -546,6 +617,25 @@ int wgemm_debug_set_trace(uint64_t* device_buffer, int ctas) {
 }
 
 int wgemm_debug_trace_build(void) { return WGEMM_TRACE; }
+
+int wgemm_debug_max_workers(int config_id) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (config_id < 0 || config_id >= (int)registry().entries.size()) return WGEMM_ERR_CONFIG;
+  int dev;
+  DeviceState* st;
+  const int rc = device_state(&dev, &st);
+  if (rc != WGEMM_OK) return rc;
+  return max_workers(*st, config_id);
+}
+
+double wgemm_debug_predict_us(int M, int N, int K, int lda, int ldb, int config_id, int mode,
+                              int splits, int workers) {
+  const auto& es = registry().entries;
+  if (config_id < 0 || config_id >= (int)es.size() || M <= 0 || N <= 0 || K <= 0 || lda < K ||
+      ldb < K)
+    return -1.0;
+  return predict_us(*es[config_id], M, N, K, rows_on_sectors(lda, ldb), mode, splits, workers);
+}
 
 int wgemm_debug_set_flag_wait_skew(int skew) {
   if (skew < 0) return WGEMM_ERR_INVALID_ARG;

@@ -3,6 +3,9 @@ K-decomposition on this GPU and records the fastest for each shape.
 
     python -m dense_fp16_gemm_02_gb300.tune --out tune.json [--shapes all]
     python -m dense_fp16_gemm_02_gb300.tune --emit tune.json   # writes csrc/wgemm_tuned.inc
+    python -m dense_fp16_gemm_02_gb300.tune --rates rates.json # per-configuration cost model
+    python -m dense_fp16_gemm_02_gb300.tune --emit-rates rates.json   # writes csrc/wgemm_rates.inc
+    python -m dense_fp16_gemm_02_gb300.tune --validate validate.json  # the rule on off-table shapes
 
 Each candidate call runs alone (L2 flushed with a 256 MiB write before it)
 and is timed with CUDA events on the launching stream; the median of the
@@ -21,6 +24,13 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 TUNED_INC = os.path.join(HERE, "csrc", "wgemm_tuned.inc")
+RATES_INC = os.path.join(HERE, "csrc", "wgemm_rates.inc")
+# Shapes outside the table, for checking the rule against an exhaustive sweep.
+OFF_TABLE = [(3000, 5000, 3000), (6144, 6144, 2048), (1000, 8000, 4096), (5000, 700, 12000),
+             (2304, 4608, 1536), (12288, 3072, 1024), (777, 1999, 5003), (4096, 1024, 8192)]
+# Shapes no constant of the rule was chosen against (checked only).
+HELD_OUT = [(2500, 7000, 2500), (6000, 4000, 3000), (1536, 6144, 6144), (10000, 10000, 2000),
+            (512, 12288, 4096), (9000, 1500, 5000)]
 
 SHAPES = {
     "all": [(1024, 1024, 1024), (1536, 1536, 1536), (2048, 2048, 2048), (3072, 1280, 2048),
@@ -128,14 +138,179 @@ def emit(json_path, inc_path=TUNED_INC):
     return inc_path
 
 
+def _time_calls(wgemm, torch, bufs, M, N, K, fn, flush, reps=7, warm=2):
+    stream = torch.cuda.current_stream()
+    times = []
+    for r in range(warm + reps):
+        flush.fill_(float(r))
+        torch.cuda._sleep(400_000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        rc = fn()
+        e1.record(stream)
+        if rc != 0:
+            return None
+        if r >= warm:
+            times.append((e0, e1))
+    torch.cuda.synchronize()
+    if wgemm.wgemm_check(stream.cuda_stream) != 0:
+        raise RuntimeError(f"device error: {wgemm.wgemm_last_device_error()}")
+    return statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in times)
+
+
+# (waves, K) points of the rate fit: the K range of most off-table calls.
+RATE_POINTS = [(1, 1024), (1, 4096), (2, 1024), (2, 4096), (3, 2048), (4, 3072)]
+
+
+def rates(out_path, points=RATE_POINTS):
+    """Per data-parallel configuration: time whole waves of tiles (as many
+    tiles per wave as co-resident workers) at several K and wave counts and
+    fit t = t0 + waves · (a + b · kblocks) by least squares; once with operand
+    rows on 32-byte sectors (pitch a multiple of 16 elements) and once with
+    rows 16 bytes off them (pitch ≡ 8 mod 16)."""
+    import numpy as np
+    import torch
+
+    sys.path.insert(0, ROOT)
+    from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
+    build.build()
+    lib = wgemm.load()
+    names = wgemm.config_names()
+    torch.cuda.set_device(0)
+    h = torch.cuda.current_stream().cuda_stream
+    flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device="cuda")
+    max_waves = max(w for w, _ in points)
+    Kmax = max(k for _, k in points)
+    pitches = {"": Kmax + 16, "u": Kmax + 8}  # the buffers hold Kmax + 16 per row
+    out = []
+    for cid, name in enumerate(names):
+        W = lib.wgemm_debug_max_workers(cid)
+        cols, rows = (int(v) for v in name.split("_")[1].split("x"))
+        tn = max(d for d in range(1, 9) if W % d == 0)
+        tm = W // tn
+        M1, N = tm * rows, tn * cols
+        A, B = inputs.gemm_operands(max_waves * M1, N, Kmax, seed=11, kind="uniform",
+                                    lda=Kmax + 16, ldb=Kmax + 16)
+        dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        C = torch.empty((max_waves * M1, N), dtype=torch.float32, device="cuda")
+        del A, B
+        print(f"# rates {name} W={W} tiles {tm}x{tn}", file=sys.stderr, flush=True)
+        row = {"config": name, "workers": W}
+        for tag, ld in pitches.items():
+            X, y = [], []
+            for waves, K in points:
+                M = waves * M1
+                call = (lambda M=M, K=K, ld=ld: wgemm.wgemm_f16f32_config(
+                    dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, ld, ld, N, cid, 0, 1,
+                    h))
+                t = _time_calls(wgemm, torch, None, M, N, K, call, flush)
+                kb = (K + 63) // 64
+                X.append([1.0, waves, waves * kb])
+                y.append(t)
+            (t0, a, b), *_ = np.linalg.lstsq(np.array(X), np.array(y), rcond=None)
+            row.update({f"t0{tag}_us": round(float(t0), 3), f"a{tag}_us": round(float(a), 3),
+                        f"b{tag}_us": round(float(b), 5),
+                        f"runs{tag}_us": [round(v, 2) for v in y]})
+        out.append(row)
+        print(json.dumps(row), flush=True)
+        del dA, dB, C
+        torch.cuda.empty_cache()
+    with open(out_path, "w") as f:
+        json.dump({"gpu": torch.cuda.get_device_name(0), "points": points, "rates": out}, f,
+                  indent=1)
+
+
+def emit_rates(json_path, inc_path=RATES_INC):
+    with open(json_path) as f:
+        d = json.load(f)
+    lines = [
+        "// Measured per-configuration rates (generated by dense_fp16_gemm_02_gb300/tune.py",
+        f"// --rates on {d.get('gpu', 'a GB300')}; do not edit by hand). {{configuration,",
+        "// t0 µs, a µs per wave, b µs per wave per k-block: rows on 32-byte sectors; the",
+        "// same three with rows 16 bytes off}.",
+    ]
+    for r in d["rates"]:
+        lines.append(f'{{"{r["config"]}", {r["t0_us"]:.3f}, {r["a_us"]:.3f}, {r["b_us"]:.5f}, '
+                     f'{r["t0u_us"]:.3f}, {r["au_us"]:.3f}, {r["bu_us"]:.5f}}},')
+    with open(inc_path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+    return inc_path
+
+
+def validate(out_path, shapes=OFF_TABLE + HELD_OUT):
+    """For shapes outside the table: the rule's own choice against the best of
+    an exhaustive sweep of configurations and K-decompositions."""
+    import torch
+
+    sys.path.insert(0, ROOT)
+    from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
+    build.build()
+    names = wgemm.config_names()
+    torch.cuda.set_device(0)
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    h = torch.cuda.current_stream().cuda_stream
+    flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device="cuda")
+    res = []
+    for (M, N, K) in shapes:
+        ld = (K + 7) // 8 * 8
+        A, B = inputs.gemm_operands(M, N, K, seed=3, kind="uniform", lda=ld, ldb=ld)
+        dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        C = torch.empty((M, (N + 3) // 4 * 4), dtype=torch.float32, device="cuda")
+        ldc = C.shape[1]
+        cid, mode, sp = wgemm.wgemm_select(M, N, K, ld, ld)
+        t_rule = _time_calls(wgemm, torch, None, M, N, K,
+                             lambda: wgemm.wgemm_f16f32(dA.data_ptr(), dB.data_ptr(),
+                                                        C.data_ptr(), M, N, K, ld, ld, ldc, h),
+                             flush)
+        best = None
+        lib = wgemm.load()
+        timed = []
+        for c2, m2, s2 in candidates(M, N, K, names, sm // 2, sm):
+            print(f"# validate {M}x{N}x{K} {names[c2]} mode {m2} splits {s2}", file=sys.stderr,
+                  flush=True)
+            t = _time_calls(wgemm, torch, None, M, N, K,
+                            lambda: wgemm.wgemm_f16f32_config(
+                                dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, ld, ld,
+                                ldc, c2, m2, s2, h), flush, reps=5)
+            if t is not None and (best is None or t < best[0]):
+                best = (t, names[c2], m2, s2)
+            if t is not None:
+                pred = lib.wgemm_debug_predict_us(M, N, K, ld, ld, c2, m2, s2,
+                                                  lib.wgemm_debug_max_workers(c2))
+                timed.append([names[c2], m2, s2, round(t, 2), round(pred, 2)])
+        row = {"shape": [M, N, K], "set": "held out" if (M, N, K) in HELD_OUT else "tuned",
+               "rule": [names[cid], mode, sp], "rule_us": round(t_rule, 2),
+               "best": [best[1], best[2], best[3]], "best_us": round(best[0], 2),
+               "rule_over_best": round(t_rule / best[0], 3),
+               "candidates": sorted(timed, key=lambda x: x[3])}
+        res.append(row)
+        print(json.dumps(row), flush=True)
+        del dA, dB, C
+        torch.cuda.empty_cache()
+    with open(out_path, "w") as f:
+        json.dump(res, f, indent=1)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--out", default="tune.json")
     ap.add_argument("--shapes", default="all")
     ap.add_argument("--emit", metavar="JSON", help="write csrc/wgemm_tuned.inc from a sweep")
+    ap.add_argument("--rates", metavar="JSON", help="measure per-configuration rates")
+    ap.add_argument("--emit-rates", metavar="JSON", help="write csrc/wgemm_rates.inc")
+    ap.add_argument("--validate", metavar="JSON", help="check the rule on off-table shapes")
     args = ap.parse_args(argv)
     if args.emit:
         print(emit(args.emit))
+        return 0
+    if args.emit_rates:
+        print(emit_rates(args.emit_rates))
+        return 0
+    if args.rates:
+        rates(args.rates)
+        return 0
+    if args.validate:
+        validate(args.validate)
         return 0
     sweep(SHAPES[args.shapes], args.out)
     return 0

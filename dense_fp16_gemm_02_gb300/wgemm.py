@@ -57,7 +57,7 @@ def load():
         lib.wgemm_num_configs.restype = i
         lib.wgemm_config_name.argtypes = [i]
         lib.wgemm_config_name.restype = ctypes.c_char_p
-        lib.wgemm_select.argtypes = [i, i, i, ctypes.POINTER(i), ctypes.POINTER(i),
+        lib.wgemm_select.argtypes = [i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i),
                                      ctypes.POINTER(i)]
         lib.wgemm_select.restype = i
         lib.wgemm_check.argtypes = [p]
@@ -74,6 +74,10 @@ def load():
         lib.wgemm_debug_set_trace.restype = i
         lib.wgemm_debug_trace_build.argtypes = []
         lib.wgemm_debug_trace_build.restype = i
+        lib.wgemm_debug_max_workers.argtypes = [i]
+        lib.wgemm_debug_max_workers.restype = i
+        lib.wgemm_debug_predict_us.argtypes = [i] * 9
+        lib.wgemm_debug_predict_us.restype = ctypes.c_double
         lib.wgemm_debug_set_flag_wait_skew.argtypes = [i]
         lib.wgemm_debug_set_flag_wait_skew.restype = i
         lib.wgemm_debug_smem_desc.argtypes = [u32]
@@ -142,9 +146,15 @@ def wgemm_f16f32_splitk_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, 
     return load().wgemm_f16f32_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, splits, stream)
 
 
-def wgemm_select(M: int, N: int, K: int) -> tuple[int, int, int]:
+def wgemm_select(M: int, N: int, K: int, lda: int | None = None,
+                 ldb: int | None = None) -> tuple[int, int, int]:
+    """(configuration id, mode, splits) that wgemm_f16f32 runs for this shape
+    and these row pitches (K when omitted)."""
+    lda = K if lda is None else lda
+    ldb = K if ldb is None else ldb
     c, m, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    rc = load().wgemm_select(M, N, K, ctypes.byref(c), ctypes.byref(m), ctypes.byref(s))
+    rc = load().wgemm_select(M, N, K, lda, ldb, ctypes.byref(c), ctypes.byref(m),
+                             ctypes.byref(s))
     if rc != WGEMM_OK:
         raise WgemmError(rc, "wgemm_select")
     return c.value, m.value, s.value

@@ -96,10 +96,19 @@ int wgemm_num_configs(void);
 const char* wgemm_config_name(int config_id);
 
 /*
- * The choice wgemm_f16f32 makes for a shape on the current device:
- * writes the configuration id, mode and splits. Returns WGEMM_OK or an error.
+ * The choice wgemm_f16f32 makes for a shape and operand row pitches (lda,
+ * ldb, in elements) on the current device: the measured per-shape table if
+ * the shape is in it and both pitches are multiples of 16 elements (rows on
+ * 32-byte sectors, as the table was measured), else the configuration and
+ * K-decomposition with the least time predicted from measured
+ * per-configuration rates (waves of tiles × per-k-block cost + fixed costs),
+ * fitted separately for rows on and off 32-byte sectors. A K split is chosen
+ * only when it predicts at least 20% less time than the best data-parallel
+ * configuration. Writes the configuration id, mode and splits (any pointer
+ * may be NULL). Returns WGEMM_OK, WGEMM_ERR_INVALID_ARG (negative size or a
+ * pitch below K) or a device error.
  */
-int wgemm_select(int M, int N, int K, int* config_id, int* mode, int* splits);
+int wgemm_select(int M, int N, int K, int lda, int ldb, int* config_id, int* mode, int* splits);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
@@ -197,6 +206,19 @@ int wgemm_debug_set_flag_wait_skew(int skew);
  */
 int wgemm_debug_set_trace(uint64_t* device_buffer, int ctas);
 int wgemm_debug_trace_build(void);
+
+/*
+ * The per-shape rule. wgemm_debug_max_workers: co-resident workers (CTAs or
+ * clusters) of a configuration on the current device (a negative status on
+ * error). wgemm_debug_predict_us: the time the rule predicts for a shape,
+ * configuration and K-decomposition with `workers` workers and operand row
+ * pitches lda, ldb, from the measured per-configuration rates compiled into
+ * the library (-1 if the configuration has none or an argument is invalid).
+ * Host arithmetic only.
+ */
+int wgemm_debug_max_workers(int config_id);
+double wgemm_debug_predict_us(int M, int N, int K, int lda, int ldb, int config_id, int mode,
+                              int splits, int workers);
 
 uint64_t wgemm_debug_smem_desc(uint32_t smem_addr);
 uint32_t wgemm_debug_idesc(int M, int N);

@@ -109,3 +109,31 @@ def test_status_strings(lib):
         s = lib.wgemm_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.wgemm_status_string(-99).decode() == "unknown status"
+
+
+def test_rule_predictions_from_measured_rates(lib):
+    """The per-shape rule's host arithmetic: every configuration has measured
+    rates, predictions grow with K and with waves of tiles, and invalid
+    arguments give -1."""
+    n = lib.wgemm_num_configs()
+    for cid in range(n):
+        name = lib.wgemm_config_name(cid).decode()
+        w = 36 if "m2_" in name else (152 if name.startswith("g1_") else 76)
+        p = lambda M, N, K, ld=None, mode=0, s=1: lib.wgemm_debug_predict_us(
+            M, N, K, ld or K, ld or K, cid, mode, s, w)
+        assert p(4096, 4096, 2048) > 0, name
+        assert p(4096, 4096, 4096) > p(4096, 4096, 2048), name
+        assert p(16384, 16384, 2048) > p(4096, 4096, 2048), name
+        assert p(4096, 4096, 2048, ld=2056) > 0, name
+        assert p(4096, 4096, 2048, ld=1024) == -1.0, name  # pitch below K
+    assert lib.wgemm_debug_predict_us(64, 64, 64, 64, 64, n, 0, 1, 76) == -1.0
+    assert lib.wgemm_debug_predict_us(64, 64, 64, 64, 64, -1, 0, 1, 76) == -1.0
+
+
+def test_rule_charges_rows_off_sectors(lib):
+    """Rows 16 bytes off 32-byte sectors cost 256-column pair tiles more than a
+    fifth more time at 3000×5000×3000 (measured), and the prediction says so."""
+    cid = wgemm.config_id("g2_256x224_s7_a2_direct")
+    on = lib.wgemm_debug_predict_us(3000, 5000, 3000, 3008, 3008, cid, 0, 1, 76)
+    off = lib.wgemm_debug_predict_us(3000, 5000, 3000, 3000, 3000, cid, 0, 1, 76)
+    assert off > 1.1 * on > 0

@@ -351,3 +351,27 @@ def test_large_compute_bound_sampled(n):
         assert_tol(Ch[rows[:64], :].astype(np.float64), ref, ref_abs, f"{n}^3 rows")
     del C
     torch.cuda.empty_cache()
+
+
+# Off-table shapes: the per-shape rule picks from the measured rates, with
+# operand pitches on and off 32-byte sectors.
+OFF_TABLE = [
+    (3000, 5000, 3000, 3000),   # rows 6000 B apart: 16 bytes off a sector
+    (777, 1999, 5003, 5008),
+    (2500, 7000, 2500, 2504),
+    (5000, 700, 12000, 12000),
+    (1000, 8000, 4096, 4096),
+]
+
+
+@pytest.mark.parametrize("M,N,K,pitch", OFF_TABLE)
+def test_off_table_rule_sampled(M, N, K, pitch):
+    cid, mode, splits = wgemm.wgemm_select(M, N, K, pitch, pitch)
+    assert 0 <= cid < wgemm.wgemm_num_configs() and mode in (0, 1, 2) and splits >= 1
+    A, B = inputs.gemm_operands(M, N, K, seed=3000 + M + N + K, kind="uniform", lda=pitch,
+                                ldb=pitch)
+    C = run(A, B, K)
+    check_sampled(A, B, C, M, N, K, "uniform", 32, 91,
+                  f"{M}x{N}x{K} pitch {pitch} via {wgemm.config_names()[cid]} mode {mode}")
+    del C
+    torch.cuda.empty_cache()
