@@ -195,13 +195,22 @@ def oracle_sample_rate(shapes, seconds_total: float, nthreads: int = 0):
         if (N, K) not in _B_CACHE:
             _B_CACHE[(N, K)] = inputs.matrix(N, K, 1000, 1)
         B = _B_CACHE[(N, K)]
-        # Calibrate on one row per thread, then size the sample to the budget.
-        rows = min(M, threads)
-        A = inputs.matrix(rows, K, 1000, 0)
-        t0 = time.perf_counter()
-        oracle.gemm_f64(A, B, nthreads=threads)
-        dt = max(time.perf_counter() - t0, 1e-4)
-        rows = int(min(M, max(rows, rows * budget / dt)))
+        # Calibrate at one and at four rows per thread (each call also decodes
+        # all of B: a fixed cost), then size the sample to the budget.
+        cal = []
+        for r in sorted({min(M, threads), min(M, 4 * threads)}):
+            A = inputs.matrix(r, K, 1000, 0)
+            t0 = time.perf_counter()
+            oracle.gemm_f64(A, B, nthreads=threads)
+            cal.append((r, time.perf_counter() - t0))
+        if len(cal) == 2:
+            (r1, t1), (r2, t2) = cal
+            per_row = max((t2 - t1) / (r2 - r1), t2 / r2 * 0.05, 1e-7)
+            fixed = max(t1 - per_row * r1, 0.0)
+        else:
+            per_row, fixed = max(cal[0][1], 1e-4) / cal[0][0], 0.0
+        rows = cal[0][0]
+        rows = int(min(M, max(rows, (budget - fixed) / per_row)))
         if rows > threads:
             rows -= rows % threads
         A = inputs.matrix(rows, K, 1000, 0)

@@ -367,7 +367,7 @@ OFF_TABLE = [
 @pytest.mark.parametrize("M,N,K,pitch", OFF_TABLE)
 def test_off_table_rule_sampled(M, N, K, pitch):
     cid, mode, splits = wgemm.wgemm_select(M, N, K, pitch, pitch)
-    assert 0 <= cid < wgemm.wgemm_num_configs() and mode in (0, 1, 2) and splits >= 1
+    assert 0 <= cid < len(wgemm.config_names()) and mode in (0, 1, 2) and splits >= 1
     A, B = inputs.gemm_operands(M, N, K, seed=3000 + M + N + K, kind="uniform", lda=pitch,
                                 ldb=pitch)
     C = run(A, B, K)
