@@ -12,6 +12,7 @@ struct KernelEntry {
   int mc;                    // MMA groups per cluster sharing the A tile
   int sched;                 // 0: static persistent grid, 1: cluster launch control
   int tile_rows, tile_cols;  // C rows / columns of one worker tile
+  int out;                   // 0: fp32 C; 1: 16-bit C (fp16 or bf16), data parallel only
   uint32_t smem_bytes;
   const void* func;          // the __global__ function (host stub)
 };
@@ -27,22 +28,31 @@ extern const KernelEntry kEntriesMulticast[];
 extern const int kNumEntriesMulticast;
 extern const KernelEntry kEntriesClc[];
 extern const int kNumEntriesClc;
+extern const KernelEntry kEntriesOut16A[];
+extern const int kNumEntriesOut16A;
+extern const KernelEntry kEntriesOut16B[];
+extern const int kNumEntriesOut16B;
 
 }  // namespace wg
 
 // Builds the entry of one configuration (only in .cu files that include the
 // kernel template). MC = MMA groups per cluster sharing the A tile; SCHED =
-// kSchedStatic or kSchedClc.
-#define WG_ENTRY_FULL(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED)                          \
+// kSchedStatic or kSchedClc; OUT = kOut32 or kOut16.
+#define WG_ENTRY_OUT(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT)                      \
   wg::KernelEntry {                                                                             \
     NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED,                                            \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED>::kTileRows,                          \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED>::kTileCols,                          \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED>::kSmemBytes,                         \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT>::kTileRows,                     \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT>::kTileCols, OUT,                \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT>::kSmemBytes,                    \
         reinterpret_cast<const void*>(                                                          \
-            &wg::wgemm_kernel<wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED>>)              \
+            &wg::wgemm_kernel<wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT>>)         \
   }
+#define WG_ENTRY_FULL(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED) \
+  WG_ENTRY_OUT(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, wg::kOut32)
 #define WG_ENTRY_MC(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC) \
   WG_ENTRY_FULL(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, wg::kSchedStatic)
 #define WG_ENTRY(NAME, CG, REPS, BN, STAGES, ACC, EPI) \
   WG_ENTRY_FULL(NAME, CG, REPS, BN, STAGES, ACC, EPI, 1, wg::kSchedStatic)
+// 16-bit C: the same configuration with "_h" appended to its name.
+#define WG_ENTRY_H(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED) \
+  WG_ENTRY_OUT(NAME "_h", CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, wg::kOut16)

@@ -11,6 +11,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <string>
 #include <utility>
 #include <vector>
 
@@ -24,12 +25,14 @@ namespace wg {
 // The per-device status word the kernels write on a failed wait.
 __device__ DeviceStatus g_device_status;
 
-__global__ void wgemm_zero_kernel(float* C, int32_t M, int32_t N, int64_t ldc) {
+__global__ void wgemm_zero_kernel(void* C, int32_t M, int32_t N, int64_t ldc,
+                                  int32_t elem_bytes) {
   const int64_t total = (int64_t)M * N;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / N, c = i - r * N;
-    C[r * ldc + c] = 0.f;
+    if (elem_bytes == 4) static_cast<float*>(C)[r * ldc + c] = 0.f;
+    else static_cast<uint16_t*>(C)[r * ldc + c] = 0;  // +0 in fp16 and in bf16
   }
 }
 
@@ -45,6 +48,8 @@ struct Registry {
     for (int i = 0; i < kNumEntriesPair2; ++i) entries.push_back(&kEntriesPair2[i]);
     for (int i = 0; i < kNumEntriesMulticast; ++i) entries.push_back(&kEntriesMulticast[i]);
     for (int i = 0; i < kNumEntriesClc; ++i) entries.push_back(&kEntriesClc[i]);
+    for (int i = 0; i < kNumEntriesOut16A; ++i) entries.push_back(&kEntriesOut16A[i]);
+    for (int i = 0; i < kNumEntriesOut16B; ++i) entries.push_back(&kEntriesOut16B[i]);
   }
 };
 
@@ -221,9 +226,17 @@ const RateRow kRates[] = {
     {nullptr, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0},
 };
 
+// A 16-bit-output configuration ("..._h") without rates of its own takes
+// those of its fp32 twin (same main loop; its epilogue writes half the bytes).
 const RateRow* rate_of(const char* name) {
   for (const RateRow& r : kRates)
     if (r.config && std::strcmp(r.config, name) == 0) return &r;
+  const size_t n = std::strlen(name);
+  if (n > 2 && std::strcmp(name + n - 2, "_h") == 0) {
+    const std::string twin(name, n - 2);
+    for (const RateRow& r : kRates)
+      if (r.config && twin == r.config) return &r;
+  }
   return nullptr;
 }
 
@@ -260,11 +273,11 @@ double predict_us(const KernelEntry& e, int M, int N, int K, bool aligned, int m
   return t0 + waves * (a + b * (double)kblocks);
 }
 
-Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma_ok) {
-  // The table was measured with rows on 32-byte sectors.
+Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma_ok, int out) {
+  // The table was measured with fp32 C and rows on 32-byte sectors.
   const bool aligned = rows_on_sectors(lda, ldb);
   for (const TunedRow& r : kTuned) {
-    if (aligned && r.M == M && r.N == N && r.K == K) {
+    if (out == 0 && aligned && r.M == M && r.N == N && r.K == K) {
       const int id = find_config(r.config);
       const bool tma = std::strstr(r.config, "_tma") != nullptr;
       if (id >= 0 && (c_tma_ok || !tma)) return {id, r.mode, r.splits};
@@ -280,7 +293,7 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
   double best_us = 0.0, best_split_us = 0.0;
   for (int id = 0; id < (int)es.size(); ++id) {
     const KernelEntry& e = *es[id];
-    if (e.epi == kEpiTma && !c_tma_ok) continue;
+    if (e.out != out || (e.epi == kEpiTma && !c_tma_ok)) continue;
     const int w = max_workers(st, id);
     if (w <= 0) continue;
     auto consider = [&](int mode, int splits) {
@@ -293,7 +306,7 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
       }
     };
     consider(kDataParallel, 1);
-    const bool ksplit = e.epi == kEpiTma && e.mc == 1 && e.sched == 0;
+    const bool ksplit = e.epi == kEpiTma && e.mc == 1 && e.sched == 0 && e.out == 0;
     const int64_t tiles = (int64_t)((M + e.tile_rows - 1) / e.tile_rows) *
                           ((N + e.tile_cols - 1) / e.tile_cols);
     const int kblocks = (K + kBK - 1) / kBK;
@@ -307,8 +320,9 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
     return best_split;
   if (best.config >= 0) return best;
   // No rates compiled in: a plain fallback.
-  if (!c_tma_ok) return {find_config("g2_256x256_s6_a2_direct"), kDataParallel, 1};
-  return {find_config("g2_256x256_s6_a2_tma"), kDataParallel, 1};
+  const char* fb = c_tma_ok ? "g2_256x256_s6_a2_tma" : "g2_256x256_s6_a2_direct";
+  if (out == 0) return {find_config(fb), kDataParallel, 1};
+  return {find_config((std::string(fb) + "_h").c_str()), kDataParallel, 1};
 }
 
 // Tile rows per raster group (WGEMM_RASTER_GROUP overrides the default 8).
@@ -321,8 +335,18 @@ int raster_group() {
   return g;
 }
 
+// Element types of the typed entry points (WGEMM_F32 / WGEMM_F16 / WGEMM_BF16).
+bool ab_type_ok(int t) { return t == WGEMM_F16 || t == WGEMM_BF16; }
+bool c_type_ok(int t) { return t == WGEMM_F32 || t == WGEMM_F16 || t == WGEMM_BF16; }
+int c_bytes(int t) { return t == WGEMM_F32 ? 4 : 2; }
+CUtensorMapDataType tma_type(int t) {
+  return t == WGEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+         : t == WGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
 int check_args(const void* A, const void* B, const void* C, int M, int N, int K, int lda, int ldb,
-               int ldc) {
+               int ldc, int c_elem_bytes = 4) {
   if (M < 0 || N < 0 || K < 0) return WGEMM_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return WGEMM_OK;
   if (!C) return WGEMM_ERR_INVALID_ARG;
@@ -333,13 +357,13 @@ int check_args(const void* A, const void* B, const void* C, int M, int N, int K,
         (lda % 8) || (ldb % 8))
       return WGEMM_ERR_ALIGNMENT;
   }
-  if (reinterpret_cast<uintptr_t>(C) & 3) return WGEMM_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(C) & (uintptr_t)(c_elem_bytes - 1)) return WGEMM_ERR_ALIGNMENT;
   return WGEMM_OK;
 }
 
 // C can be written by TMA (16-byte aligned base and row stride).
-bool c_tma_ok(const void* C, int ldc) {
-  return !(reinterpret_cast<uintptr_t>(C) & 15) && !(ldc % 4);
+bool c_tma_ok(const void* C, int ldc, int c_elem_bytes = 4) {
+  return !(reinterpret_cast<uintptr_t>(C) & 15) && !(((int64_t)ldc * c_elem_bytes) % 16);
 }
 
 // Fills the plan for a configuration; WGEMM_ERR_CONFIG if the mode cannot run.
@@ -358,7 +382,7 @@ int make_plan(const KernelEntry& e, int M, int N, int K, int mode, int splits, i
   p->mode = mode;
   p->splits = 1;
   p->group = raster_group();
-  if (mode != kDataParallel && (e.epi != kEpiTma || e.mc != 1 || e.sched != 0))
+  if (mode != kDataParallel && (e.epi != kEpiTma || e.mc != 1 || e.sched != 0 || e.out != 0))
     return WGEMM_ERR_CONFIG;
   p->sched = e.sched;
   if (mode == kDataParallel && e.sched == 1) {
@@ -406,9 +430,11 @@ int workspace(int dev, cudaStream_t stream, size_t words, Workspace** out) {
   return WGEMM_OK;
 }
 
-int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int lda, int ldb,
-        int ldc, int config_id, int mode, int splits, cudaStream_t stream) {
-  int rc = check_args(A, B, C, M, N, K, lda, ldb, ldc);
+int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, int N, int K,
+        int lda, int ldb, int ldc, int config_id, int mode, int splits, cudaStream_t stream) {
+  if (!ab_type_ok(ab_type) || !c_type_ok(c_type)) return WGEMM_ERR_INVALID_ARG;
+  const int cb = c_bytes(c_type), out = c_type == WGEMM_F32 ? 0 : 1;
+  int rc = check_args(A, B, C, M, N, K, lda, ldb, ldc, cb);
   if (rc != WGEMM_OK) return rc;
   if (M == 0 || N == 0) return WGEMM_OK;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -418,26 +444,29 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
   if (K == 0) {
     const int64_t total = (int64_t)M * N;
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)st->sm_count * 8);
-    wgemm_zero_kernel<<<blocks, 256, 0, stream>>>(C, M, N, ldc);
+    wgemm_zero_kernel<<<blocks, 256, 0, stream>>>(C, M, N, ldc, cb);
     return cudaGetLastError() == cudaSuccess ? WGEMM_OK : WGEMM_ERR_LAUNCH;
   }
   const auto& es = registry().entries;
-  const bool c_ok = c_tma_ok(C, ldc);
+  const bool c_ok = c_tma_ok(C, ldc, cb);
   if (config_id < 0) {
-    Choice c = choose(*st, M, N, K, lda, ldb, c_ok);
+    Choice c = choose(*st, M, N, K, lda, ldb, c_ok, out);
     config_id = c.config;
     mode = c.mode;
     splits = c.splits;
   }
   if (config_id < 0 || config_id >= (int)es.size()) return WGEMM_ERR_CONFIG;
   const KernelEntry& e = *es[config_id];
+  if (e.out != out) return WGEMM_ERR_CONFIG;
   if (e.epi == kEpiTma && !c_ok) return WGEMM_ERR_ALIGNMENT;
   if (mode < 0) {
-    Choice c = choose(*st, M, N, K, lda, ldb, c_ok);
+    Choice c = choose(*st, M, N, K, lda, ldb, c_ok, out);
     mode = c.mode;
     splits = c.splits;
     if (mode != kDataParallel && e.epi != kEpiTma) mode = kDataParallel;
   }
+  // 16-bit C is rounded once from the full fp32 sum: no K split.
+  if (out != 0 && mode != kDataParallel) return WGEMM_ERR_CONFIG;
   const int mw = max_workers(*st, config_id);
   if (mw < 0) return mw;
   if ((rc = encoder()) != WGEMM_OK) return rc;
@@ -446,16 +475,18 @@ int run(const uint16_t* A, const uint16_t* B, float* C, int M, int N, int K, int
   std::memset(&params, 0, sizeof(params));
   if ((rc = make_plan(e, M, N, K, mode, splits, mw, &params.plan)) != WGEMM_OK) return rc;
   const int brows_a = e.bn / e.cg / e.mc, rows_b = 128 * e.reps;
-  if (!encode_2d(&params.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
-                 (uint64_t)lda * 2, kBK, (uint32_t)brows_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&params.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)K, (uint64_t)N,
-                 (uint64_t)ldb * 2, kBK, (uint32_t)rows_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (!encode_2d(&params.tmA, tma_type(ab_type), A, (uint64_t)K, (uint64_t)M, (uint64_t)lda * 2,
+                 kBK, (uint32_t)brows_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&params.tmB, tma_type(ab_type), B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb * 2,
+                 kBK, (uint32_t)rows_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
       (e.epi == kEpiTma &&
-       !encode_2d(&params.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, (uint64_t)N, (uint64_t)M,
-                  (uint64_t)ldc * 4, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE)))
+       !encode_2d(&params.tmC, tma_type(c_type), C, (uint64_t)N, (uint64_t)M,
+                  (uint64_t)ldc * cb, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE)))
     return WGEMM_ERR_LAUNCH;
   params.C = C;
   params.ldc = ldc;
+  params.idesc = umma_idesc_f16(128u * e.cg, (uint32_t)e.bn, ab_type == WGEMM_BF16);
+  params.c_bf16 = c_type == WGEMM_BF16 ? 1 : 0;
   params.status = st->status;
   params.trace = g_debug_trace;
   params.trace_ctas = g_debug_trace_ctas;
@@ -492,16 +523,45 @@ extern "C" {
 
 int wgemm_f16f32(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C, int M, int N, int K,
                  int lda, int ldb, int ldc, wgemm_stream_t stream) {
-  return run(A, B, C, M, N, K, lda, ldb, ldc, -1, -1, 1, reinterpret_cast<cudaStream_t>(stream));
+  return run(A, B, C, WGEMM_F16, WGEMM_F32, M, N, K, lda, ldb, ldc, -1, -1, 1,
+             reinterpret_cast<cudaStream_t>(stream));
 }
 
 int wgemm_f16f32_config(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C, int M, int N, int K,
                         int lda, int ldb, int ldc, int config_id, int mode, int splits,
                         wgemm_stream_t stream) {
+  return wgemm_gemm_config(A, B, C, WGEMM_F16, WGEMM_F32, M, N, K, lda, ldb, ldc, config_id, mode,
+                           splits, stream);
+}
+
+int wgemm_gemm(const void* A, const void* B, void* C, int ab_type, int c_type, int M, int N, int K,
+               int lda, int ldb, int ldc, wgemm_stream_t stream) {
+  return run(A, B, C, ab_type, c_type, M, N, K, lda, ldb, ldc, -1, -1, 1,
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int wgemm_gemm_config(const void* A, const void* B, void* C, int ab_type, int c_type, int M, int N,
+                      int K, int lda, int ldb, int ldc, int config_id, int mode, int splits,
+                      wgemm_stream_t stream) {
   if (config_id < 0 || config_id >= (int)registry().entries.size()) return WGEMM_ERR_CONFIG;
   if (mode < -1 || mode > 2) return WGEMM_ERR_CONFIG;
-  return run(A, B, C, M, N, K, lda, ldb, ldc, config_id, mode, splits,
+  return run(A, B, C, ab_type, c_type, M, N, K, lda, ldb, ldc, config_id, mode, splits,
              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int wgemm_bf16f32(const wgemm_bf16_t* A, const wgemm_bf16_t* B, float* C, int M, int N, int K,
+                  int lda, int ldb, int ldc, wgemm_stream_t stream) {
+  return wgemm_gemm(A, B, C, WGEMM_BF16, WGEMM_F32, M, N, K, lda, ldb, ldc, stream);
+}
+
+int wgemm_f16f16(const wgemm_f16_t* A, const wgemm_f16_t* B, wgemm_f16_t* C, int M, int N, int K,
+                 int lda, int ldb, int ldc, wgemm_stream_t stream) {
+  return wgemm_gemm(A, B, C, WGEMM_F16, WGEMM_F16, M, N, K, lda, ldb, ldc, stream);
+}
+
+int wgemm_bf16bf16(const wgemm_bf16_t* A, const wgemm_bf16_t* B, wgemm_bf16_t* C, int M, int N,
+                   int K, int lda, int ldb, int ldc, wgemm_stream_t stream) {
+  return wgemm_gemm(A, B, C, WGEMM_BF16, WGEMM_BF16, M, N, K, lda, ldb, ldc, stream);
 }
 
 int wgemm_num_configs(void) { return (int)registry().entries.size(); }
@@ -511,15 +571,16 @@ const char* wgemm_config_name(int id) {
   return (id >= 0 && id < (int)es.size()) ? es[id]->name : "";
 }
 
-int wgemm_select(int M, int N, int K, int lda, int ldb, int* config_id, int* mode,
+int wgemm_select(int M, int N, int K, int lda, int ldb, int c_type, int* config_id, int* mode,
                  int* splits) {
-  if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K) return WGEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || !c_type_ok(c_type))
+    return WGEMM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
   int dev;
   DeviceState* st;
   const int rc = device_state(&dev, &st);
   if (rc != WGEMM_OK) return rc;
-  Choice c = choose(*st, M, N, K, lda, ldb, true);
+  Choice c = choose(*st, M, N, K, lda, ldb, true, c_type == WGEMM_F32 ? 0 : 1);
   if (config_id) *config_id = c.config;
   if (mode) *mode = c.mode;
   if (splits) *splits = c.splits;
@@ -646,7 +707,14 @@ int wgemm_debug_set_flag_wait_skew(int skew) {
 
 uint64_t wgemm_debug_smem_desc(uint32_t smem_addr) { return umma_smem_desc_sw128(smem_addr); }
 
-uint32_t wgemm_debug_idesc(int M, int N) { return umma_idesc_f16((uint32_t)M, (uint32_t)N); }
+uint32_t wgemm_debug_idesc(int M, int N, int bf16) {
+  return umma_idesc_f16((uint32_t)M, (uint32_t)N, bf16 != 0);
+}
+
+int wgemm_debug_config_out(int config_id) {
+  const auto& es = registry().entries;
+  return (config_id >= 0 && config_id < (int)es.size()) ? es[config_id]->out : WGEMM_ERR_CONFIG;
+}
 
 uint32_t wgemm_debug_sw128_offset(uint32_t row, uint32_t k) { return sw128_offset_f16(row, k); }
 
@@ -731,7 +799,7 @@ int run_noalloc(const uint16_t* A, const uint16_t* B, float* C, int M, int N, in
   if (K == 0) {
     const int64_t total = (int64_t)M * N;
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)st->sm_count * 8);
-    wgemm_zero_kernel<<<blocks, 256, 0, stream>>>(C, M, N, ldc);
+    wgemm_zero_kernel<<<blocks, 256, 0, stream>>>(C, M, N, ldc, 4);
     return cudaGetLastError() == cudaSuccess ? WGEMM_OK : WGEMM_ERR_LAUNCH;
   }
   const int config_id = find_config("g2_512x256_s4_a1_tma");
@@ -755,6 +823,7 @@ int run_noalloc(const uint16_t* A, const uint16_t* B, float* C, int M, int N, in
     return WGEMM_ERR_LAUNCH;
   params.C = C;
   params.ldc = ldc;
+  params.idesc = umma_idesc_f16(128u * e.cg, (uint32_t)e.bn, false);
   params.status = st->status;
   params.flags = na->flags;
   params.flag_words = (int32_t)kNoAllocFlagWords;

@@ -1,5 +1,8 @@
 // The GEMM kernel family: one warp-specialised persistent kernel, templated on
-// its tile, pair mode, ring depth, accumulator count and epilogue.
+// its tile, pair mode, ring depth, accumulator count, epilogue and C element
+// width (fp32, or a 16-bit type: fp16 or bf16, chosen at run time). The
+// operand type (fp16 or bf16, both the same) is the instruction descriptor's
+// and the tensor maps' business alone, so one kernel serves both.
 //
 // Roles ("SASS-Level Kernel Generation for Blackwell", sections "What a
 // Blackwell GEMM is" and "Writing a kernel"), 256 threads per CTA:
@@ -29,6 +32,8 @@
 // the CTA then tears down normally (TMEM freed) and exits.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -79,12 +84,14 @@ enum WaitSite : int32_t {
 };
 
 struct KParams {
-  CUtensorMap tmA;  // A (M×K fp16): the MMA's B operand, box {64, BN/CG}
-  CUtensorMap tmB;  // B (N×K fp16): the MMA's A operand, box {64, 128·REPS}
-  CUtensorMap tmC;  // C (M×N fp32): box {32, 32}, for the TMA epilogue
+  CUtensorMap tmA;  // A (M×K fp16 or bf16): the MMA's B operand, box {64, BN/CG}
+  CUtensorMap tmB;  // B (N×K, A's type): the MMA's A operand, box {64, 128·REPS}
+  CUtensorMap tmC;  // C (M×N, fp32 or 16-bit): box {32, 32}, for the TMA epilogue
   Plan plan;
-  float* C;
-  int64_t ldc;
+  void* C;          // fp32 C, or 16-bit C in 16-bit-output kernels
+  int64_t ldc;      // in elements
+  uint32_t idesc;   // tcgen05.mma instruction descriptor (operand types, M, N)
+  int32_t c_bf16;   // 16-bit-output kernels: 1 = bf16, 0 = fp16
   uint32_t* flags;  // split-K / stream-K flags (monotone epochs)
   uint32_t epoch;
   int32_t flag_words;  // words the flag array holds
@@ -126,9 +133,12 @@ constexpr uint32_t pow2_at_least_32(uint32_t x) {
 
 enum SchedMode : int { kSchedStatic = 0, kSchedClc = 1 };
 
+enum OutWidth : int { kOut32 = 0, kOut16 = 1 };
+
 template <int CG_, int REPS_, int BN_, int STAGES_, int ACC_, int EPI_, int MC_ = 1,
-          int SCHED_ = kSchedStatic>
+          int SCHED_ = kSchedStatic, int OUT_ = kOut32>
 struct Cfg {
+  static constexpr int OUT = OUT_;        // OutWidth: fp32 C, or 16-bit C (data parallel only)
   static constexpr int SCHED = SCHED_;    // SchedMode
   static constexpr int CG = CG_;          // CTAs per MMA: 1, or 2 (pair)
   static constexpr int MC = MC_;          // MMA groups per cluster sharing the A tile
@@ -154,13 +164,13 @@ struct Cfg {
   static constexpr uint32_t kStageBytes = kAbytes + kBbytes;
   static constexpr uint32_t kAccCols = REPS * BN;   // TMEM columns per accumulator
   static constexpr uint32_t kTmemCols = pow2_at_least_32(kAccCols * ACC);
-  static constexpr uint32_t kEpiSlotBytes = 32 * 32 * 4;  // one 32×32 fp32 staging tile
+  static constexpr uint32_t kCBytes = OUT == kOut16 ? 2 : 4;  // bytes per C element
+  static constexpr uint32_t kEpiSlotBytes = 32 * 32 * kCBytes;  // one 32×32 staging tile
   // TMEM chunks (32 columns each) drained per wait: 4 when storing from
   // registers, 2 when staging through shared memory (one slot per chunk).
   static constexpr int kEpiBatch = EPI == kEpiTma ? (BN / 32 >= 2 ? 2 : 1)
                                                   : (BN / 32 >= 4 ? 4 : BN / 32);
   static constexpr uint32_t kEpiBytes = EPI == kEpiTma ? 4 * kEpiBatch * kEpiSlotBytes : 0;
-  static constexpr uint32_t kIdesc = umma_idesc_f16(128 * CG, BN);
 
   // Shared-memory layout (offsets from a 1024-byte-aligned base).
   static constexpr uint32_t kOffStages = 0;
@@ -177,6 +187,7 @@ struct Cfg {
   static constexpr uint32_t kSmemBytes = kOffResp + 16 * kClcDepth + 1024;  // + alignment slack
 
   static_assert(CG == 1 || CG == 2, "CG");
+  static_assert(OUT == kOut32 || OUT == kOut16, "OUT");
   static_assert(MC == 1 || MC == 2, "MC");
   static_assert(kBrowsPart % 8 == 0, "multicast part in 8-row groups");
   static_assert(REPS == 1 || REPS == 2, "REPS");
@@ -186,6 +197,14 @@ struct Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
+
+// An fp32 accumulator value (its bits) rounded to the 16-bit C type, to
+// nearest with ties to even: bf16 or fp16.
+__device__ __forceinline__ uint16_t to_c16(uint32_t bits, bool bf16) {
+  const float f = __uint_as_float(bits);
+  return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(f))
+              : __half_as_ushort(__float2half_rn(f));
+}
 
 __device__ __forceinline__ void record_error(DeviceStatus* st, int32_t code, int32_t site,
                                              uint32_t parity) {
@@ -497,6 +516,7 @@ struct Kernel {
     // groups' multicasts write into it), so its release goes to all CTAs.
     constexpr uint16_t kAllCtas = (uint16_t)((1u << K::kClusterSize) - 1u);
     const uint16_t own = group_mask(grp);
+    const uint32_t idesc = p.idesc;
     uint32_t s = 0, ph = 0, ab = 0, aph = 0;
     bool ok = true;
     for (int32_t i = 0; ok; ++i) {
@@ -527,7 +547,7 @@ struct Kernel {
           for (int j = 0; j < kBK / 16; ++j) {
             const uint64_t adesc = umma_smem_desc_sw128(sa + r * 128 * 128 + j * 32);
             const uint64_t bdesc = umma_smem_desc_sw128(sb + j * 32);
-            umma_f16<K::CG>(d + r * K::BN, adesc, bdesc, K::kIdesc,
+            umma_f16<K::CG>(d + r * K::BN, adesc, bdesc, idesc,
                             (kb > u.kb_begin || j > 0) ? 1u : 0u);
           }
         }
@@ -598,14 +618,42 @@ struct Kernel {
       }
     }
     if (!live) return;
-    if constexpr (K::EPI == kEpiDirect) {
+    if constexpr (K::EPI == kEpiDirect && K::OUT == kOut16) {
+      const int32_t col = col_warp + (int32_t)lane;
+      if (col < N) {
+        const bool bf = p.c_bf16 != 0;
+#pragma unroll
+        for (int b = 0; b < NBB; ++b) {
+          if (b >= nb) break;
+          const int32_t row_c = row0 + (c0 + b) * 32;
+          uint16_t* dst = static_cast<uint16_t*>(p.C) + (int64_t)row_c * ldc + col;
+          if (WGEMM_CHECKED) {
+            for (int e = 0; e < 32; ++e) {
+              const int64_t off = (int64_t)(row_c + e) * ldc + col;
+              if (row_c + e < M &&
+                  WG_CHECK(p.status, col >= 0 && off >= 0 && off < (int64_t)(M - 1) * ldc + N,
+                           kCheckStore, off))
+                dst[e * ldc] = to_c16(v[b][e], bf);
+            }
+          } else if (row_c + 32 <= M) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dst[e * ldc] = to_c16(v[b][e], bf);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (row_c + e < M) dst[e * ldc] = to_c16(v[b][e], bf);
+          }
+        }
+      }
+      __syncwarp();
+    } else if constexpr (K::EPI == kEpiDirect) {
       const int32_t col = col_warp + (int32_t)lane;
       if (col < N) {
 #pragma unroll
         for (int b = 0; b < NBB; ++b) {
           if (b >= nb) break;
           const int32_t row_c = row0 + (c0 + b) * 32;
-          float* dst = p.C + (int64_t)row_c * ldc + col;
+          float* dst = static_cast<float*>(p.C) + (int64_t)row_c * ldc + col;
           if (WGEMM_CHECKED) {
             for (int e = 0; e < 32; ++e) {
               const int64_t off = (int64_t)(row_c + e) * ldc + col;
@@ -640,9 +688,17 @@ struct Kernel {
 #pragma unroll
       for (int b = 0; b < NBB; ++b) {
         if (b >= nb) break;
-        float* sp = reinterpret_cast<float*>(smem + (stage_base - base) + b * K::kEpiSlotBytes);
+        if constexpr (K::OUT == kOut16) {
+          const bool bf = p.c_bf16 != 0;
+          uint16_t* sp =
+              reinterpret_cast<uint16_t*>(smem + (stage_base - base) + b * K::kEpiSlotBytes);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sp[e * 32 + lane] = __uint_as_float(v[b][e]);
+          for (int e = 0; e < 32; ++e) sp[e * 32 + lane] = to_c16(v[b][e], bf);
+        } else {
+          float* sp = reinterpret_cast<float*>(smem + (stage_base - base) + b * K::kEpiSlotBytes);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sp[e * 32 + lane] = __uint_as_float(v[b][e]);
+        }
       }
       fence_proxy_async_shared();
       __syncwarp();
@@ -652,7 +708,9 @@ struct Kernel {
           if (b >= nb) break;
           const uint32_t sbuf = stage_base + b * K::kEpiSlotBytes;
           const int32_t row_c = row0 + (c0 + b) * 32;
-          if (add) tma_reduce_add_2d(&p.tmC, sbuf, col_warp, row_c);
+          // 16-bit C is written by data-parallel units only: partial sums
+          // are never rounded to 16 bits before they are added.
+          if (K::OUT == kOut32 && add) tma_reduce_add_2d(&p.tmC, sbuf, col_warp, row_c);
           else tma_store_2d(&p.tmC, sbuf, col_warp, row_c);
         }
         bulk_commit_group();
@@ -671,7 +729,7 @@ struct Kernel {
     bool ok = true;
     uint32_t sync_phase = 0;
 
-    if constexpr (K::EPI == kEpiTma) {
+    if constexpr (K::EPI == kEpiTma && K::OUT == kOut32) {
       if (p.plan.mode == kSplitK)
         ok = zero_slices(p, base, rank, grp, worker, sync_phase, abort_flag);
     }
@@ -792,7 +850,7 @@ struct Kernel {
                     kCheckZero, row_end))
         continue;
       for (int32_t r = row_begin; r < row_end; ++r) {
-        float* row = p.C + (int64_t)r * ldc + col_begin;
+        float* row = static_cast<float*>(p.C) + (int64_t)r * ldc + col_begin;
         for (int32_t v = t; v < nvec; v += 128)
           reinterpret_cast<float4*>(row)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int32_t c = nvec * 4 + t; c < ncols; c += 128) row[c] = 0.f;
@@ -893,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   if (WGEMM_TRACE && threadIdx.x == 0) trace_event(p, kTrExit);
 }
 
-// K == 0: C := 0 (the empty sum).
-__global__ void wgemm_zero_kernel(float* C, int32_t M, int32_t N, int64_t ldc);
+// K == 0: C := 0 (the empty sum), for C elements of `elem_bytes` (4 or 2).
+__global__ void wgemm_zero_kernel(void* C, int32_t M, int32_t N, int64_t ldc, int32_t elem_bytes);
 
 }  // namespace wg

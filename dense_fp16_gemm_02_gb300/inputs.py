@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for C = A·Bᵀ (fp16 A: M×K, fp16 B: N×K, row-major).
+"""Seeded synthetic inputs for C = A·Bᵀ (A: M×K, B: N×K, row-major; fp16, or
+bf16 given as uint16 bit patterns).
 
 This module holds no GEMM arithmetic. It is the one piece that both the CUDA
 path (tests, bench) and the CPU oracle are fed from, so that both see the same
@@ -22,6 +23,11 @@ Values.
   with round-to-nearest-even (numpy's float64 → float16 cast keeps fp16
   subnormals).
 * "int": v = ((h >> 32) · 5) >> 32, x = v − 2 in {−2, …, 2} (exact in fp16).
+* dtype "bf16": the same x (the uniform draw 2u − 1 before any rounding, or
+  the integer), rounded to bf16 with round-to-nearest-even: with
+  x = m · 2^e, m in [0.5, 1), the significand m · 2^8 is rounded to an integer
+  (numpy's rint: ties to even) and scaled back; the result is exact in fp32,
+  whose upper 16 bits are the bf16 pattern.
 
 The pages measured on integers in [−3, 3] from a hash of the index
 ("SASS-Level Kernel Generation for Blackwell", How we measured); the
@@ -39,9 +45,10 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _MASK = (1 << 64) - 1
 
-# fp16 quiet NaN, used to poison padding columns so that a reader that strays
-# past K is caught.
+# fp16 and bf16 quiet NaNs, used to poison padding columns so that a reader
+# that strays past K is caught.
 F16_NAN_BITS = 0x7E00
+BF16_NAN_BITS = 0x7FC0
 
 
 def mix64_int(z: int) -> int:
@@ -69,33 +76,54 @@ def hash_stream(key: int, start: int, count: int) -> np.ndarray:
         return _mix64(np.uint64(key) + idx * _GAMMA)
 
 
-def _values(h: np.ndarray, kind: str) -> np.ndarray:
+def _draws(h: np.ndarray, kind: str) -> np.ndarray:
+    """The values before rounding to the element type, as float64."""
     if kind == "uniform":
         u = (h >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
-        return (2.0 * u - 1.0).astype(np.float16)
+        return 2.0 * u - 1.0
     if kind == "int":
         with np.errstate(over="ignore"):
             v = ((h >> np.uint64(32)) * np.uint64(5)) >> np.uint64(32)
-        return (v.astype(np.int64) - 2).astype(np.float16)
+        return (v.astype(np.int64) - 2).astype(np.float64)
     raise ValueError(f"unknown value kind {kind!r}")
+
+
+def bf16_bits_rne(x: np.ndarray) -> np.ndarray:
+    """float64 values (|x| within fp32's normal range or 0) rounded to bf16,
+    to nearest with ties to even; returns the uint16 bit patterns."""
+    m, e = np.frexp(x)
+    y = np.ldexp(np.rint(m * 256.0), e - 8)  # 8 significant bits, exact in fp32
+    return (y.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def _values(h: np.ndarray, kind: str, dtype: str) -> np.ndarray:
+    x = _draws(h, kind)
+    if dtype == "f16":
+        return x.astype(np.float16)
+    if dtype == "bf16":
+        return bf16_bits_rne(x)
+    raise ValueError(f"unknown element type {dtype!r}")
 
 
 def matrix(rows: int, cols: int, seed: int, tensor_id: int, kind: str = "uniform",
            ld: int | None = None, pad: str = "zero",
-           chunk_elems: int = 1 << 22) -> np.ndarray:
-    """A rows×ld fp16 array whose first `cols` columns hold the seeded stream.
+           chunk_elems: int = 1 << 22, dtype: str = "f16") -> np.ndarray:
+    """A rows×ld array whose first `cols` columns hold the seeded stream:
+    float16 for dtype "f16", uint16 bf16 bit patterns for dtype "bf16".
 
-    Columns [cols, ld) are padding: zeros (pad="zero") or fp16 NaN (pad="nan").
+    Columns [cols, ld) are padding: zeros (pad="zero") or NaN (pad="nan").
     The stream index of element (r, c) is r·cols + c, so the values do not
     depend on `ld`.
     """
     ld = cols if ld is None else ld
     if ld < cols:
         raise ValueError("ld < cols")
-    out = np.empty((rows, ld), dtype=np.float16)
+    if dtype not in ("f16", "bf16"):
+        raise ValueError(f"unknown element type {dtype!r}")
+    out = np.empty((rows, ld), dtype=np.float16 if dtype == "f16" else np.uint16)
     if ld > cols:
         if pad == "nan":
-            out[:, cols:].view(np.uint16)[...] = F16_NAN_BITS
+            out[:, cols:].view(np.uint16)[...] = F16_NAN_BITS if dtype == "f16" else BF16_NAN_BITS
         else:
             out[:, cols:] = 0
     if rows == 0 or cols == 0:
@@ -106,7 +134,7 @@ def matrix(rows: int, cols: int, seed: int, tensor_id: int, kind: str = "uniform
     def fill(r0: int) -> None:
         r1 = min(rows, r0 + rows_per_chunk)
         h = hash_stream(key, r0 * cols, (r1 - r0) * cols)
-        out[r0:r1, :cols] = _values(h, kind).reshape(r1 - r0, cols)
+        out[r0:r1, :cols] = _values(h, kind, dtype).reshape(r1 - r0, cols)
 
     starts = range(0, rows, rows_per_chunk)
     if len(starts) == 1:
@@ -119,10 +147,11 @@ def matrix(rows: int, cols: int, seed: int, tensor_id: int, kind: str = "uniform
 
 def gemm_operands(M: int, N: int, K: int, seed: int, kind: str = "uniform",
                   lda: int | None = None, ldb: int | None = None,
-                  pad: str = "zero") -> tuple[np.ndarray, np.ndarray]:
-    """The A (M×lda) and B (N×ldb) fp16 operands of one problem: tensor ids 0 and 1."""
-    A = matrix(M, K, seed, 0, kind, lda, pad)
-    B = matrix(N, K, seed, 1, kind, ldb, pad)
+                  pad: str = "zero", dtype: str = "f16") -> tuple[np.ndarray, np.ndarray]:
+    """The A (M×lda) and B (N×ldb) operands of one problem (tensor ids 0 and
+    1), fp16 or bf16 (bit patterns)."""
+    A = matrix(M, K, seed, 0, kind, lda, pad, dtype=dtype)
+    B = matrix(N, K, seed, 1, kind, ldb, pad, dtype=dtype)
     return A, B
 
 

@@ -23,6 +23,7 @@ STATUS_NAMES = {
     -7: "WGEMM_ERR_WORKSPACE", -8: "WGEMM_ERR_NOALLOC_TOO_LARGE",
 }
 MODE_DATA_PARALLEL, MODE_SPLIT_K, MODE_STREAM_K = 0, 1, 2
+WGEMM_F32, WGEMM_F16, WGEMM_BF16 = 0, 1, 2
 
 
 class WgemmError(RuntimeError):
@@ -53,11 +54,18 @@ def load():
         lib.wgemm_f16f32_config.restype = i
         lib.wgemm_f16f32_splitk_noalloc.argtypes = [p, p, p, i, i, i, i, i, i, i, p]
         lib.wgemm_f16f32_splitk_noalloc.restype = i
+        lib.wgemm_gemm.argtypes = [p, p, p, i, i, i, i, i, i, i, i, p]
+        lib.wgemm_gemm.restype = i
+        lib.wgemm_gemm_config.argtypes = [p, p, p, i, i, i, i, i, i, i, i, i, i, i, p]
+        lib.wgemm_gemm_config.restype = i
+        for name in ("wgemm_bf16f32", "wgemm_f16f16", "wgemm_bf16bf16"):
+            getattr(lib, name).argtypes = [p, p, p, i, i, i, i, i, i, p]
+            getattr(lib, name).restype = i
         lib.wgemm_num_configs.argtypes = []
         lib.wgemm_num_configs.restype = i
         lib.wgemm_config_name.argtypes = [i]
         lib.wgemm_config_name.restype = ctypes.c_char_p
-        lib.wgemm_select.argtypes = [i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i),
+        lib.wgemm_select.argtypes = [i, i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i),
                                      ctypes.POINTER(i)]
         lib.wgemm_select.restype = i
         lib.wgemm_check.argtypes = [p]
@@ -82,8 +90,10 @@ def load():
         lib.wgemm_debug_set_flag_wait_skew.restype = i
         lib.wgemm_debug_smem_desc.argtypes = [u32]
         lib.wgemm_debug_smem_desc.restype = u64
-        lib.wgemm_debug_idesc.argtypes = [i, i]
+        lib.wgemm_debug_idesc.argtypes = [i, i, i]
         lib.wgemm_debug_idesc.restype = u32
+        lib.wgemm_debug_config_out.argtypes = [i]
+        lib.wgemm_debug_config_out.restype = i
         lib.wgemm_debug_sw128_offset.argtypes = [u32, u32]
         lib.wgemm_debug_sw128_offset.restype = u32
         lib.wgemm_debug_plan.argtypes = [i, i, i, i, i, i, i, p, i, ctypes.POINTER(i),
@@ -139,6 +149,36 @@ def wgemm_f16f32_config(A: int, B: int, C: int, M: int, N: int, K: int, lda: int
                                       stream)
 
 
+def wgemm_gemm(A: int, B: int, C: int, ab_type: int, c_type: int, M: int, N: int, K: int,
+               lda: int, ldb: int, ldc: int, stream: int | None) -> int:
+    """The typed C call on device pointers; returns the status code."""
+    return load().wgemm_gemm(A, B, C, ab_type, c_type, M, N, K, lda, ldb, ldc, stream)
+
+
+def wgemm_gemm_config(A: int, B: int, C: int, ab_type: int, c_type: int, M: int, N: int, K: int,
+                      lda: int, ldb: int, ldc: int, config: int, mode: int, splits: int,
+                      stream: int | None) -> int:
+    return load().wgemm_gemm_config(A, B, C, ab_type, c_type, M, N, K, lda, ldb, ldc, config,
+                                    mode, splits, stream)
+
+
+def wgemm_bf16f32(A, B, C, M, N, K, lda, ldb, ldc, stream) -> int:
+    return load().wgemm_bf16f32(A, B, C, M, N, K, lda, ldb, ldc, stream)
+
+
+def wgemm_f16f16(A, B, C, M, N, K, lda, ldb, ldc, stream) -> int:
+    return load().wgemm_f16f16(A, B, C, M, N, K, lda, ldb, ldc, stream)
+
+
+def wgemm_bf16bf16(A, B, C, M, N, K, lda, ldb, ldc, stream) -> int:
+    return load().wgemm_bf16bf16(A, B, C, M, N, K, lda, ldb, ldc, stream)
+
+
+def config_out(config: int) -> int:
+    """0 if the configuration writes fp32 C, 1 if 16-bit C."""
+    return load().wgemm_debug_config_out(config)
+
+
 def wgemm_f16f32_splitk_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int,
                                 ldb: int, ldc: int, splits: int, stream: int | None) -> int:
     """Split-K on device pointers with the library's fixed scratch array (no
@@ -146,14 +186,14 @@ def wgemm_f16f32_splitk_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, 
     return load().wgemm_f16f32_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, splits, stream)
 
 
-def wgemm_select(M: int, N: int, K: int, lda: int | None = None,
-                 ldb: int | None = None) -> tuple[int, int, int]:
-    """(configuration id, mode, splits) that wgemm_f16f32 runs for this shape
-    and these row pitches (K when omitted)."""
+def wgemm_select(M: int, N: int, K: int, lda: int | None = None, ldb: int | None = None,
+                 c_type: int = WGEMM_F32) -> tuple[int, int, int]:
+    """(configuration id, mode, splits) that the library runs for this shape,
+    these row pitches (K when omitted) and this C type."""
     lda = K if lda is None else lda
     ldb = K if ldb is None else ldb
     c, m, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    rc = load().wgemm_select(M, N, K, lda, ldb, ctypes.byref(c), ctypes.byref(m),
+    rc = load().wgemm_select(M, N, K, lda, ldb, c_type, ctypes.byref(c), ctypes.byref(m),
                              ctypes.byref(s))
     if rc != WGEMM_OK:
         raise WgemmError(rc, "wgemm_select")
@@ -186,17 +226,27 @@ def _stream_handle(stream) -> int | None:
     return getattr(stream, "cuda_stream", stream)
 
 
-def gemm(A, B, C=None, *, config: int | str | None = None, mode: int = -1, splits: int = 1,
-         stream=None):
-    """C = A·Bᵀ for torch tensors: A (M×K fp16), B (N×K fp16), C (M×N fp32).
+def _wgemm_type(dtype) -> int:
+    import torch
+    types = {torch.float32: WGEMM_F32, torch.float16: WGEMM_F16, torch.bfloat16: WGEMM_BF16}
+    if dtype not in types:
+        raise TypeError(f"unsupported element type {dtype}")
+    return types[dtype]
+
+
+def gemm(A, B, C=None, *, out_dtype=None, config: int | str | None = None, mode: int = -1,
+         splits: int = 1, stream=None):
+    """C = A·Bᵀ for torch tensors: A (M×K) and B (N×K) both float16 or both
+    bfloat16; C (M×N) float32 (the default), float16 or bfloat16.
 
     A and B may have a row stride larger than K (a column slice of a wider
-    tensor); their last dimension must be contiguous. C is allocated when not
-    given. The work is enqueued on `stream` (default: torch's current stream).
+    tensor); their last dimension must be contiguous. C is allocated (of
+    `out_dtype`, default float32) when not given. The work is enqueued on
+    `stream` (default: torch's current stream).
     """
     import torch
-    if A.dtype != torch.float16 or B.dtype != torch.float16:
-        raise TypeError("A and B must be float16")
+    if A.dtype not in (torch.float16, torch.bfloat16) or B.dtype != A.dtype:
+        raise TypeError("A and B must both be float16 or both bfloat16")
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
         raise ValueError("A must be M×K and B N×K")
     if A.stride(1) != 1 or B.stride(1) != 1:
@@ -206,20 +256,21 @@ def gemm(A, B, C=None, *, config: int | str | None = None, mode: int = -1, split
     M, K = A.shape
     N = B.shape[0]
     if C is None:
-        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    if C.dtype != torch.float32 or C.shape != (M, N) or C.stride(1) != 1:
-        raise ValueError("C must be an M×N float32 tensor with a contiguous last dimension")
+        C = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
+    if C.shape != (M, N) or C.stride(1) != 1:
+        raise ValueError("C must be M×N with a contiguous last dimension")
+    ab_type, c_type = _wgemm_type(A.dtype), _wgemm_type(C.dtype)
     lda, ldb, ldc = A.stride(0), B.stride(0), C.stride(0)
     if M == 0 or N == 0:
         return C
     h = _stream_handle(stream)
     if config is None:
-        rc = wgemm_f16f32(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, max(lda, K),
-                          max(ldb, K), ldc, h)
+        rc = wgemm_gemm(A.data_ptr(), B.data_ptr(), C.data_ptr(), ab_type, c_type, M, N, K,
+                        max(lda, K), max(ldb, K), ldc, h)
     else:
         cid = config_id(config) if isinstance(config, str) else int(config)
-        rc = wgemm_f16f32_config(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, max(lda, K),
-                                 max(ldb, K), ldc, cid, mode, splits, h)
+        rc = wgemm_gemm_config(A.data_ptr(), B.data_ptr(), C.data_ptr(), ab_type, c_type, M, N,
+                               K, max(lda, K), max(ldb, K), ldc, cid, mode, splits, h)
     if rc != WGEMM_OK:
-        raise WgemmError(rc, "wgemm_f16f32")
+        raise WgemmError(rc, "wgemm_gemm")
     return C

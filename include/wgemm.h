@@ -1,6 +1,7 @@
 /*
  * wgemm — dense GEMM C = A·Bᵀ for NVIDIA GB300 (sm_103a): fp16 A and B,
- * fp32 accumulation, fp32 C.
+ * fp32 accumulation, fp32 C; and the same with bf16 A and B and/or a 16-bit
+ * (fp16 or bf16) C.
  *
  * The operation is the one "SASS-Level Kernel Generation for Blackwell"
  * measures (section "The numbers", Setup paragraph: fp16 inputs, fp32
@@ -50,14 +51,22 @@ typedef struct CUstream_st* wgemm_stream_t;
 /* An fp16 (IEEE binary16) value, passed as its bit pattern. */
 typedef uint16_t wgemm_f16_t;
 
+/* A bf16 (bfloat16: the upper 16 bits of an IEEE binary32) value, as its bit pattern. */
+typedef uint16_t wgemm_bf16_t;
+
+/* Element types of wgemm_gemm. */
+#define WGEMM_F32 0
+#define WGEMM_F16 1
+#define WGEMM_BF16 2
+
 /* Status codes. */
 #define WGEMM_OK 0
-#define WGEMM_ERR_INVALID_ARG -1      /* M/N/K < 0, NULL with a non-empty operand, lda < K, ldb < K, ldc < N */
-#define WGEMM_ERR_ALIGNMENT -2        /* A or B not 16-byte aligned, lda or ldb not a multiple of 8, C not 4-byte aligned, or a TMA-epilogue configuration forced on a C that is not 16-byte aligned with ldc % 4 == 0 */
+#define WGEMM_ERR_INVALID_ARG -1      /* M/N/K < 0, NULL with a non-empty operand, lda < K, ldb < K, ldc < N, an unknown element type */
+#define WGEMM_ERR_ALIGNMENT -2        /* A or B not 16-byte aligned, lda or ldb not a multiple of 8, C not aligned to its element size, or a TMA-epilogue configuration forced on a C whose base or row pitch (ldc · element size) is not a multiple of 16 bytes */
 #define WGEMM_ERR_LAUNCH -3           /* a CUDA call failed while preparing or launching */
 #define WGEMM_ERR_NO_DEVICE -4        /* no current device, or it is not compute capability 10.3 */
 #define WGEMM_ERR_DEVICE_TIMEOUT -5   /* a bounded wait inside a kernel expired (see wgemm_last_device_error) */
-#define WGEMM_ERR_CONFIG -6           /* the forced configuration id does not exist or cannot run this shape */
+#define WGEMM_ERR_CONFIG -6           /* the forced configuration id does not exist, is for the other C width, or cannot run this shape or mode */
 #define WGEMM_ERR_WORKSPACE -7        /* the flag workspace could not be allocated */
 #define WGEMM_ERR_NOALLOC_TOO_LARGE -8 /* the problem needs more split-K flags than wgemm_f16f32_splitk_noalloc's fixed array holds */
 
@@ -91,24 +100,68 @@ int wgemm_f16f32_config(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
                         int config_id, int mode, int splits,
                         wgemm_stream_t stream);
 
+/*
+ * The same product for other element types. Page 1's measured operation has
+ * fp16 operands and fp32 C; bf16 operands and a 16-bit C are the adjacent
+ * variants of the same tensor-core instruction (tcgen05.mma .kind::f16 takes
+ * fp16 or bf16 operands, both of the same type, and accumulates in fp32).
+ *   ab_type: WGEMM_F16 or WGEMM_BF16 — the type of both A and B.
+ *   c_type:  WGEMM_F32, WGEMM_F16 or WGEMM_BF16. A 16-bit C holds the fp32
+ *            sum rounded once to nearest, ties to even; it is computed data
+ *            parallel only (K is never split, so no partial sum is rounded).
+ * Layout, strides and alignment as wgemm_f16f32, with C's alignment and TMA
+ * conditions taken in C's element size: C aligned to its element size; the
+ * TMA epilogue wants a 16-byte aligned C and ldc · element size a multiple
+ * of 16. Returns as wgemm_f16f32; WGEMM_ERR_INVALID_ARG for an unknown type.
+ * wgemm_gemm(A, B, C, WGEMM_F16, WGEMM_F32, ...) is wgemm_f16f32.
+ */
+int wgemm_gemm(const void* A, const void* B, void* C, int ab_type, int c_type,
+               int M, int N, int K, int lda, int ldb, int ldc,
+               wgemm_stream_t stream);
+
+/*
+ * As wgemm_gemm with the configuration and K-decomposition forced (see
+ * wgemm_f16f32_config). A configuration serves one C width: those whose
+ * name ends in "_h" write a 16-bit C and run data parallel only (mode 0 or
+ * -1); the others write fp32. WGEMM_ERR_CONFIG otherwise.
+ */
+int wgemm_gemm_config(const void* A, const void* B, void* C, int ab_type, int c_type,
+                      int M, int N, int K, int lda, int ldb, int ldc,
+                      int config_id, int mode, int splits,
+                      wgemm_stream_t stream);
+
+/* Typed shorthands of wgemm_gemm: bf16 → fp32, fp16 → fp16, bf16 → bf16. */
+int wgemm_bf16f32(const wgemm_bf16_t* A, const wgemm_bf16_t* B, float* C,
+                  int M, int N, int K, int lda, int ldb, int ldc,
+                  wgemm_stream_t stream);
+int wgemm_f16f16(const wgemm_f16_t* A, const wgemm_f16_t* B, wgemm_f16_t* C,
+                 int M, int N, int K, int lda, int ldb, int ldc,
+                 wgemm_stream_t stream);
+int wgemm_bf16bf16(const wgemm_bf16_t* A, const wgemm_bf16_t* B, wgemm_bf16_t* C,
+                   int M, int N, int K, int lda, int ldb, int ldc,
+                   wgemm_stream_t stream);
+
 /* Number of compiled kernel configurations, and the name of one ("" if out of range). */
 int wgemm_num_configs(void);
 const char* wgemm_config_name(int config_id);
 
 /*
- * The choice wgemm_f16f32 makes for a shape and operand row pitches (lda,
- * ldb, in elements) on the current device: the measured per-shape table if
- * the shape is in it and both pitches are multiples of 16 elements (rows on
- * 32-byte sectors, as the table was measured), else the configuration and
+ * The choice wgemm_f16f32 (c_type WGEMM_F32) or wgemm_gemm (any c_type; the
+ * operand type does not enter) makes for a shape and operand row pitches
+ * (lda, ldb, in elements) on the current device: for fp32 C, the measured
+ * per-shape table if the shape is in it and both pitches are multiples of 16
+ * elements (rows on 32-byte sectors, as the table was measured); else the
+ * configuration of C's width and
  * K-decomposition with the least time predicted from measured
  * per-configuration rates (waves of tiles × per-k-block cost + fixed costs),
  * fitted separately for rows on and off 32-byte sectors. A K split is chosen
  * only when it predicts at least 20% less time than the best data-parallel
  * configuration. Writes the configuration id, mode and splits (any pointer
- * may be NULL). Returns WGEMM_OK, WGEMM_ERR_INVALID_ARG (negative size or a
- * pitch below K) or a device error.
+ * may be NULL). Returns WGEMM_OK, WGEMM_ERR_INVALID_ARG (negative size, a
+ * pitch below K, an unknown c_type) or a device error.
  */
-int wgemm_select(int M, int N, int K, int lda, int ldb, int* config_id, int* mode, int* splits);
+int wgemm_select(int M, int N, int K, int lda, int ldb, int c_type, int* config_id, int* mode,
+                 int* splits);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
@@ -175,7 +228,10 @@ int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16_t* B, floa
  * kernels build for a K-major fp16 operand tile with the 128-byte swizzle,
  * starting at shared byte address `smem_addr`.
  * wgemm_debug_idesc: the 32-bit instruction descriptor of a kind::f16 MMA of
- * shape M×N×16 with an f32 accumulator.
+ * shape M×N×16 with an f32 accumulator, fp16 operands (bf16 = 0) or bf16
+ * operands (bf16 = 1).
+ * wgemm_debug_config_out: 0 if a configuration writes fp32 C, 1 if 16-bit C,
+ * WGEMM_ERR_CONFIG for an unknown id.
  * wgemm_debug_sw128_offset: byte offset of fp16 element (row, k) inside a
  * 1024-byte-aligned 128-byte-swizzled K-major tile.
  * wgemm_debug_plan: fills `out` (7 int32 per unit: tile, tm, tn, kb_begin,
@@ -221,7 +277,8 @@ double wgemm_debug_predict_us(int M, int N, int K, int lda, int ldb, int config_
                               int splits, int workers);
 
 uint64_t wgemm_debug_smem_desc(uint32_t smem_addr);
-uint32_t wgemm_debug_idesc(int M, int N);
+uint32_t wgemm_debug_idesc(int M, int N, int bf16);
+int wgemm_debug_config_out(int config_id);
 uint32_t wgemm_debug_sw128_offset(uint32_t row, uint32_t k);
 int wgemm_debug_plan(int M, int N, int K, int config_id, int mode, int splits, int workers,
                      int32_t* out, int max_units, int* tile_rows, int* tile_cols);

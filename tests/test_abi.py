@@ -74,11 +74,12 @@ def test_sw128_layout_matches_address_bit_xor(lib):
     assert len(seen) == 128 * 64  # a bijection onto the tile's bytes (2-byte steps)
 
 
+@pytest.mark.parametrize("bf16", [0, 1])
 @pytest.mark.parametrize("M,N", [(128, 256), (128, 64), (256, 256), (256, 128), (128, 16)])
-def test_instruction_descriptor_fields(lib, M, N):
-    d = lib.wgemm_debug_idesc(M, N)
+def test_instruction_descriptor_fields(lib, M, N, bf16):
+    d = lib.wgemm_debug_idesc(M, N, bf16)
     assert (d >> 4) & 3 == 1            # D = f32
-    assert (d >> 7) & 7 == 0 and (d >> 10) & 7 == 0  # A, B = f16
+    assert (d >> 7) & 7 == bf16 and (d >> 10) & 7 == bf16  # A, B: 0 = f16, 1 = bf16
     assert (d >> 13) & 0xF == 0         # no negation, both K-major
     assert (d >> 17) & 0x3F == N >> 3
     assert (d >> 24) & 0x1F == M >> 4
@@ -137,3 +138,30 @@ def test_rule_charges_rows_off_sectors(lib):
     on = lib.wgemm_debug_predict_us(3000, 5000, 3000, 3008, 3008, cid, 0, 1, 76)
     off = lib.wgemm_debug_predict_us(3000, 5000, 3000, 3000, 3000, cid, 0, 1, 76)
     assert off > 1.1 * on > 0
+
+
+def test_typed_entry_points_check_arguments_without_launch(lib):
+    ok = 1 << 20
+    F32, F16, BF16 = wgemm.WGEMM_F32, wgemm.WGEMM_F16, wgemm.WGEMM_BF16
+    g = lambda A, B, C, ab, c, ldc=8: lib.wgemm_gemm(A, B, C, ab, c, 4, 4, 8, 8, 8, ldc, None)
+    assert g(ok, ok, ok, F32, F32) == -1          # fp32 operands: not a tensor-core type here
+    assert g(ok, ok, ok, 3, F32) == -1
+    assert g(ok, ok, ok, F16, 7) == -1
+    assert g(ok, ok, ok + 1, F16, F16) == -2      # 16-bit C must be 2-byte aligned
+    assert g(ok, ok, ok + 2, BF16, F32) == -2     # fp32 C must be 4-byte aligned
+    assert g(ok, ok, ok, BF16, BF16, ldc=2) == -1  # ldc < N
+    assert lib.wgemm_gemm(None, None, None, F16, BF16, 0, 4, 8, 8, 8, 4, None) == 0
+    for fn in (lib.wgemm_bf16f32, lib.wgemm_f16f16, lib.wgemm_bf16bf16):
+        assert fn(ok, ok, ok, -1, 4, 8, 8, 8, 4, None) == -1
+
+
+def test_configurations_name_their_c_width(lib):
+    names = wgemm.config_names()
+    outs = [lib.wgemm_debug_config_out(i) for i in range(len(names))]
+    assert all(o == (1 if n.endswith("_h") else 0) for n, o in zip(names, outs))
+    assert 0 in outs and 1 in outs
+    assert lib.wgemm_debug_config_out(len(names)) == -6
+    # every 16-bit configuration is an fp32 configuration with another epilogue
+    for n in names:
+        if n.endswith("_h"):
+            assert n[:-2] in names

@@ -45,3 +45,32 @@ def test_sample_indices():
     assert len(idx) == 256 and idx[0] == 0 and idx[-1] == 8191
     assert np.all(np.diff(idx) > 0)
     assert np.array_equal(inputs.sample_indices(10, 256, 3, 2), np.arange(10))
+
+
+def test_bf16_values_are_the_draws_rounded_to_nearest_even():
+    """bf16 operands hold the same seeded draws as fp16 ones, each rounded to
+    the nearest bf16 (numpy's reading of the pattern as an fp32's upper half;
+    ties to the even pattern)."""
+    rows, cols = 64, 257
+    bits = inputs.matrix(rows, cols, 5, 0, "uniform", dtype="bf16")
+    h = inputs.hash_stream(inputs.stream_key(5, 0), 0, rows * cols)
+    x = 2.0 * ((h >> np.uint64(11)).astype(np.float64) * 2.0 ** -53) - 1.0
+    v = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64).ravel()
+    up = (((bits.astype(np.uint32) + 1) << np.uint32(16)).view(np.float32)
+          .astype(np.float64).ravel())
+    dn = (((bits.astype(np.uint32) - 1) << np.uint32(16)).view(np.float32)
+          .astype(np.float64).ravel())
+    err = np.abs(x - v)
+    assert np.all(err <= np.abs(x - up)) and np.all(err <= np.abs(x - dn))
+    tie = (err == np.abs(x - up)) | (err == np.abs(x - dn))
+    assert np.all(bits.ravel()[tie] % 2 == 0)
+    # the fp16 copy rounds the same draws: the two differ by under one bf16 step
+    f16 = inputs.matrix(rows, cols, 5, 0, "uniform").astype(np.float64).ravel()
+    assert np.all(np.abs(f16 - v) <= np.abs(v) * 2.0 ** -7 + 2.0 ** -24)
+
+
+def test_bf16_integers_and_padding():
+    bits = inputs.matrix(20, 30, 3, 1, "int", ld=40, pad="nan", dtype="bf16")
+    v = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    assert np.array_equal(v[:, :30], inputs.matrix(20, 30, 3, 1, "int").astype(np.float32))
+    assert np.all(bits[:, 30:] == inputs.BF16_NAN_BITS)
