@@ -33,6 +33,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = ("µs/call and TFLOP/s per shape (1 GB300) + fraction of dense fp16 tensor peak")
+# Operand and C element types: the pages' product (fp16 -> fp32) and the
+# adjacent variants of the same kernels.
+TYPES = {"f16f32": ("f16", "f32"), "bf16f32": ("bf16", "f32"), "f16f16": ("f16", "f16"),
+         "bf16bf16": ("bf16", "bf16")}
+
 WORKLOADS = {
     "c1": [(1024, 1024, 1024)],
     "sweep": [(1536, 1536, 1536), (2048, 2048, 2048), (4096, 4096, 4096), (3072, 1280, 2048),
@@ -178,7 +183,7 @@ def dist_setup(args):
 _B_CACHE = {}
 
 
-def oracle_sample_rate(shapes, seconds_total: float, nthreads: int = 0):
+def oracle_sample_rate(shapes, seconds_total: float, nthreads: int = 0, ab: str = "f16"):
     """Times the CPU oracle on a row sample of every shape, about
     `seconds_total` of oracle work in all (a shape that finishes in full hands
     its unused share to the larger ones); returns (TFLOP/s over the sample,
@@ -192,14 +197,14 @@ def oracle_sample_rate(shapes, seconds_total: float, nthreads: int = 0):
     for n_done, i in enumerate(order):
         M, N, K = shapes[i]
         budget = left / (len(order) - n_done)
-        if (N, K) not in _B_CACHE:
-            _B_CACHE[(N, K)] = inputs.matrix(N, K, 1000, 1)
-        B = _B_CACHE[(N, K)]
+        if (N, K, ab) not in _B_CACHE:
+            _B_CACHE[(N, K, ab)] = inputs.matrix(N, K, 1000, 1, dtype=ab)
+        B = _B_CACHE[(N, K, ab)]
         # Calibrate at one and at four rows per thread (each call also decodes
         # all of B: a fixed cost), then size the sample to the budget.
         cal = []
         for r in sorted({min(M, threads), min(M, 4 * threads)}):
-            A = inputs.matrix(r, K, 1000, 0)
+            A = inputs.matrix(r, K, 1000, 0, dtype=ab)
             t0 = time.perf_counter()
             oracle.gemm_f64(A, B, nthreads=threads)
             cal.append((r, time.perf_counter() - t0))
@@ -213,7 +218,7 @@ def oracle_sample_rate(shapes, seconds_total: float, nthreads: int = 0):
         rows = int(min(M, max(rows, (budget - fixed) / per_row)))
         if rows > threads:
             rows -= rows % threads
-        A = inputs.matrix(rows, K, 1000, 0)
+        A = inputs.matrix(rows, K, 1000, 0, dtype=ab)
         t0 = time.perf_counter()
         oracle.gemm_f64(A, B, nthreads=threads)
         dt = time.perf_counter() - t0
@@ -230,11 +235,12 @@ def run_reference(args):
         return 0
     shapes = WORKLOADS[args.workload]
     budget = max(0.5 * len(shapes), min(60.0, 120.0 / max(1, args.steps + args.warmup)))
+    ab = TYPES[args.types][0]
     for _ in range(args.warmup):
-        oracle_sample_rate(shapes, budget / 4)
+        oracle_sample_rate(shapes, budget / 4, ab=ab)
     vals, last = [], None
     for _ in range(args.steps):
-        last = oracle_sample_rate(shapes, budget)
+        last = oracle_sample_rate(shapes, budget, ab=ab)
         vals.append(last[0])
     value = statistics.median(vals)
     tflop_per_step = sum(2.0 * M * N * K for (M, N, K) in shapes) / 1e12
@@ -244,6 +250,7 @@ def run_reference(args):
         "ms_per_step": tflop_per_step / value * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload + ": " + ", ".join(shape_name(s) for s in shapes),
+                   "types": args.types,
                    "oracle": "plain fp64 triple loop in C (oracle/wgemm_oracle.c)",
                    "sample": "row sample per shape, extrapolated per call"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last[1], "kind": "oracle",
@@ -272,13 +279,22 @@ def run_ours(args):
     shapes = WORKLOADS[args.workload]
     stream = torch.cuda.current_stream()
     h = stream.cuda_stream
+    ab, c = TYPES[args.types]
+    ab_type = wgemm.WGEMM_F16 if ab == "f16" else wgemm.WGEMM_BF16
+    c_type = {"f32": wgemm.WGEMM_F32, "f16": wgemm.WGEMM_F16, "bf16": wgemm.WGEMM_BF16}[c]
+    c_torch = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[c]
+    c_bytes = 4 if c == "f32" else 2
+
+    def as_tensor(x):  # fp16 arrays, or bf16 bit patterns (uint16)
+        t = torch.from_numpy(x if ab == "f16" else x.view(np.int16))
+        return t if ab == "f16" else t.view(torch.bfloat16)
 
     # Inputs: generated on the host once, uploaded before timing.
     data = []
     for i, (M, N, K) in enumerate(shapes):
-        A, B = inputs.gemm_operands(M, N, K, seed=1000 + i, kind="uniform")
-        dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
-        C = torch.empty((M, N), dtype=torch.float32, device=dev)
+        A, B = inputs.gemm_operands(M, N, K, seed=1000 + i, kind="uniform", dtype=ab)
+        dA, dB = as_tensor(A).to(dev), as_tensor(B).to(dev)
+        C = torch.empty((M, N), dtype=c_torch, device=dev)
         data.append((A, B, dA, dB, C))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     names = wgemm.config_names()
@@ -286,9 +302,14 @@ def run_ours(args):
     def call(i):
         (M, N, K) = shapes[i]
         _, _, dA, dB, C = data[i]
-        rc = wgemm.wgemm_f16f32(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, K, K, N, h)
+        if ab_type == wgemm.WGEMM_F16 and c_type == wgemm.WGEMM_F32:
+            rc = wgemm.wgemm_f16f32(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, K, K, N,
+                                    h)
+        else:
+            rc = wgemm.wgemm_gemm(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), ab_type, c_type, M,
+                                  N, K, K, K, N, h)
         if rc != 0:
-            raise RuntimeError(f"wgemm_f16f32 failed: {rc}")
+            raise RuntimeError(f"wgemm call failed: {rc}")
 
     def one_step(events):
         for i in range(len(shapes)):
@@ -338,7 +359,7 @@ def run_ours(args):
     by_config = {}
     for i, (M, N, K) in enumerate(shapes):
         us = times[:, i] * 1e3
-        cfg, mode, splits = wgemm.wgemm_select(M, N, K)
+        cfg, mode, splits = wgemm.wgemm_select(M, N, K, c_type=c_type)
         med = float(np.median(us))
         tf = flops[i] / (med * 1e-6) / 1e12
         bytes_min = 2.0 * (M * K + N * K) + 4.0 * M * N
@@ -364,9 +385,9 @@ def run_ours(args):
     # pinned memory, the call, D2H of C, all inside the timed region.
     pinned = []
     for (A, B, _, _, C) in data:
-        hA = torch.from_numpy(A).pin_memory()
-        hB = torch.from_numpy(B).pin_memory()
-        hC = torch.empty(C.shape, dtype=torch.float32).pin_memory()
+        hA = as_tensor(A).pin_memory()
+        hB = as_tensor(B).pin_memory()
+        hC = torch.empty(C.shape, dtype=c_torch).pin_memory()
         pinned.append((hA, hB, hC))
     e2e_steps = max(3, min(args.steps, 10))
     e2e_ms = []
@@ -389,24 +410,24 @@ def run_ours(args):
             e2e_ms.append(tot)
     e2e_step_ms = max_over_ranks([statistics.median(e2e_ms)], dev)[0]
     h2d = sum(2 * (M * K + N * K) for (M, N, K) in shapes)
-    d2h = sum(4 * M * N for (M, N, K) in shapes)
+    d2h = sum(c_bytes * M * N for (M, N, K) in shapes)
 
     line = None
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            rate, cores, sample, secs = oracle_sample_rate(shapes, args.cpu_seconds)
+            rate, cores, sample, secs = oracle_sample_rate(shapes, args.cpu_seconds, ab=ab)
             cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                    "sample": f"{sample} ({secs:.1f} s of oracle work)"}
         line = {
             "metric": METRIC, "value": round(float(value), 2), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "vs_baseline": None, "dtype": ab, "data": "synthetic",
             "config": {
                 "workload": args.workload + ": " + ", ".join(shape_name(s) for s in shapes),
-                "inputs": "uniform[-1,1] rounded to fp16, seeded SplitMix64, resident in HBM",
-                "accumulate": "f32", "output": "f32",
+                "inputs": f"uniform[-1,1] rounded to {ab}, seeded SplitMix64, resident in HBM",
+                "accumulate": "f32", "output": c,
                 "l2": "flushed between calls (256 MiB write), each call timed alone",
                 "timing": ("CUDA events on the launching stream around each call; a GPU-side "
                        "spin ahead of the start event hides host enqueue latency"),
@@ -446,6 +467,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="oracle time budget of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--types", choices=sorted(TYPES), default="f16f32",
+                    help="operand and C types (the measured product is f16f32)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.shape:

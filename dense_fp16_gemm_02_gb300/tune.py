@@ -43,6 +43,8 @@ def candidates(M, N, K, names, workers_pair, workers_single):
     kb = -(-K // 64)
     out = []
     for cid, name in enumerate(names):
+        if name.endswith("_h"):  # 16-bit C: not a candidate for an fp32 call
+            continue
         cg = 2 if name.startswith("g2") else 1
         cols, rows = (int(v) for v in name.split("_")[1].split("x"))
         tiles = -(-M // rows) * -(-N // cols)
@@ -192,7 +194,10 @@ def rates(out_path, points=RATE_POINTS):
         A, B = inputs.gemm_operands(max_waves * M1, N, Kmax, seed=11, kind="uniform",
                                     lda=Kmax + 16, ldb=Kmax + 16)
         dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
-        C = torch.empty((max_waves * M1, N), dtype=torch.float32, device="cuda")
+        # A 16-bit-output configuration ("_h") is timed writing fp16 C.
+        c_type = wgemm.WGEMM_F16 if name.endswith("_h") else wgemm.WGEMM_F32
+        C = torch.empty((max_waves * M1, N), device="cuda",
+                        dtype=torch.float16 if name.endswith("_h") else torch.float32)
         del A, B
         print(f"# rates {name} W={W} tiles {tm}x{tn}", file=sys.stderr, flush=True)
         row = {"config": name, "workers": W}
@@ -200,9 +205,9 @@ def rates(out_path, points=RATE_POINTS):
             X, y = [], []
             for waves, K in points:
                 M = waves * M1
-                call = (lambda M=M, K=K, ld=ld: wgemm.wgemm_f16f32_config(
-                    dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, ld, ld, N, cid, 0, 1,
-                    h))
+                call = (lambda M=M, K=K, ld=ld: wgemm.wgemm_gemm_config(
+                    dA.data_ptr(), dB.data_ptr(), C.data_ptr(), wgemm.WGEMM_F16, c_type, M, N,
+                    K, ld, ld, N, cid, 0, 1, h))
                 t = _time_calls(wgemm, torch, None, M, N, K, call, flush)
                 kb = (K + 63) // 64
                 X.append([1.0, waves, waves * kb])
