@@ -117,6 +117,18 @@ __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
 }
 
+// Programmatic dependent launch. griddep_wait: block until the grids this
+// grid depends on have completed and their memory operations are visible (a
+// no-op when the grid was launched without a programmatic dependency).
+// griddep_launch_dependents: this CTA allows the grid that depends on this
+// one to be scheduled (once every CTA of this grid has done so or exited).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 2-D tile load into this CTA's shared memory; completion is counted on
 // `bar` of this CTA.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar,

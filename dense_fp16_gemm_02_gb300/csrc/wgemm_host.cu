@@ -79,6 +79,7 @@ std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 uint32_t g_debug_wait_skew = 0;  // see wgemm_debug_set_flag_wait_skew
 uint64_t* g_debug_trace = nullptr;  // see wgemm_debug_set_trace
+bool g_pdl = false;                 // see wgemm_set_pdl
 int g_debug_trace_ctas = 0;
 
 bool env_log() {
@@ -503,9 +504,16 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
     std::fprintf(stderr, "wgemm: %dx%dx%d config %s mode %d splits %d workers %d tiles %d\n", M, N,
                  K, e.name, params.plan.mode, params.plan.splits, params.plan.workers,
                  params.plan.num_tiles);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_config(e, params.plan.workers, stream, attr);
   if (e.cg * e.mc == 1) cfg.numAttrs = 0;  // no cluster: a plain launch
+  if (g_pdl) {
+    // May start (set-up only; loads wait) while the previous kernel on the
+    // stream finishes, once that kernel allows its dependents to launch.
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
+  }
   void* args[] = {&params};
   if (cudaLaunchKernelExC(&cfg, e.func, args) != cudaSuccess) {
     cudaGetLastError();
@@ -562,6 +570,14 @@ int wgemm_f16f16(const wgemm_f16_t* A, const wgemm_f16_t* B, wgemm_f16_t* C, int
 int wgemm_bf16bf16(const wgemm_bf16_t* A, const wgemm_bf16_t* B, wgemm_bf16_t* C, int M, int N,
                    int K, int lda, int ldb, int ldc, wgemm_stream_t stream) {
   return wgemm_gemm(A, B, C, WGEMM_BF16, WGEMM_BF16, M, N, K, lda, ldb, ldc, stream);
+}
+
+int wgemm_set_pdl(int enable) {
+  if (enable != 0 && enable != 1) return WGEMM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  const int prev = g_pdl ? 1 : 0;
+  g_pdl = enable == 1;
+  return prev;
 }
 
 int wgemm_num_configs(void) { return (int)registry().entries.size(); }

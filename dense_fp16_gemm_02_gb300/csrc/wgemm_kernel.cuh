@@ -910,6 +910,14 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     }
     *abort_flag = 0;
     fence_mbarrier_init();
+    // Programmatic dependent launch: everything above touches no global
+    // memory that an earlier grid writes, so it overlaps that grid's tail;
+    // the first operand load waits for it. A grid that depends on this one
+    // may be scheduled from now on: it cannot start on an SM before this
+    // grid's CTA there exits (shared memory), and it waits for this grid's
+    // completion before it touches memory.
+    griddep_wait();
+    griddep_launch_dependents();
     if constexpr (K::kClusterSize == 1) prefilled = Kernel<K>::prefill(p, base, worker, rank, grp);
   }
   if (warp == 1) {
@@ -922,6 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   tcgen05_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (WGEMM_TRACE && threadIdx.x == 0) trace_event(p, kTrSetUp);
+  griddep_wait();  // every role reads or writes global memory only after this
 
   if (warp == 0) {
     // Thread 0 initialised the barriers and prefilled the ring, so it produces.

@@ -296,6 +296,63 @@ def validate(out_path, shapes=OFF_TABLE + HELD_OUT):
         json.dump(res, f, indent=1)
 
 
+PDL_SHAPES = [(1024, 1024, 1024), (2048, 2048, 2048), (4096, 4096, 1024), (4096, 4096, 4096),
+              (8192, 8192, 8192)]
+
+
+def pdl_report(out_path, shapes=PDL_SHAPES, calls=40, rounds=8):
+    """Back-to-back calls of one shape (no L2 flush between them), with
+    programmatic dependent launch off and on: time per call. A separate
+    report: the per-call metric times every call alone."""
+    import torch
+
+    sys.path.insert(0, ROOT)
+    from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
+    build.build()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    h = stream.cuda_stream
+    flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device="cuda")
+    res = []
+    for (M, N, K) in shapes:
+        A, B = inputs.gemm_operands(M, N, K, seed=5, kind="uniform")
+        dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        row = {"shape": [M, N, K], "calls": calls}
+        per = {False: [], True: []}
+        # Rounds alternate off, on, off, on ... so that both settings see the
+        # same clocks and temperature (long batches settle under the power cap).
+        for r in range(rounds + 1):
+            for pdl in ((False, True) if r % 2 == 0 else (True, False)):
+                wgemm.wgemm_set_pdl(pdl)
+                flush.fill_(float(r))
+                torch.cuda._sleep(2_000_000)  # the whole batch is enqueued before it starts
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(calls):
+                    rc = wgemm.wgemm_f16f32(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K,
+                                            K, K, N, h)
+                    if rc != 0:
+                        raise RuntimeError(f"call failed: {rc}")
+                e1.record(stream)
+                e1.synchronize()
+                if r > 0:
+                    per[pdl].append(e0.elapsed_time(e1) * 1e3 / calls)
+        wgemm.wgemm_set_pdl(False)
+        if wgemm.wgemm_check(h) != 0:
+            raise RuntimeError(f"device error: {wgemm.wgemm_last_device_error()}")
+        row["pdl_off_us"] = round(statistics.median(per[False]), 3)
+        row["pdl_on_us"] = round(statistics.median(per[True]), 3)
+        row["saved_us_per_call"] = round(row["pdl_off_us"] - row["pdl_on_us"], 3)
+        row["tflops_pdl_on"] = round(2.0 * M * N * K / (row["pdl_on_us"] * 1e-6) / 1e12, 1)
+        res.append(row)
+        print(json.dumps(row), flush=True)
+        del dA, dB, C
+        torch.cuda.empty_cache()
+    with open(out_path, "w") as f:
+        json.dump({"gpu": torch.cuda.get_device_name(0), "rows": res}, f, indent=1)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--out", default="tune.json")
@@ -304,6 +361,8 @@ def main(argv=None):
     ap.add_argument("--rates", metavar="JSON", help="measure per-configuration rates")
     ap.add_argument("--emit-rates", metavar="JSON", help="write csrc/wgemm_rates.inc")
     ap.add_argument("--validate", metavar="JSON", help="check the rule on off-table shapes")
+    ap.add_argument("--pdl-report", metavar="JSON",
+                    help="back-to-back calls with programmatic dependent launch off and on")
     args = ap.parse_args(argv)
     if args.emit:
         print(emit(args.emit))
@@ -316,6 +375,9 @@ def main(argv=None):
         return 0
     if args.validate:
         validate(args.validate)
+        return 0
+    if args.pdl_report:
+        pdl_report(args.pdl_report)
         return 0
     sweep(SHAPES[args.shapes], args.out)
     return 0

@@ -61,6 +61,8 @@ def load():
         for name in ("wgemm_bf16f32", "wgemm_f16f16", "wgemm_bf16bf16"):
             getattr(lib, name).argtypes = [p, p, p, i, i, i, i, i, i, p]
             getattr(lib, name).restype = i
+        lib.wgemm_set_pdl.argtypes = [i]
+        lib.wgemm_set_pdl.restype = i
         lib.wgemm_num_configs.argtypes = []
         lib.wgemm_num_configs.restype = i
         lib.wgemm_config_name.argtypes = [i]
@@ -115,6 +117,15 @@ def status_string(code: int) -> str:
         return load().wgemm_status_string(code).decode()
     except RuntimeError:
         return STATUS_NAMES.get(code, "unknown")
+
+
+def wgemm_set_pdl(enable: bool) -> int:
+    """Programmatic dependent launch on or off (process-wide); returns the
+    previous setting."""
+    rc = load().wgemm_set_pdl(1 if enable else 0)
+    if rc < 0:
+        raise WgemmError(rc, "wgemm_set_pdl")
+    return rc
 
 
 def num_configs() -> int:

@@ -141,6 +141,23 @@ int wgemm_bf16bf16(const wgemm_bf16_t* A, const wgemm_bf16_t* B, wgemm_bf16_t* C
                    int M, int N, int K, int lda, int ldb, int ldc,
                    wgemm_stream_t stream);
 
+/*
+ * Programmatic dependent launch, process-wide, off by default. When on,
+ * wgemm_f16f32 and wgemm_gemm launch their kernel with CUDA's programmatic
+ * stream serialization: the kernel may be scheduled before the previous
+ * kernel on the stream has finished (once that kernel allows it: every wgemm
+ * kernel does so right after its set-up), runs its set-up (barriers, tensor
+ * memory, tensor-map prefetch) and then waits, in griddepcontrol.wait, for
+ * the previous kernel to complete and its writes to be visible before its
+ * first load or store. Results are those of ordinary stream order; only
+ * launch latency and set-up overlap the previous call's tail. (PTX ISA,
+ * griddepcontrol; "SASS-Level Kernel Generation for Blackwell" measures with
+ * it off.) The split-K no-allocation entry point and the K = 0 path ignore
+ * the setting. Returns the previous setting (0 or 1), or
+ * WGEMM_ERR_INVALID_ARG unless enable is 0 or 1.
+ */
+int wgemm_set_pdl(int enable);
+
 /* Number of compiled kernel configurations, and the name of one ("" if out of range). */
 int wgemm_num_configs(void);
 const char* wgemm_config_name(int config_id);

@@ -165,3 +165,11 @@ def test_configurations_name_their_c_width(lib):
     for n in names:
         if n.endswith("_h"):
             assert n[:-2] in names
+
+
+def test_pdl_switch(lib):
+    assert lib.wgemm_set_pdl(2) == -1 and lib.wgemm_set_pdl(-1) == -1
+    prev = lib.wgemm_set_pdl(1)
+    assert prev in (0, 1)
+    assert lib.wgemm_set_pdl(0) == 1
+    assert lib.wgemm_set_pdl(prev) == 0
