@@ -294,15 +294,23 @@ def run_ours(args):
     for i, (M, N, K) in enumerate(shapes):
         A, B = inputs.gemm_operands(M, N, K, seed=1000 + i, kind="uniform", dtype=ab)
         dA, dB = as_tensor(A).to(dev), as_tensor(B).to(dev)
-        C = torch.empty((M, N), dtype=c_torch, device=dev)
+        C = torch.zeros((M, N), dtype=c_torch, device=dev)
         data.append((A, B, dA, dB, C))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     names = wgemm.config_names()
 
+    fused = args.epilogue == "fused"
+    biases = [torch.from_numpy(inputs.matrix(1, N, 2000 + i, 6, "uniform").astype(np.float32)
+                               .ravel()).to(dev) for i, (M, N, K) in enumerate(shapes)]
+
     def call(i):
         (M, N, K) = shapes[i]
         _, _, dA, dB, C = data[i]
-        if ab_type == wgemm.WGEMM_F16 and c_type == wgemm.WGEMM_F32:
+        if fused:  # D = A·Bᵀ + D + bias: the previous result read back in place
+            rc = wgemm.wgemm_gemm_ex(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), C.data_ptr(),
+                                     biases[i].data_ptr(), 1.0, 1.0, ab_type, c_type, M, N, K,
+                                     K, K, N, N, h)
+        elif ab_type == wgemm.WGEMM_F16 and c_type == wgemm.WGEMM_F32:
             rc = wgemm.wgemm_f16f32(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, K, K, N,
                                     h)
         else:
@@ -359,10 +367,12 @@ def run_ours(args):
     by_config = {}
     for i, (M, N, K) in enumerate(shapes):
         us = times[:, i] * 1e3
-        cfg, mode, splits = wgemm.wgemm_select(M, N, K, c_type=c_type)
+        cfg, mode, splits = wgemm.wgemm_select(M, N, K, c_type=c_type,
+                                               fused=args.epilogue == "fused")
         med = float(np.median(us))
         tf = flops[i] / (med * 1e-6) / 1e12
-        bytes_min = 2.0 * (M * K + N * K) + 4.0 * M * N
+        c_rw = (2 if args.epilogue == "fused" else 1) * c_bytes * M * N  # C written (and read)
+        bytes_min = 2.0 * (M * K + N * K) + c_rw
         per_shape.append({
             "shape": shape_name((M, N, K)), "us_median": round(med, 3),
             "us_min": round(float(us.min()), 3), "us_max": round(float(us.max()), 3),
@@ -388,19 +398,22 @@ def run_ours(args):
         hA = as_tensor(A).pin_memory()
         hB = as_tensor(B).pin_memory()
         hC = torch.empty(C.shape, dtype=c_torch).pin_memory()
-        pinned.append((hA, hB, hC))
+        hCin = torch.zeros(C.shape, dtype=c_torch).pin_memory() if fused else None
+        pinned.append((hA, hB, hC, hCin))
     e2e_steps = max(3, min(args.steps, 10))
     e2e_ms = []
     for s in range(e2e_steps + 1):
         tot = 0.0
         for i, (M, N, K) in enumerate(shapes):
-            hA, hB, hC = pinned[i]
+            hA, hB, hC, hCin = pinned[i]
             _, _, dA, dB, C = data[i]
             flush.fill_(0.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             dA.copy_(hA, non_blocking=True)
             dB.copy_(hB, non_blocking=True)
+            if hCin is not None:  # the fused epilogue's Cin is an input too
+                C.copy_(hCin, non_blocking=True)
             call(i)
             hC.copy_(C, non_blocking=True)
             e1.record(stream)
@@ -409,7 +422,7 @@ def run_ours(args):
         if s > 0:  # the first pass warms the copy engines
             e2e_ms.append(tot)
     e2e_step_ms = max_over_ranks([statistics.median(e2e_ms)], dev)[0]
-    h2d = sum(2 * (M * K + N * K) for (M, N, K) in shapes)
+    h2d = sum(2 * (M * K + N * K) + (c_bytes * M * N if fused else 0) for (M, N, K) in shapes)
     d2h = sum(c_bytes * M * N for (M, N, K) in shapes)
 
     line = None
@@ -428,6 +441,8 @@ def run_ours(args):
                 "workload": args.workload + ": " + ", ".join(shape_name(s) for s in shapes),
                 "inputs": f"uniform[-1,1] rounded to {ab}, seeded SplitMix64, resident in HBM",
                 "accumulate": "f32", "output": c,
+                "epilogue": ("D = A·Bᵀ + D + bias (fused; C read back in place)"
+                             if args.epilogue == "fused" else "C = A·Bᵀ"),
                 "l2": "flushed between calls (256 MiB write), each call timed alone",
                 "timing": ("CUDA events on the launching stream around each call; a GPU-side "
                        "spin ahead of the start event hides host enqueue latency"),
@@ -469,6 +484,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--types", choices=sorted(TYPES), default="f16f32",
                     help="operand and C types (the measured product is f16f32)")
+    ap.add_argument("--epilogue", choices=["plain", "fused"], default="plain",
+                    help="fused: D = A·Bᵀ + D + bias through the alpha/beta/bias epilogue")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.shape:

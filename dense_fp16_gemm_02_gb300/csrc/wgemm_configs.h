@@ -13,6 +13,7 @@ struct KernelEntry {
   int sched;                 // 0: static persistent grid, 1: cluster launch control
   int tile_rows, tile_cols;  // C rows / columns of one worker tile
   int out;                   // 0: fp32 C; 1: 16-bit C (fp16 or bf16), data parallel only
+  int fuse;                  // > 0: alpha/beta/bias epilogue (its Cin ring depth), data parallel only
   uint32_t smem_bytes;
   const void* func;          // the __global__ function (host stub)
 };
@@ -32,21 +33,25 @@ extern const KernelEntry kEntriesOut16A[];
 extern const int kNumEntriesOut16A;
 extern const KernelEntry kEntriesOut16B[];
 extern const int kNumEntriesOut16B;
+extern const KernelEntry kEntriesFused[];
+extern const int kNumEntriesFused;
 
 }  // namespace wg
 
 // Builds the entry of one configuration (only in .cu files that include the
 // kernel template). MC = MMA groups per cluster sharing the A tile; SCHED =
-// kSchedStatic or kSchedClc; OUT = kOut32 or kOut16.
-#define WG_ENTRY_OUT(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT)                      \
+// kSchedStatic or kSchedClc; OUT = kOut32 or kOut16; FUSE = 0 or 1.
+#define WG_ENTRY_ANY(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE)                \
   wg::KernelEntry {                                                                             \
     NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED,                                            \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT>::kTileRows,                     \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT>::kTileCols, OUT,                \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT>::kSmemBytes,                    \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE>::kTileRows,               \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE>::kTileCols, OUT, FUSE,    \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE>::kSmemBytes,              \
         reinterpret_cast<const void*>(                                                          \
-            &wg::wgemm_kernel<wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT>>)         \
+            &wg::wgemm_kernel<wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE>>)   \
   }
+#define WG_ENTRY_OUT(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT) \
+  WG_ENTRY_ANY(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, 0)
 #define WG_ENTRY_FULL(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED) \
   WG_ENTRY_OUT(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, wg::kOut32)
 #define WG_ENTRY_MC(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC) \
@@ -56,3 +61,12 @@ extern const int kNumEntriesOut16B;
 // 16-bit C: the same configuration with "_h" appended to its name.
 #define WG_ENTRY_H(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED) \
   WG_ENTRY_OUT(NAME "_h", CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, wg::kOut16)
+// alpha/beta/bias epilogue (register stores, static schedule) with a Cin
+// ring of SLOTS blocks per epilogue warp: "_ab<SLOTS>", and "_ab<SLOTS>_h"
+// with a 16-bit C.
+#define WG_ENTRY_AB(NAME, CG, REPS, BN, STAGES, ACC, SLOTS) \
+  WG_ENTRY_ANY(NAME "_ab" #SLOTS, CG, REPS, BN, STAGES, ACC, wg::kEpiDirect, 1, wg::kSchedStatic, \
+               wg::kOut32, SLOTS)
+#define WG_ENTRY_AB_H(NAME, CG, REPS, BN, STAGES, ACC, SLOTS) \
+  WG_ENTRY_ANY(NAME "_ab" #SLOTS "_h", CG, REPS, BN, STAGES, ACC, wg::kEpiDirect, 1, \
+               wg::kSchedStatic, wg::kOut16, SLOTS)

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -36,9 +37,48 @@ __global__ void wgemm_zero_kernel(void* C, int32_t M, int32_t N, int64_t ldc,
   }
 }
 
+// K == 0 with the fused epilogue: D := beta·Cin + bias[column] (the product
+// of an empty sum is 0), D and Cin of `elem_bytes` (4: fp32; 2: fp16 or bf16
+// by `bf16`). Cin is read only when beta != 0; bias may be null.
+__global__ void wgemm_axpby_kernel(void* D, int64_t ldd, const void* Cin, int64_t ldcin,
+                                   const float* bias, float beta, int32_t M, int32_t N,
+                                   int32_t elem_bytes, int32_t bf16) {
+  const int64_t total = (int64_t)M * N;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / N, c = i - r * N;
+    float v = bias ? bias[c] : 0.f;
+    if (beta != 0.f) {
+      float x;
+      if (elem_bytes == 4) {
+        x = static_cast<const float*>(Cin)[r * ldcin + c];
+      } else {
+        const uint16_t h = static_cast<const uint16_t*>(Cin)[r * ldcin + c];
+        x = bf16 ? __bfloat162float(__ushort_as_bfloat16(h)) : __half2float(__ushort_as_half(h));
+      }
+      v = fmaf(beta, x, v);
+    }
+    if (elem_bytes == 4) {
+      static_cast<float*>(D)[r * ldd + c] = v;
+    } else {
+      static_cast<uint16_t*>(D)[r * ldd + c] =
+          bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
+    }
+  }
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
+
+// The fused epilogue's operands (plain calls: fused = false).
+struct EpiArgs {
+  bool fused = false;
+  const void* cin = nullptr;
+  int ldcin = 0;
+  const float* bias = nullptr;
+  float alpha = 1.f, beta = 0.f;
+};
 
 struct Registry {
   std::vector<const KernelEntry*> entries;
@@ -50,6 +90,7 @@ struct Registry {
     for (int i = 0; i < kNumEntriesClc; ++i) entries.push_back(&kEntriesClc[i]);
     for (int i = 0; i < kNumEntriesOut16A; ++i) entries.push_back(&kEntriesOut16A[i]);
     for (int i = 0; i < kNumEntriesOut16B; ++i) entries.push_back(&kEntriesOut16B[i]);
+    for (int i = 0; i < kNumEntriesFused; ++i) entries.push_back(&kEntriesFused[i]);
   }
 };
 
@@ -274,11 +315,13 @@ double predict_us(const KernelEntry& e, int M, int N, int K, bool aligned, int m
   return t0 + waves * (a + b * (double)kblocks);
 }
 
-Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma_ok, int out) {
-  // The table was measured with fp32 C and rows on 32-byte sectors.
+Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma_ok, int out,
+              int fuse = 0) {
+  // The table was measured with fp32 C, the plain epilogue and rows on
+  // 32-byte sectors.
   const bool aligned = rows_on_sectors(lda, ldb);
   for (const TunedRow& r : kTuned) {
-    if (out == 0 && aligned && r.M == M && r.N == N && r.K == K) {
+    if (out == 0 && fuse == 0 && aligned && r.M == M && r.N == N && r.K == K) {
       const int id = find_config(r.config);
       const bool tma = std::strstr(r.config, "_tma") != nullptr;
       if (id >= 0 && (c_tma_ok || !tma)) return {id, r.mode, r.splits};
@@ -294,7 +337,8 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
   double best_us = 0.0, best_split_us = 0.0;
   for (int id = 0; id < (int)es.size(); ++id) {
     const KernelEntry& e = *es[id];
-    if (e.out != out || (e.epi == kEpiTma && !c_tma_ok)) continue;
+    if (e.out != out || (e.fuse != 0) != (fuse != 0) || (e.epi == kEpiTma && !c_tma_ok))
+      continue;
     const int w = max_workers(st, id);
     if (w <= 0) continue;
     auto consider = [&](int mode, int splits) {
@@ -307,7 +351,7 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
       }
     };
     consider(kDataParallel, 1);
-    const bool ksplit = e.epi == kEpiTma && e.mc == 1 && e.sched == 0 && e.out == 0;
+    const bool ksplit = e.epi == kEpiTma && e.mc == 1 && e.sched == 0 && e.out == 0 && !e.fuse;
     const int64_t tiles = (int64_t)((M + e.tile_rows - 1) / e.tile_rows) *
                           ((N + e.tile_cols - 1) / e.tile_cols);
     const int kblocks = (K + kBK - 1) / kBK;
@@ -321,6 +365,10 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
     return best_split;
   if (best.config >= 0) return best;
   // No rates compiled in: a plain fallback.
+  if (fuse) {
+    return {find_config(out == 0 ? "g2_256x256_s6_a2_direct_ab2" : "g2_256x256_s6_a2_direct_ab4_h"),
+            kDataParallel, 1};
+  }
   const char* fb = c_tma_ok ? "g2_256x256_s6_a2_tma" : "g2_256x256_s6_a2_direct";
   if (out == 0) return {find_config(fb), kDataParallel, 1};
   return {find_config((std::string(fb) + "_h").c_str()), kDataParallel, 1};
@@ -383,7 +431,8 @@ int make_plan(const KernelEntry& e, int M, int N, int K, int mode, int splits, i
   p->mode = mode;
   p->splits = 1;
   p->group = raster_group();
-  if (mode != kDataParallel && (e.epi != kEpiTma || e.mc != 1 || e.sched != 0 || e.out != 0))
+  if (mode != kDataParallel &&
+      (e.epi != kEpiTma || e.mc != 1 || e.sched != 0 || e.out != 0 || e.fuse != 0))
     return WGEMM_ERR_CONFIG;
   p->sched = e.sched;
   if (mode == kDataParallel && e.sched == 1) {
@@ -432,11 +481,19 @@ int workspace(int dev, cudaStream_t stream, size_t words, Workspace** out) {
 }
 
 int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, int N, int K,
-        int lda, int ldb, int ldc, int config_id, int mode, int splits, cudaStream_t stream) {
+        int lda, int ldb, int ldc, int config_id, int mode, int splits, cudaStream_t stream,
+        const EpiArgs& ep = EpiArgs()) {
   if (!ab_type_ok(ab_type) || !c_type_ok(c_type)) return WGEMM_ERR_INVALID_ARG;
   const int cb = c_bytes(c_type), out = c_type == WGEMM_F32 ? 0 : 1;
+  const int fuse = ep.fused ? 1 : 0;
   int rc = check_args(A, B, C, M, N, K, lda, ldb, ldc, cb);
   if (rc != WGEMM_OK) return rc;
+  const bool load_cin = ep.fused && ep.beta != 0.f;
+  if (load_cin) {
+    if (M > 0 && N > 0 && (!ep.cin || ep.ldcin < N)) return WGEMM_ERR_INVALID_ARG;
+    // Cin is read by TMA: 16-byte aligned base and row pitch.
+    if (M > 0 && N > 0 && !c_tma_ok(ep.cin, ep.ldcin, cb)) return WGEMM_ERR_ALIGNMENT;
+  }
   if (M == 0 || N == 0) return WGEMM_OK;
   std::lock_guard<std::mutex> lock(g_mu);
   int dev;
@@ -445,29 +502,35 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
   if (K == 0) {
     const int64_t total = (int64_t)M * N;
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)st->sm_count * 8);
-    wgemm_zero_kernel<<<blocks, 256, 0, stream>>>(C, M, N, ldc, cb);
+    if (ep.fused)
+      wgemm_axpby_kernel<<<blocks, 256, 0, stream>>>(C, ldc, ep.cin, ep.ldcin, ep.bias,
+                                                     load_cin ? ep.beta : 0.f, M, N, cb,
+                                                     c_type == WGEMM_BF16 ? 1 : 0);
+    else
+      wgemm_zero_kernel<<<blocks, 256, 0, stream>>>(C, M, N, ldc, cb);
     return cudaGetLastError() == cudaSuccess ? WGEMM_OK : WGEMM_ERR_LAUNCH;
   }
   const auto& es = registry().entries;
   const bool c_ok = c_tma_ok(C, ldc, cb);
   if (config_id < 0) {
-    Choice c = choose(*st, M, N, K, lda, ldb, c_ok, out);
+    Choice c = choose(*st, M, N, K, lda, ldb, c_ok, out, fuse);
     config_id = c.config;
     mode = c.mode;
     splits = c.splits;
   }
   if (config_id < 0 || config_id >= (int)es.size()) return WGEMM_ERR_CONFIG;
   const KernelEntry& e = *es[config_id];
-  if (e.out != out) return WGEMM_ERR_CONFIG;
+  if (e.out != out || (e.fuse != 0) != (fuse != 0)) return WGEMM_ERR_CONFIG;
   if (e.epi == kEpiTma && !c_ok) return WGEMM_ERR_ALIGNMENT;
   if (mode < 0) {
-    Choice c = choose(*st, M, N, K, lda, ldb, c_ok, out);
+    Choice c = choose(*st, M, N, K, lda, ldb, c_ok, out, fuse);
     mode = c.mode;
     splits = c.splits;
     if (mode != kDataParallel && e.epi != kEpiTma) mode = kDataParallel;
   }
-  // 16-bit C is rounded once from the full fp32 sum: no K split.
-  if (out != 0 && mode != kDataParallel) return WGEMM_ERR_CONFIG;
+  // 16-bit C is rounded once from the full fp32 sum, and the fused epilogue
+  // applies alpha, beta and bias to the full sum: no K split.
+  if ((out != 0 || fuse) && mode != kDataParallel) return WGEMM_ERR_CONFIG;
   const int mw = max_workers(*st, config_id);
   if (mw < 0) return mw;
   if ((rc = encoder()) != WGEMM_OK) return rc;
@@ -488,6 +551,15 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
   params.ldc = ldc;
   params.idesc = umma_idesc_f16(128u * e.cg, (uint32_t)e.bn, ab_type == WGEMM_BF16);
   params.c_bf16 = c_type == WGEMM_BF16 ? 1 : 0;
+  if (ep.fused) {
+    params.alpha = ep.alpha;
+    params.beta = ep.beta;
+    params.bias = ep.bias;
+    params.load_cin = load_cin ? 1 : 0;
+    if (load_cin && !encode_2d(&params.tmCin, tma_type(c_type), ep.cin, (uint64_t)N, (uint64_t)M,
+                               (uint64_t)ep.ldcin * cb, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return WGEMM_ERR_LAUNCH;
+  }
   params.status = st->status;
   params.trace = g_debug_trace;
   params.trace_ctas = g_debug_trace_ctas;
@@ -557,6 +629,34 @@ int wgemm_gemm_config(const void* A, const void* B, void* C, int ab_type, int c_
              reinterpret_cast<cudaStream_t>(stream));
 }
 
+int wgemm_gemm_ex(const void* A, const void* B, void* D, const void* Cin, const float* bias,
+                  float alpha, float beta, int ab_type, int c_type, int M, int N, int K, int lda,
+                  int ldb, int ldd, int ldcin, wgemm_stream_t stream) {
+  return wgemm_gemm_ex_config(A, B, D, Cin, bias, alpha, beta, ab_type, c_type, M, N, K, lda,
+                              ldb, ldd, ldcin, -1, stream);
+}
+
+int wgemm_gemm_ex_config(const void* A, const void* B, void* D, const void* Cin,
+                         const float* bias, float alpha, float beta, int ab_type, int c_type,
+                         int M, int N, int K, int lda, int ldb, int ldd, int ldcin,
+                         int config_id, wgemm_stream_t stream) {
+  if (config_id < -1 || config_id >= (int)registry().entries.size()) return WGEMM_ERR_CONFIG;
+  if (!std::isfinite(alpha) || !std::isfinite(beta)) return WGEMM_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // alpha = 1, beta = 0 and no bias is the plain product: every kernel.
+  if (config_id < 0 && alpha == 1.f && beta == 0.f && bias == nullptr)
+    return run(A, B, D, ab_type, c_type, M, N, K, lda, ldb, ldd, -1, -1, 1, s);
+  EpiArgs ep;
+  ep.fused = true;
+  ep.cin = Cin;
+  ep.ldcin = ldcin;
+  ep.bias = bias;
+  ep.alpha = alpha;
+  ep.beta = beta;
+  return run(A, B, D, ab_type, c_type, M, N, K, lda, ldb, ldd, config_id,
+             config_id < 0 ? -1 : kDataParallel, 1, s, ep);
+}
+
 int wgemm_bf16f32(const wgemm_bf16_t* A, const wgemm_bf16_t* B, float* C, int M, int N, int K,
                   int lda, int ldb, int ldc, wgemm_stream_t stream) {
   return wgemm_gemm(A, B, C, WGEMM_BF16, WGEMM_F32, M, N, K, lda, ldb, ldc, stream);
@@ -587,16 +687,17 @@ const char* wgemm_config_name(int id) {
   return (id >= 0 && id < (int)es.size()) ? es[id]->name : "";
 }
 
-int wgemm_select(int M, int N, int K, int lda, int ldb, int c_type, int* config_id, int* mode,
-                 int* splits) {
-  if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || !c_type_ok(c_type))
+int wgemm_select(int M, int N, int K, int lda, int ldb, int c_type, int fused, int* config_id,
+                 int* mode, int* splits) {
+  if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || !c_type_ok(c_type) ||
+      (fused != 0 && fused != 1))
     return WGEMM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
   int dev;
   DeviceState* st;
   const int rc = device_state(&dev, &st);
   if (rc != WGEMM_OK) return rc;
-  Choice c = choose(*st, M, N, K, lda, ldb, true, c_type == WGEMM_F32 ? 0 : 1);
+  Choice c = choose(*st, M, N, K, lda, ldb, true, c_type == WGEMM_F32 ? 0 : 1, fused);
   if (config_id) *config_id = c.config;
   if (mode) *mode = c.mode;
   if (splits) *splits = c.splits;
@@ -730,6 +831,12 @@ uint32_t wgemm_debug_idesc(int M, int N, int bf16) {
 int wgemm_debug_config_out(int config_id) {
   const auto& es = registry().entries;
   return (config_id >= 0 && config_id < (int)es.size()) ? es[config_id]->out : WGEMM_ERR_CONFIG;
+}
+
+int wgemm_debug_config_fused(int config_id) {
+  const auto& es = registry().entries;
+  return (config_id >= 0 && config_id < (int)es.size()) ? (es[config_id]->fuse != 0 ? 1 : 0)
+                                                          : WGEMM_ERR_CONFIG;
 }
 
 uint32_t wgemm_debug_sw128_offset(uint32_t row, uint32_t k) { return sw128_offset_f16(row, k); }

@@ -69,6 +69,7 @@ enum WaitSite : int32_t {
   kSiteEpiFlagOwner = 0x22,
   kSiteEpiFlagZero = 0x23,
   kSiteEpiSync = 0x24,
+  kSiteEpiCinFull = 0x25,
   // index checks of debug builds
   kCheckPlan = 0x31,
   kCheckTmemMma = 0x32,
@@ -81,6 +82,7 @@ enum WaitSite : int32_t {
   kSiteClcFull = 0x42,
   kSiteAbortLoads = 0x51,
   kSiteAbortClc = 0x52,
+  kSiteAbortCin = 0x53,
 };
 
 struct KParams {
@@ -92,6 +94,11 @@ struct KParams {
   int64_t ldc;      // in elements
   uint32_t idesc;   // tcgen05.mma instruction descriptor (operand types, M, N)
   int32_t c_bf16;   // 16-bit-output kernels: 1 = bf16, 0 = fp16
+  // Fused epilogue (FUSE kernels): D = alpha·acc + beta·Cin + bias[column].
+  CUtensorMap tmCin;    // Cin (M×N, C's type): box {32, 32}; read when load_cin
+  const float* bias;    // N fp32 values, or null
+  float alpha, beta;
+  int32_t load_cin;     // 1: read Cin (beta != 0)
   uint32_t* flags;  // split-K / stream-K flags (monotone epochs)
   uint32_t epoch;
   int32_t flag_words;  // words the flag array holds
@@ -136,9 +143,12 @@ enum SchedMode : int { kSchedStatic = 0, kSchedClc = 1 };
 enum OutWidth : int { kOut32 = 0, kOut16 = 1 };
 
 template <int CG_, int REPS_, int BN_, int STAGES_, int ACC_, int EPI_, int MC_ = 1,
-          int SCHED_ = kSchedStatic, int OUT_ = kOut32>
+          int SCHED_ = kSchedStatic, int OUT_ = kOut32, int FUSE_ = 0>
 struct Cfg {
   static constexpr int OUT = OUT_;        // OutWidth: fp32 C, or 16-bit C (data parallel only)
+  // FUSE > 0: alpha/beta/bias epilogue (data parallel only) whose Cin ring
+  // has FUSE slots per epilogue warp.
+  static constexpr int FUSE = FUSE_;
   static constexpr int SCHED = SCHED_;    // SchedMode
   static constexpr int CG = CG_;          // CTAs per MMA: 1, or 2 (pair)
   static constexpr int MC = MC_;          // MMA groups per cluster sharing the A tile
@@ -171,23 +181,31 @@ struct Cfg {
   static constexpr int kEpiBatch = EPI == kEpiTma ? (BN / 32 >= 2 ? 2 : 1)
                                                   : (BN / 32 >= 4 ? 4 : BN / 32);
   static constexpr uint32_t kEpiBytes = EPI == kEpiTma ? 4 * kEpiBatch * kEpiSlotBytes : 0;
+  // Fused epilogue: each epilogue warp prefetches its 32×32 blocks of Cin
+  // with TMA into a private ring of kCinSlots slots.
+  static constexpr int kCinSlots = FUSE;
+  static constexpr uint32_t kCinBytes = 4 * kCinSlots * kEpiSlotBytes;
 
   // Shared-memory layout (offsets from a 1024-byte-aligned base).
   static constexpr uint32_t kOffStages = 0;
   static constexpr uint32_t kOffEpi = STAGES * kStageBytes;
-  static constexpr uint32_t kOffBars = kOffEpi + kEpiBytes;
+  static constexpr uint32_t kOffCin = kOffEpi + kEpiBytes;
+  static constexpr uint32_t kOffBars = kOffCin + kCinBytes;
   // Cluster launch control: a ring of kClcDepth 16-byte responses, each with a
   // full barrier (bytes of the response) and an empty barrier (releases of
   // every consumer in the cluster, gathered in the cluster leader).
   static constexpr int kClcDepth = SCHED == kSchedClc ? 4 : 0;
   static constexpr uint32_t kClcConsumers = kClusterSize * 6 + MC;
-  static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 2 + 2 * kClcDepth;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 2 + 2 * kClcDepth + 4 * kCinSlots;
   static constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
   static constexpr uint32_t kOffResp = (kOffMisc + 16 + 15) / 16 * 16;
   static constexpr uint32_t kSmemBytes = kOffResp + 16 * kClcDepth + 1024;  // + alignment slack
 
   static_assert(CG == 1 || CG == 2, "CG");
   static_assert(OUT == kOut32 || OUT == kOut16, "OUT");
+  static_assert(!FUSE || EPI == kEpiDirect, "the fused epilogue stores from registers");
+  static_assert(!FUSE || SCHED == kSchedStatic, "the Cin ring prefetches the next unit");
+  static_assert(FUSE >= 0 && FUSE <= 8, "Cin ring depth");
   static_assert(MC == 1 || MC == 2, "MC");
   static_assert(kBrowsPart % 8 == 0, "multicast part in 8-row groups");
   static_assert(REPS == 1 || REPS == 2, "REPS");
@@ -284,6 +302,22 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch,
   }
 }
 
+// Fused epilogue state of one epilogue warp (warp-uniform, except `bias`):
+// the current unit's geometry, its Cin blocks, and the ring counters.
+struct CinUnit {
+  int32_t col_cta, row0;  // the unit's first C column of this CTA, first C row
+  int32_t lc;             // chunks (32 rows) of the unit holding rows of C, per atom
+  int32_t nblk;           // Cin blocks of this warp in the unit: atoms with columns × lc
+};
+struct FuseState {
+  CinUnit cur, next;      // this unit, and the worker's next unit (nblk 0: none)
+  int32_t t;              // next block of the unit to consume
+  int32_t cur_issued;     // blocks of this unit issued so far (in order)
+  int32_t pre;            // blocks of the next unit issued so far (in order)
+  uint32_t issued, consumed;  // Cin loads issued / consumed since kernel start
+  float bias[2];          // bias of this lane's column, per atom (0 without bias)
+};
+
 template <class K>
 struct Kernel {
   // Barrier addresses.
@@ -311,6 +345,14 @@ struct Kernel {
     return base + K::kOffBars + 8 * (2 * K::STAGES + 2 * K::ACC + 2 + K::kClcDepth + j);
   }
   __device__ static uint32_t clc_resp(uint32_t base, int j) { return base + K::kOffResp + 16 * j; }
+  // Fused epilogue: Cin slot s of epilogue warp q, and its full barrier.
+  __device__ static uint32_t bar_cin(uint32_t base, uint32_t q, uint32_t s) {
+    return base + K::kOffBars +
+           8 * (2 * K::STAGES + 2 * K::ACC + 2 + 2 * K::kClcDepth + q * K::kCinSlots + s);
+  }
+  __device__ static uint32_t cin_slot(uint32_t base, uint32_t q, uint32_t s) {
+    return base + K::kOffCin + (q * K::kCinSlots + s) * K::kEpiSlotBytes;
+  }
 
   // Unit i of this CTA's worker (cluster). Static scheduling: the plan's
   // order. Cluster launch control: unit 0 is the worker's own tile, unit
@@ -587,11 +629,132 @@ struct Kernel {
   // columns col_warp + lane. Chunks wholly outside C are skipped. When
   // `release` is set the accumulator is handed back to the MMA warp once the
   // batch's TMEM reads are complete.
+  // Fused epilogue, lane 0: load Cin block t of unit `g` (atom t / lc, chunk
+  // t % lc) of epilogue warp q into the next ring slot.
+  __device__ static void cin_issue(const KParams& p, uint32_t base, uint32_t q, const CinUnit& g,
+                                   uint32_t issued, int32_t t) {
+    const int32_t r = t / g.lc, c = t - r * g.lc;
+    const uint32_t slot = issued % (uint32_t)K::kCinSlots;
+    const uint32_t bar = bar_cin(base, q, slot);
+    mbar_arrive_expect_tx(bar, K::kEpiSlotBytes);
+    tma_load_2d(cin_slot(base, q, slot), &p.tmCin, bar, g.col_cta + r * 128 + (int32_t)q * 32,
+                g.row0 + 32 * c);
+  }
+
+  // The Cin geometry of unit i of `worker` for epilogue warp q (nblk = 0 when
+  // the worker has no unit i).
+  __device__ static CinUnit cin_unit(const KParams& p, uint32_t q, uint32_t rank, uint32_t grp,
+                                     int32_t worker, int32_t i) {
+    CinUnit g{0, 0, 0, 0};
+    Unit u;
+    if (!plan_unit(p.plan, worker, i, u)) return g;
+    const int32_t M = p.plan.M, N = p.plan.N;
+    constexpr int kChunks = K::BN / 32;
+    g.col_cta = u.tn * K::kTileCols + (int32_t)grp * K::kGroupCols + (int32_t)rank * K::kCtaCols;
+    g.row0 = u.tm * K::kTileRows;
+    const int32_t rows = M - g.row0;
+    g.lc = rows <= 0 ? 0 : ((rows + 31) / 32 < kChunks ? (rows + 31) / 32 : kChunks);
+    int32_t atoms = 0;
+#pragma unroll
+    for (int r = 0; r < K::REPS; ++r)
+      if (g.col_cta + r * 128 + (int32_t)q * 32 < N) atoms = r + 1;
+    g.nblk = atoms * g.lc;
+    return g;
+  }
+
+  // Fused epilogue, at the start of unit i (before its accumulator is full):
+  // this lane's bias, the next unit's geometry, and the unit's first Cin
+  // loads (those the previous unit did not already issue).
+  __device__ static void fuse_begin(const KParams& p, uint32_t base, uint32_t q, uint32_t rank,
+                                    uint32_t grp, int32_t worker, int32_t i, FuseState& f) {
+    const uint32_t lane = threadIdx.x % 32;
+    const int32_t N = p.plan.N;
+    f.cur = i == 0 ? cin_unit(p, q, rank, grp, worker, 0) : f.next;
+    f.next = cin_unit(p, q, rank, grp, worker, i + 1);
+#pragma unroll
+    for (int r = 0; r < K::REPS; ++r) {
+      const int32_t col = f.cur.col_cta + r * 128 + (int32_t)q * 32 + (int32_t)lane;
+      f.bias[r] = (p.bias != nullptr && col < N) ? p.bias[col] : 0.f;
+    }
+    f.t = 0;
+    f.cur_issued = i == 0 ? 0 : f.pre;  // issued while the previous unit drained
+    f.pre = 0;
+    if (!p.load_cin) return;
+    // The slots were last read by this warp's generic loads: order those
+    // reads before the TMA writes that refill them.
+    fence_proxy_async_shared();
+    __syncwarp();
+    // Fill the ring: at most kCinSlots loads in flight.
+    while (f.cur_issued < f.cur.nblk && f.issued - f.consumed < (uint32_t)K::kCinSlots) {
+      if (lane == 0) cin_issue(p, base, q, f.cur, f.issued, f.cur_issued);
+      ++f.issued;
+      ++f.cur_issued;
+    }
+  }
+
+  // Fused epilogue: turn the accumulator values of chunks [c0, c0 + nb) of
+  // atom r into alpha·acc + beta·Cin + bias, consuming the Cin blocks in
+  // ring order and refilling each slot with the block kCinSlots ahead (of
+  // this unit, else of the next one). False if a wait gave up.
   template <int NBB>
-  __device__ static void drain(const KParams& p, uint32_t base, uint8_t* smem, uint32_t tmem,
+  __device__ static bool fuse_apply(const KParams& p, uint32_t base, uint8_t* smem, uint32_t q,
+                                    int r, int c0, int nb, uint32_t (&v)[NBB][32], FuseState& f,
+                                    volatile uint32_t* abort_flag) {
+    const uint32_t lane = threadIdx.x % 32;
+    const float alpha = p.alpha, beta = p.beta, bias = f.bias[r];
+#pragma unroll
+    for (int b = 0; b < NBB; ++b) {
+      if (b >= nb) break;
+      const int32_t c = c0 + b;
+      if (c >= f.cur.lc) break;  // rows past M: nothing of this chunk is stored
+      if (p.load_cin) {
+        const uint32_t slot = f.consumed % (uint32_t)K::kCinSlots;
+        if (!wait_bar(bar_cin(base, q, slot), (f.consumed / (uint32_t)K::kCinSlots) & 1u,
+                      abort_flag, p.status, kSiteEpiCinFull))
+          return false;
+        const uint8_t* sp = smem + (cin_slot(base, q, slot) - base);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float cin;
+          if constexpr (K::OUT == kOut16) {
+            const uint16_t h = reinterpret_cast<const uint16_t*>(sp)[e * 32 + lane];
+            cin = p.c_bf16 ? __bfloat162float(__ushort_as_bfloat16(h))
+                           : __half2float(__ushort_as_half(h));
+          } else {
+            cin = reinterpret_cast<const float*>(sp)[e * 32 + lane];
+          }
+          v[b][e] = __float_as_uint(fmaf(alpha, __uint_as_float(v[b][e]), fmaf(beta, cin, bias)));
+        }
+        ++f.consumed;
+        fence_proxy_async_shared();
+        __syncwarp();
+        // The freed slot takes the next block in consumption order: this
+        // unit's, else the next unit's.
+        if (f.cur_issued < f.cur.nblk) {
+          if (lane == 0) cin_issue(p, base, q, f.cur, f.issued, f.cur_issued);
+          ++f.issued;
+          ++f.cur_issued;
+        } else if (f.pre < f.next.nblk) {
+          if (lane == 0) cin_issue(p, base, q, f.next, f.issued, f.pre);
+          ++f.issued;
+          ++f.pre;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          v[b][e] = __float_as_uint(fmaf(alpha, __uint_as_float(v[b][e]), bias));
+      }
+      ++f.t;
+    }
+    return true;
+  }
+
+  template <int NBB>
+  __device__ static bool drain(const KParams& p, uint32_t base, uint8_t* smem, uint32_t tmem,
                                uint32_t tatom, int c0, int nb, int32_t col_warp, int32_t row0,
                                bool add, uint32_t stage_base, bool release, uint32_t ab,
-                               uint32_t grp) {
+                               uint32_t grp, int r, FuseState& fs,
+                               volatile uint32_t* abort_flag) {
     const uint32_t lane = threadIdx.x % 32;
     const int32_t M = p.plan.M, N = p.plan.N;
     const int64_t ldc = p.ldc;
@@ -617,7 +780,11 @@ struct Kernel {
         else mbar_arrive_cluster(mapa_shared(bar_acce(base, ab), group_leader(grp)));
       }
     }
-    if (!live) return;
+    if (!live) return true;
+    if constexpr (K::FUSE) {
+      if (!fuse_apply<NBB>(p, base, smem, (threadIdx.x / 32) & 3u, r, c0, nb, v, fs, abort_flag))
+        return false;
+    }
     if constexpr (K::EPI == kEpiDirect && K::OUT == kOut16) {
       const int32_t col = col_warp + (int32_t)lane;
       if (col < N) {
@@ -682,7 +849,7 @@ struct Kernel {
                     stage_base - base + nb * K::kEpiSlotBytes <= K::kOffBars &&
                         stage_base - base >= K::kOffEpi,
                     kCheckStaging, stage_base - base))
-        return;
+        return true;
       if (lane == 0) bulk_wait_group_read<0>();
       __syncwarp();
 #pragma unroll
@@ -716,6 +883,7 @@ struct Kernel {
         bulk_commit_group();
       }
     }
+    return true;
   }
 
   // ------------------------------------------------------------ epilogue
@@ -736,11 +904,16 @@ struct Kernel {
 
     uint32_t ab = 0, aph = 0;
     const uint32_t stage_base = base + K::kOffEpi + q * 2 * K::kEpiSlotBytes;
+    FuseState fs{};
     for (int32_t i = 0; ok; ++i) {
       Unit u;
       bool got = next_unit(p, base, worker, i, lane == 0, true, u, ok, abort_flag, kSiteClcFull);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!got || !ok) break;
+      if constexpr (K::FUSE) {
+        // Start this unit's Cin loads before its accumulator is full.
+        fuse_begin(p, base, q, rank, grp, worker, i, fs);
+      }
       if (!wait_bar(bar_accf(base, ab), aph, abort_flag, p.status, kSiteEpiAccFull)) {
         ok = false;
         break;
@@ -791,10 +964,16 @@ struct Kernel {
           // The last batch of an atom may be short (kChunks not a multiple of
           // NB); one register array of NB chunks serves every batch.
           const int nb = kChunks - c0 < NB ? kChunks - c0 : NB;
-          drain<NB>(p, base, smem, tmem, tacc + r * K::BN, c0, nb, col_warp, row0, add,
-                    stage_base, last_atom && c0 + nb == kChunks, ab, grp);
+          if (!drain<NB>(p, base, smem, tmem, tacc + r * K::BN, c0, nb, col_warp, row0, add,
+                         stage_base, last_atom && c0 + nb == kChunks, ab, grp, r, fs,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
         }
+        if (!ok) break;
       }
+      if (!ok) break;
       if constexpr (K::EPI == kEpiTma) {
         if (u.kind == kUnitStoreRaise) {
           // Owner of the tile's first k-block: make the stores complete and
@@ -816,6 +995,14 @@ struct Kernel {
     }
     if constexpr (K::EPI == kEpiTma) {
       if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
+    }
+    if constexpr (K::FUSE) {
+      // Aborted: let this warp's Cin loads in flight land before exit.
+      if (!ok && p.load_cin && lane == 0)
+        for (uint32_t j = fs.consumed; j != fs.issued; ++j)
+          wait_bar_final(bar_cin(base, q, j % (uint32_t)K::kCinSlots),
+                         (j / (uint32_t)K::kCinSlots) & 1u, p.status, kSiteAbortCin);
       __syncwarp();
     }
     if (WGEMM_TRACE && threadIdx.x == 128) trace_event(p, kTrEpiDone);
@@ -908,6 +1095,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
       mbar_init(Kernel<K>::bar_clc_full(base, j), 1);
       mbar_init(Kernel<K>::bar_clc_empty(base, j), K::kClcConsumers);
     }
+    for (int j = 0; j < 4 * K::kCinSlots; ++j)
+      mbar_init(Kernel<K>::bar_cin(base, j / K::kCinSlots, j % K::kCinSlots), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     // Programmatic dependent launch: everything above touches no global

@@ -43,7 +43,7 @@ def candidates(M, N, K, names, workers_pair, workers_single):
     kb = -(-K // 64)
     out = []
     for cid, name in enumerate(names):
-        if name.endswith("_h"):  # 16-bit C: not a candidate for an fp32 call
+        if name.endswith("_h") or "_ab" in name:  # 16-bit C or fused: not a plain fp32 call
             continue
         cg = 2 if name.startswith("g2") else 1
         cols, rows = (int(v) for v in name.split("_")[1].split("x"))
@@ -205,9 +205,14 @@ def rates(out_path, points=RATE_POINTS):
             X, y = [], []
             for waves, K in points:
                 M = waves * M1
-                call = (lambda M=M, K=K, ld=ld: wgemm.wgemm_gemm_config(
-                    dA.data_ptr(), dB.data_ptr(), C.data_ptr(), wgemm.WGEMM_F16, c_type, M, N,
-                    K, ld, ld, N, cid, 0, 1, h))
+                if "_ab" in name:  # fused epilogue: D = 1·A·Bᵀ + 1·D (Cin read in place)
+                    call = (lambda M=M, K=K, ld=ld: wgemm.wgemm_gemm_ex_config(
+                        dA.data_ptr(), dB.data_ptr(), C.data_ptr(), C.data_ptr(), None, 1.0,
+                        1.0, wgemm.WGEMM_F16, c_type, M, N, K, ld, ld, N, N, cid, h))
+                else:
+                    call = (lambda M=M, K=K, ld=ld: wgemm.wgemm_gemm_config(
+                        dA.data_ptr(), dB.data_ptr(), C.data_ptr(), wgemm.WGEMM_F16, c_type, M,
+                        N, K, ld, ld, N, cid, 0, 1, h))
                 t = _time_calls(wgemm, torch, None, M, N, K, call, flush)
                 kb = (K + 63) // 64
                 X.append([1.0, waves, waves * kb])

@@ -58,6 +58,14 @@ def load():
         lib.wgemm_gemm.restype = i
         lib.wgemm_gemm_config.argtypes = [p, p, p, i, i, i, i, i, i, i, i, i, i, i, p]
         lib.wgemm_gemm_config.restype = i
+        f = ctypes.c_float
+        lib.wgemm_gemm_ex.argtypes = [p, p, p, p, p, f, f, i, i, i, i, i, i, i, i, i, p]
+        lib.wgemm_gemm_ex.restype = i
+        lib.wgemm_gemm_ex_config.argtypes = [p, p, p, p, p, f, f, i, i, i, i, i, i, i, i, i, i,
+                                             p]
+        lib.wgemm_gemm_ex_config.restype = i
+        lib.wgemm_debug_config_fused.argtypes = [i]
+        lib.wgemm_debug_config_fused.restype = i
         for name in ("wgemm_bf16f32", "wgemm_f16f16", "wgemm_bf16bf16"):
             getattr(lib, name).argtypes = [p, p, p, i, i, i, i, i, i, p]
             getattr(lib, name).restype = i
@@ -67,7 +75,7 @@ def load():
         lib.wgemm_num_configs.restype = i
         lib.wgemm_config_name.argtypes = [i]
         lib.wgemm_config_name.restype = ctypes.c_char_p
-        lib.wgemm_select.argtypes = [i, i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i),
+        lib.wgemm_select.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i),
                                      ctypes.POINTER(i)]
         lib.wgemm_select.restype = i
         lib.wgemm_check.argtypes = [p]
@@ -185,6 +193,24 @@ def wgemm_bf16bf16(A, B, C, M, N, K, lda, ldb, ldc, stream) -> int:
     return load().wgemm_bf16bf16(A, B, C, M, N, K, lda, ldb, ldc, stream)
 
 
+def wgemm_gemm_ex(A, B, D, Cin, bias, alpha, beta, ab_type, c_type, M, N, K, lda, ldb, ldd,
+                  ldcin, stream) -> int:
+    """The fused-epilogue C call on device pointers; returns the status code."""
+    return load().wgemm_gemm_ex(A, B, D, Cin, bias, alpha, beta, ab_type, c_type, M, N, K, lda,
+                                ldb, ldd, ldcin, stream)
+
+
+def wgemm_gemm_ex_config(A, B, D, Cin, bias, alpha, beta, ab_type, c_type, M, N, K, lda, ldb,
+                         ldd, ldcin, config, stream) -> int:
+    return load().wgemm_gemm_ex_config(A, B, D, Cin, bias, alpha, beta, ab_type, c_type, M, N,
+                                       K, lda, ldb, ldd, ldcin, config, stream)
+
+
+def config_fused(config: int) -> int:
+    """1 if the configuration has the alpha/beta/bias epilogue, else 0."""
+    return load().wgemm_debug_config_fused(config)
+
+
 def config_out(config: int) -> int:
     """0 if the configuration writes fp32 C, 1 if 16-bit C."""
     return load().wgemm_debug_config_out(config)
@@ -198,14 +224,14 @@ def wgemm_f16f32_splitk_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, 
 
 
 def wgemm_select(M: int, N: int, K: int, lda: int | None = None, ldb: int | None = None,
-                 c_type: int = WGEMM_F32) -> tuple[int, int, int]:
+                 c_type: int = WGEMM_F32, fused: bool = False) -> tuple[int, int, int]:
     """(configuration id, mode, splits) that the library runs for this shape,
-    these row pitches (K when omitted) and this C type."""
+    these row pitches (K when omitted), this C type and epilogue."""
     lda = K if lda is None else lda
     ldb = K if ldb is None else ldb
     c, m, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    rc = load().wgemm_select(M, N, K, lda, ldb, c_type, ctypes.byref(c), ctypes.byref(m),
-                             ctypes.byref(s))
+    rc = load().wgemm_select(M, N, K, lda, ldb, c_type, 1 if fused else 0, ctypes.byref(c),
+                             ctypes.byref(m), ctypes.byref(s))
     if rc != WGEMM_OK:
         raise WgemmError(rc, "wgemm_select")
     return c.value, m.value, s.value
@@ -243,6 +269,45 @@ def _wgemm_type(dtype) -> int:
     if dtype not in types:
         raise TypeError(f"unsupported element type {dtype}")
     return types[dtype]
+
+
+def gemm_ex(A, B, D=None, *, Cin=None, bias=None, alpha: float = 1.0, beta: float = 0.0,
+            out_dtype=None, config: int | str | None = None, stream=None):
+    """D = alpha·A·Bᵀ + beta·Cin + bias[None, :] for torch tensors (the fused
+    epilogue): A, B as for gemm(); Cin of D's type (M×N, may be D itself);
+    bias an N-element float32 tensor. D is allocated when not given."""
+    import torch
+    if A.dtype not in (torch.float16, torch.bfloat16) or B.dtype != A.dtype:
+        raise TypeError("A and B must both be float16 or both bfloat16")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError("A must be M×K and B N×K")
+    if A.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("A and B need a contiguous last dimension")
+    M, K = A.shape
+    N = B.shape[0]
+    if D is None:
+        D = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
+    if D.shape != (M, N) or D.stride(1) != 1:
+        raise ValueError("D must be M×N with a contiguous last dimension")
+    if Cin is not None and (Cin.shape != (M, N) or Cin.stride(1) != 1 or Cin.dtype != D.dtype):
+        raise ValueError("Cin must be M×N of D's type with a contiguous last dimension")
+    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != N
+                             or not bias.is_contiguous()):
+        raise ValueError("bias must be N contiguous float32 values")
+    ab_type, c_type = _wgemm_type(A.dtype), _wgemm_type(D.dtype)
+    if M == 0 or N == 0:
+        return D
+    h = _stream_handle(stream)
+    cid = -1 if config is None else (config_id(config) if isinstance(config, str) else int(config))
+    rc = wgemm_gemm_ex_config(A.data_ptr(), B.data_ptr(), D.data_ptr(),
+                              None if Cin is None else Cin.data_ptr(),
+                              None if bias is None else bias.data_ptr(), float(alpha),
+                              float(beta), ab_type, c_type, M, N, K, max(A.stride(0), K),
+                              max(B.stride(0), K), D.stride(0),
+                              N if Cin is None else Cin.stride(0), cid, h)
+    if rc != WGEMM_OK:
+        raise WgemmError(rc, "wgemm_gemm_ex")
+    return D
 
 
 def gemm(A, B, C=None, *, out_dtype=None, config: int | str | None = None, mode: int = -1,

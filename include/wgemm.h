@@ -130,6 +130,40 @@ int wgemm_gemm_config(const void* A, const void* B, void* C, int ab_type, int c_
                       int config_id, int mode, int splits,
                       wgemm_stream_t stream);
 
+/*
+ * The product with a fused epilogue (page 1 has no counterpart; it is the
+ * usual GEMM epilogue of a linear layer):
+ *
+ *     D[i·ldd + j] = alpha · Σ_k A[i·lda + k]·B[j·ldb + k] + beta · Cin[i·ldcin + j] + bias[j]
+ *
+ * computed in fp32 from the fp32 sum (fmaf(alpha, sum, fmaf(beta, Cin, bias))),
+ * then, for a 16-bit D, rounded once to nearest-even.
+ *   D:    M×N of c_type (WGEMM_F32, WGEMM_F16 or WGEMM_BF16), row pitch ldd.
+ *   Cin:  M×N of c_type, row pitch ldcin; read only when beta != 0 (it may
+ *         then be NULL). It is read with TMA: a 16-byte aligned base and
+ *         ldcin · element size a multiple of 16, else WGEMM_ERR_ALIGNMENT.
+ *         Cin may be D itself (ldcin == ldd): every element is read before it
+ *         is written. Any other overlap of Cin and D is undefined.
+ *   bias: N fp32 values (device memory), or NULL for none.
+ *   alpha, beta: finite fp32 scalars (WGEMM_ERR_INVALID_ARG otherwise).
+ * A, B, types and alignment as wgemm_gemm. K == 0 gives D = beta·Cin + bias.
+ * alpha = 1, beta = 0 and bias = NULL is exactly wgemm_gemm (any kernel);
+ * otherwise the call runs one of the fused configurations (names ending in
+ * "_ab", or "_ab_h" for a 16-bit D), data parallel; each epilogue warp
+ * prefetches its blocks of Cin with TMA while the unit's main loop runs.
+ * wgemm_gemm_ex_config forces a fused configuration (config_id ≥ 0), or
+ * chooses (-1); WGEMM_ERR_CONFIG for a configuration that is not fused or is
+ * of the other D width.
+ */
+int wgemm_gemm_ex(const void* A, const void* B, void* D, const void* Cin, const float* bias,
+                  float alpha, float beta, int ab_type, int c_type,
+                  int M, int N, int K, int lda, int ldb, int ldd, int ldcin,
+                  wgemm_stream_t stream);
+int wgemm_gemm_ex_config(const void* A, const void* B, void* D, const void* Cin,
+                         const float* bias, float alpha, float beta, int ab_type, int c_type,
+                         int M, int N, int K, int lda, int ldb, int ldd, int ldcin,
+                         int config_id, wgemm_stream_t stream);
+
 /* Typed shorthands of wgemm_gemm: bf16 → fp32, fp16 → fp16, bf16 → bf16. */
 int wgemm_bf16f32(const wgemm_bf16_t* A, const wgemm_bf16_t* B, float* C,
                   int M, int N, int K, int lda, int ldb, int ldc,
@@ -163,8 +197,9 @@ int wgemm_num_configs(void);
 const char* wgemm_config_name(int config_id);
 
 /*
- * The choice wgemm_f16f32 (c_type WGEMM_F32) or wgemm_gemm (any c_type; the
- * operand type does not enter) makes for a shape and operand row pitches
+ * The choice wgemm_f16f32 (c_type WGEMM_F32, fused 0), wgemm_gemm (any
+ * c_type; the operand type does not enter) or wgemm_gemm_ex (fused 1: among
+ * the fused configurations) makes for a shape and operand row pitches
  * (lda, ldb, in elements) on the current device: for fp32 C, the measured
  * per-shape table if the shape is in it and both pitches are multiples of 16
  * elements (rows on 32-byte sectors, as the table was measured); else the
@@ -175,10 +210,10 @@ const char* wgemm_config_name(int config_id);
  * only when it predicts at least 20% less time than the best data-parallel
  * configuration. Writes the configuration id, mode and splits (any pointer
  * may be NULL). Returns WGEMM_OK, WGEMM_ERR_INVALID_ARG (negative size, a
- * pitch below K, an unknown c_type) or a device error.
+ * pitch below K, an unknown c_type, fused not 0 or 1) or a device error.
  */
-int wgemm_select(int M, int N, int K, int lda, int ldb, int c_type, int* config_id, int* mode,
-                 int* splits);
+int wgemm_select(int M, int N, int K, int lda, int ldb, int c_type, int fused, int* config_id,
+                 int* mode, int* splits);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
@@ -248,7 +283,8 @@ int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16_t* B, floa
  * shape M×N×16 with an f32 accumulator, fp16 operands (bf16 = 0) or bf16
  * operands (bf16 = 1).
  * wgemm_debug_config_out: 0 if a configuration writes fp32 C, 1 if 16-bit C,
- * WGEMM_ERR_CONFIG for an unknown id.
+ * WGEMM_ERR_CONFIG for an unknown id. wgemm_debug_config_fused: 1 if it has
+ * the alpha/beta/bias epilogue, else 0 (WGEMM_ERR_CONFIG for an unknown id).
  * wgemm_debug_sw128_offset: byte offset of fp16 element (row, k) inside a
  * 1024-byte-aligned 128-byte-swizzled K-major tile.
  * wgemm_debug_plan: fills `out` (7 int32 per unit: tile, tm, tn, kb_begin,
@@ -296,6 +332,7 @@ double wgemm_debug_predict_us(int M, int N, int K, int lda, int ldb, int config_
 uint64_t wgemm_debug_smem_desc(uint32_t smem_addr);
 uint32_t wgemm_debug_idesc(int M, int N, int bf16);
 int wgemm_debug_config_out(int config_id);
+int wgemm_debug_config_fused(int config_id);
 uint32_t wgemm_debug_sw128_offset(uint32_t row, uint32_t k);
 int wgemm_debug_plan(int M, int N, int K, int config_id, int mode, int splits, int workers,
                      int32_t* out, int max_units, int* tile_rows, int* tile_cols);

@@ -63,6 +63,8 @@ def _load():
             lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
             lib.oracle_round_f64.argtypes = [p, p, i64, ctypes.c_int]
             lib.oracle_round_f64.restype = ctypes.c_int
+            lib.oracle_decode_array.argtypes = [p, p, i64, ctypes.c_int]
+            lib.oracle_decode_array.restype = ctypes.c_int
             lib.oracle_gemm_f64.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int]
             lib.oracle_gemm_f64.restype = ctypes.c_int
             lib.oracle_gemm_f64_select.argtypes = [p, p, p, i64, p, i64, i64, i64, i64, p, p, i64,
@@ -116,11 +118,34 @@ def bf16_to_f64(bits: int) -> float:
     return _load().oracle_bf16_to_f64(bits)
 
 
+def decode_array(bits: np.ndarray, kind: str) -> np.ndarray:
+    """Decode an array of fp16 ("f16") or bf16 ("bf16") bit patterns with the
+    oracle's decoders."""
+    t = {"f16": F16, "bf16": BF16}[kind]
+    flat = np.ascontiguousarray(bits, dtype=np.uint16).ravel()
+    out = np.empty(flat.shape, dtype=np.float64)
+    if _load().oracle_decode_array(_ptr(flat), _ptr(out), flat.size, t) != 0:
+        raise RuntimeError("oracle_decode_array failed")
+    return out.reshape(np.shape(bits))
+
+
 def bf16_to_f64_array(bits: np.ndarray) -> np.ndarray:
     """Decode an array of bf16 bit patterns with the oracle's decoder."""
-    f = _load().oracle_bf16_to_f64
-    flat = np.ascontiguousarray(bits, dtype=np.uint16).ravel()
-    return np.array([f(int(b)) for b in flat], dtype=np.float64).reshape(np.shape(bits))
+    return decode_array(bits, "bf16")
+
+
+def epilogue_f64(C: np.ndarray, alpha: float, beta: float = 0.0, Cin: np.ndarray | None = None,
+                 bias: np.ndarray | None = None) -> np.ndarray:
+    """The fused epilogue's definition in fp64 on the oracle's sum C:
+    D = alpha·C + beta·Cin + bias[None, :] (Cin as values, bias per column).
+    It follows no passage of the pages, which measure the plain product; it
+    is the declared contract of the library's fused entry point."""
+    D = float(alpha) * C
+    if beta != 0.0:
+        D = D + float(beta) * np.asarray(Cin, dtype=np.float64)
+    if bias is not None:
+        D = D + np.asarray(bias, dtype=np.float64)[None, :]
+    return D
 
 
 def round_f64(x: np.ndarray, to: str) -> np.ndarray:

@@ -270,6 +270,16 @@ static uint16_t round_to_format(double x, int p, int ebits)
 uint16_t oracle_f64_to_f16(double x) { return round_to_format(x, 11, 5); }
 uint16_t oracle_f64_to_bf16(double x) { return round_to_format(x, 8, 8); }
 
+/* out[i] = bits[i] decoded as ORACLE_F16 or ORACLE_BF16. */
+int oracle_decode_array(const uint16_t *bits, double *out, int64_t n, int type)
+{
+    if (n < 0 || (type != ORACLE_F16 && type != ORACLE_BF16))
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = type == ORACLE_BF16 ? oracle_bf16_to_f64(bits[i]) : oracle_f16_to_f64(bits[i]);
+    return 0;
+}
+
 /* out[i] = x[i] rounded to ORACLE_F16 or ORACLE_BF16 (bit patterns). */
 int oracle_round_f64(const double *x, uint16_t *out, int64_t n, int type)
 {

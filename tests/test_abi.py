@@ -161,9 +161,13 @@ def test_configurations_name_their_c_width(lib):
     assert all(o == (1 if n.endswith("_h") else 0) for n, o in zip(names, outs))
     assert 0 in outs and 1 in outs
     assert lib.wgemm_debug_config_out(len(names)) == -6
-    # every 16-bit configuration is an fp32 configuration with another epilogue
+    # every plain 16-bit configuration is an fp32 configuration with another
+    # epilogue; fused configurations say so in their name
+    fused = [lib.wgemm_debug_config_fused(i) for i in range(len(names))]
+    assert all(f == (1 if "_ab" in n else 0) for n, f in zip(names, fused))
+    assert 1 in fused and lib.wgemm_debug_config_fused(len(names)) == -6
     for n in names:
-        if n.endswith("_h"):
+        if n.endswith("_h") and "_ab" not in n:
             assert n[:-2] in names
 
 

@@ -83,8 +83,9 @@ def check_full(A, B, K, kind, what, **kw):
 
 
 def configs(suffix=""):
-    """fp32-output configurations whose name ends with `suffix`."""
-    return [n for n in wgemm.config_names() if n.endswith(suffix) and not n.endswith("_h")]
+    """Plain fp32-output configurations whose name ends with `suffix`."""
+    return [n for n in wgemm.config_names()
+            if n.endswith(suffix) and not n.endswith("_h") and "_ab" not in n]
 
 
 def k_split_configs():

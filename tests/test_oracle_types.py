@@ -150,3 +150,36 @@ def test_mixed_operand_types_rejected():
     B = inputs.matrix(4, 8, 1, 1, dtype="bf16")
     with pytest.raises(TypeError):
         oracle.gemm_f64(A, B)
+
+
+def test_fused_epilogue_equals_one_gemm_over_concatenated_k():
+    """alpha·A·Bᵀ + beta·A2·B2ᵀ + bias = [alpha·A | beta·A2 | 1]·[B | B2 | bias]ᵀ
+    (concatenation along K): the epilogue's definition pinned against the
+    GEMM definition itself, exact on small integers."""
+    M, N, K1, K2 = 23, 17, 40, 24
+    alpha, beta = 2.0, -3.0
+    A, B = inputs.gemm_operands(M, N, K1, seed=11, kind="int")
+    A2, B2 = inputs.gemm_operands(M, N, K2, seed=12, kind="int")
+    bias = (np.arange(N) % 7 - 3).astype(np.float64)
+    C = oracle.gemm_f64(A, B)
+    Cin = oracle.gemm_f64(A2, B2)
+    D = oracle.epilogue_f64(C, alpha, beta, Cin, bias)
+    Acat = np.concatenate([(alpha * A.astype(np.float64)).astype(np.float16),
+                           (beta * A2.astype(np.float64)).astype(np.float16),
+                           np.ones((M, 1), dtype=np.float16)], axis=1)
+    Bcat = np.concatenate([B, B2, bias.astype(np.float16)[:, None]], axis=1)
+    assert np.array_equal(D, oracle.gemm_f64(Acat, Bcat))
+    # beta = 0 never reads Cin; no bias adds nothing
+    assert np.array_equal(oracle.epilogue_f64(C, 1.0, 0.0, None, None), C)
+
+
+def test_decode_array_matches_scalar_decoders():
+    bits = np.arange(0, 1 << 16, 97, dtype=np.uint32).astype(np.uint16)
+    f = oracle.decode_array(bits, "f16")
+    b = oracle.decode_array(bits, "bf16")
+    sf = np.array([oracle.f16_to_f64(int(x)) for x in bits])
+    sb = np.array([oracle.bf16_to_f64(int(x)) for x in bits])
+    assert np.array_equal(np.isnan(f), np.isnan(sf)) and np.array_equal(f[~np.isnan(f)],
+                                                                        sf[~np.isnan(sf)])
+    assert np.array_equal(np.isnan(b), np.isnan(sb)) and np.array_equal(b[~np.isnan(b)],
+                                                                        sb[~np.isnan(sb)])

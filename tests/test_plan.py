@@ -211,9 +211,9 @@ def test_direct_epilogue_configs_reject_split_modes(lib):
         assert n == -6
 
 
-def test_16bit_output_configs_are_data_parallel_only(lib):
+def test_16bit_output_and_fused_configs_are_data_parallel_only(lib):
     for cfg, name in enumerate(wgemm.config_names()):
-        if not name.endswith("_h"):
+        if not name.endswith("_h") and "_ab" not in name:
             continue
         assert lib.wgemm_debug_plan(1024, 1024, 4096, cfg, DP, 1, 76, None, 0, None, None) > 0
         for mode, sp in ((SPLIT, 4), (STREAM, 1)):
