@@ -70,7 +70,7 @@ def peaks():
 
 KERNEL_SOURCES = ["wgemm_kernel.cuh", "wgemm_plan.h", "wgemm_configs.h", "inst_single.cu",
                   "inst_pair.cu", "inst_pair2.cu", "inst_multicast.cu", "inst_clc.cu",
-                  "sm103/ptx.cuh",
+                  "inst_out16_a.cu", "inst_out16_b.cu", "inst_fused.cu", "sm103/ptx.cuh",
                   "sm103/umma_desc.h"]
 
 
