@@ -74,13 +74,39 @@ KERNEL_SOURCES = ["wgemm_kernel.cuh", "wgemm_plan.h", "wgemm_configs.h", "inst_s
                   "sm103/umma_desc.h"]
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and whitespace (string literals kept)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':  # string literal: copy through its closing quote
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c.isspace():
+            i += 1
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_digest() -> str:
-    """Digest of the files that define the GEMM kernels (not the host code)."""
+    """Digest of the code (comments and whitespace removed) of the files that
+    define the GEMM kernels (not the host code)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp16_gemm_02_gb300", "csrc")
     for f in KERNEL_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

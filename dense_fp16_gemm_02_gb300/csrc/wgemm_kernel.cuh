@@ -45,7 +45,7 @@ namespace wg {
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kThreads = 256;
-constexpr int kBK = 64;  // K per stage: one 128-byte swizzle row of fp16
+constexpr int kBK = 64;  // K per stage: one 128-byte swizzle row of 16-bit operands
 
 enum EpilogueMode : int { kEpiDirect = 0, kEpiTma = 1 };
 
