@@ -76,3 +76,14 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_kernel_digest_ignores_comments_and_whitespace():
+    import bench
+    code = 'int f(int x) {\n  return x + 1;  // one more\n}\nconst char* s = "a // b";\n'
+    same = '/* header */ int f(int x)\n{ return x+1; }\n  const char* s = "a // b";'
+    other = 'int f(int x) { return x + 2; }\nconst char* s = "a // b";'
+    assert bench._code_only(code) == bench._code_only(same)
+    assert bench._code_only(code) != bench._code_only(other)
+    assert '"a // b"' in bench._code_only(code)  # string literals are kept whole
+    assert len(bench.kernel_source_digest()) == 16
