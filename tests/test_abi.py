@@ -177,3 +177,10 @@ def test_pdl_switch(lib):
     assert prev in (0, 1)
     assert lib.wgemm_set_pdl(0) == 1
     assert lib.wgemm_set_pdl(prev) == 0
+
+
+def test_tensor_peak_microbenchmark_compiles():
+    """The tensor-pipe microbenchmark (peak/tensor_peak.cu) builds for sm_103a."""
+    from dense_fp16_gemm_02_gb300 import peak
+    exe = peak.build_peak()
+    assert os.path.exists(exe) and os.access(exe, os.X_OK)
