@@ -283,7 +283,7 @@ def run_ours(args):
     # Inputs: generated on the host once, uploaded before timing.
     data = []
     for i, (M, N, K) in enumerate(shapes):
-        A, B = inputs.gemm_operands(M, N, K, seed=1000 + i, kind="uniform", dtype=ab)
+        A, B = inputs.gemm_operands(M, N, K, seed=1000 + i, kind=args.values, dtype=ab)
         dA, dB = as_tensor(A).to(dev), as_tensor(B).to(dev)
         C = torch.zeros((M, N), dtype=c_torch, device=dev)
         data.append((A, B, dA, dB, C))
@@ -447,7 +447,8 @@ def run_ours(args):
             "vs_baseline": None, "dtype": ab, "data": "synthetic",
             "config": {
                 "workload": args.workload + ": " + ", ".join(shape_name(s) for s in shapes),
-                "inputs": f"uniform[-1,1] rounded to {ab}, seeded SplitMix64, resident in HBM",
+                "inputs": (f"uniform[-1,1] rounded to {ab}" if args.values == "uniform" else
+                           "integers in {-2..2}") + ", seeded SplitMix64, resident in HBM",
                 "accumulate": "f32", "output": c,
                 "epilogue": ("D = A·Bᵀ + D + bias (fused; C read back in place)"
                              if args.epilogue == "fused" else "C = A·Bᵀ"),
@@ -498,6 +499,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--types", choices=sorted(TYPES), default="f16f32",
                     help="operand and C types (the measured product is f16f32)")
+    ap.add_argument("--values", choices=["uniform", "int"], default="uniform",
+                    help="operand values: uniform[-1,1] (the metric) or the integer copy")
     ap.add_argument("--epilogue", choices=["plain", "fused"], default="plain",
                     help="fused: D = A·Bᵀ + D + bias through the alpha/beta/bias epilogue")
     args = ap.parse_args(argv)
