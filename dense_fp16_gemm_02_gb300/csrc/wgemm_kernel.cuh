@@ -181,6 +181,16 @@ struct Cfg {
   static constexpr int kEpiBatch = EPI == kEpiTma ? (BN / 32 >= 2 ? 2 : 1)
                                                   : (BN / 32 >= 4 ? 4 : BN / 32);
   static constexpr uint32_t kEpiBytes = EPI == kEpiTma ? 4 * kEpiBatch * kEpiSlotBytes : 0;
+  // A worker's last unit (static schedule) is drained after every MMA has
+  // read its stages, so the stage ring is idle: its TMA epilogue stages
+  // through kTailGroups groups of kEpiBatch slots per warp carved from the
+  // ring, with that many bulk stores / reduce-adds in flight instead of one.
+  static constexpr uint32_t kTailGroupsFit =
+      EPI == kEpiTma ? (STAGES * kStageBytes / 4) / (kEpiBatch * kEpiSlotBytes) : 1;
+  static constexpr int kTailGroups =
+      (EPI == kEpiTma && SCHED == kSchedStatic) ? (kTailGroupsFit < 8 ? (int)kTailGroupsFit : 8)
+                                                : 1;
+  static constexpr uint32_t kTailWarpBytes = kTailGroups * kEpiBatch * kEpiSlotBytes;
   // Fused epilogue: each epilogue warp prefetches its 32×32 blocks of Cin
   // with TMA into a private ring of kCinSlots slots.
   static constexpr int kCinSlots = FUSE;
@@ -204,6 +214,8 @@ struct Cfg {
   static_assert(CG == 1 || CG == 2, "CG");
   static_assert(OUT == kOut32 || OUT == kOut16, "OUT");
   static_assert(!FUSE || EPI == kEpiDirect, "the fused epilogue stores from registers");
+  static_assert(kTailGroups >= 1 && 4 * kTailWarpBytes <= STAGES * kStageBytes,
+                "tail staging inside the stage ring");
   static_assert(!FUSE || SCHED == kSchedStatic, "the Cin ring prefetches the next unit");
   static_assert(FUSE >= 0 && FUSE <= 8, "Cin ring depth");
   static_assert(MC == 1 || MC == 2, "MC");
@@ -749,7 +761,10 @@ struct Kernel {
     return true;
   }
 
-  template <int NBB>
+  // WAITN: bulk groups (batches) that may still be reading staging slots
+  // when this batch's slots are written: 0 with the two per-warp slots,
+  // kTailGroups - 1 when staging rotates through the idle stage ring.
+  template <int NBB, int WAITN>
   __device__ static bool drain(const KParams& p, uint32_t base, uint8_t* smem, uint32_t tmem,
                                uint32_t tatom, int c0, int nb, int32_t col_warp, int32_t row0,
                                bool add, uint32_t stage_base, bool release, uint32_t ab,
@@ -845,12 +860,14 @@ struct Kernel {
       // reused once the previous batch's stores have read it), then one lane
       // writes them out with TMA stores or reduce-adds; TMA clips what lies
       // outside M × N.
+      const uint32_t soff = stage_base - base;
       if (!WG_CHECK(p.status,
-                    stage_base - base + nb * K::kEpiSlotBytes <= K::kOffBars &&
-                        stage_base - base >= K::kOffEpi,
-                    kCheckStaging, stage_base - base))
+                    (soff >= K::kOffEpi && soff + nb * K::kEpiSlotBytes <= K::kOffBars) ||
+                        (WAITN > 0 && soff + nb * K::kEpiSlotBytes <=
+                                          (uint32_t)K::STAGES * K::kStageBytes),
+                    kCheckStaging, soff))
         return true;
-      if (lane == 0) bulk_wait_group_read<0>();
+      if (lane == 0) bulk_wait_group_read<WAITN>();
       __syncwarp();
 #pragma unroll
       for (int b = 0; b < NBB; ++b) {
@@ -903,7 +920,8 @@ struct Kernel {
     }
 
     uint32_t ab = 0, aph = 0;
-    const uint32_t stage_base = base + K::kOffEpi + q * 2 * K::kEpiSlotBytes;
+    const uint32_t stage_base = base + K::kOffEpi + q * K::kEpiBatch * K::kEpiSlotBytes;
+    const uint32_t tail_base = base + K::kOffStages + q * K::kTailWarpBytes;
     FuseState fs{};
     for (int32_t i = 0; ok; ++i) {
       Unit u;
@@ -955,6 +973,13 @@ struct Kernel {
       constexpr int kChunks = K::BN / 32;
       constexpr int NB = K::kEpiBatch;
       const uint32_t tacc = tmem + ((q * 32u) << 16) + ab * K::kAccCols;
+      // The worker's last unit stages through the idle stage ring.
+      bool tail = false;
+      if constexpr (K::kTailGroups > 1) {
+        Unit u_next;
+        tail = !plan_unit(p.plan, worker, i + 1, u_next);
+      }
+      int32_t batch = 0;
 #pragma unroll 1
       for (int r = 0; r < K::REPS; ++r) {
         const int32_t col_warp = col_cta + r * 128 + (int32_t)q * 32;
@@ -964,9 +989,20 @@ struct Kernel {
           // The last batch of an atom may be short (kChunks not a multiple of
           // NB); one register array of NB chunks serves every batch.
           const int nb = kChunks - c0 < NB ? kChunks - c0 : NB;
-          if (!drain<NB>(p, base, smem, tmem, tacc + r * K::BN, c0, nb, col_warp, row0, add,
-                         stage_base, last_atom && c0 + nb == kChunks, ab, grp, r, fs,
-                         abort_flag)) {
+          const bool rel = last_atom && c0 + nb == kChunks;
+          bool dok;
+          if (tail) {
+            const uint32_t sb = tail_base + (uint32_t)(batch % K::kTailGroups) * NB *
+                                                K::kEpiSlotBytes;
+            dok = drain<NB, K::kTailGroups - 1>(p, base, smem, tmem, tacc + r * K::BN, c0, nb,
+                                                  col_warp, row0, add, sb, rel, ab, grp, r, fs,
+                                                  abort_flag);
+          } else {
+            dok = drain<NB, 0>(p, base, smem, tmem, tacc + r * K::BN, c0, nb, col_warp, row0,
+                               add, stage_base, rel, ab, grp, r, fs, abort_flag);
+          }
+          ++batch;
+          if (!dok) {
             ok = false;
             break;
           }
