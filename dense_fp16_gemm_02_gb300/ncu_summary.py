@@ -1,0 +1,164 @@
+"""Summaries of ncu captures for profiles/: the DRAM traffic of the sweep's
+GEMM launches (with the traffic table bench.py reads) and the roofline table
+of the eleven shapes.
+
+    python -m dense_fp16_gemm_02_gb300.ncu_summary dram DRAM_CSV
+    python -m dense_fp16_gemm_02_gb300.ncu_summary roofline ROOFLINE_CSV BENCH_JSON
+
+DRAM_CSV is the `--csv --log-file` output of the dram command in
+profiles/dram_sweep.md; ROOFLINE_CSV and BENCH_JSON are those of
+profiles/roofline_all_shapes.md. The files under profiles/ are rewritten
+(their prose is kept; the tables and the kernel-source digest are replaced).
+"""
+from __future__ import annotations
+
+import csv
+import io
+import json
+import os
+import re
+import sys
+from collections import OrderedDict
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def _bench():
+    sys.path.insert(0, ROOT)
+    import bench
+    return bench
+
+
+def read_ncu_csv(path: str) -> "OrderedDict[str, dict]":
+    """Per launch ID: {metric name: value (float), "kernel": name}."""
+    with open(path) as f:
+        lines = [l for l in f.read().splitlines() if l.startswith('"')]
+    by = OrderedDict()
+    for r in csv.DictReader(io.StringIO("\n".join(lines))):
+        d = by.setdefault(r["ID"], {"kernel": r["Kernel Name"]})
+        try:
+            d[r["Metric Name"]] = float(r["Metric Value"].replace(",", ""))
+        except ValueError:
+            d[r["Metric Name"]] = r["Metric Value"]
+    return by
+
+
+def _replace_table(text: str, header: str, rows: list[str]) -> str:
+    """Replace the markdown table that starts with `header` by header + rows."""
+    start = text.index(header)
+    end = start + len(header)
+    lines = text[end:].split("\n")
+    n = 0
+    while n < len(lines) and lines[n].startswith("|"):
+        n += 1
+    return text[:end] + "\n".join(rows) + "\n" + "\n".join(lines[n:])
+
+
+def _set_digest(text: str, digest: str) -> str:
+    return re.sub(r"digest\s*`[0-9a-f]{16}`", f"digest `{digest}`", text)
+
+
+def dram(csv_path: str) -> None:
+    b = _bench()
+    shapes = b.WORKLOADS["sweep"]
+    by = read_ncu_csv(csv_path)
+    if len(by) != len(shapes):
+        raise SystemExit(f"{len(by)} launches in {csv_path}, expected {len(shapes)}")
+    digest = b.kernel_source_digest()
+    rows, traffic = [], []
+    for (M, N, K), v in zip(shapes, by.values()):
+        cfg = _config_of_kernel(v["kernel"])
+        rd, wr = v["dram__bytes_read.sum"], v["dram__bytes_write.sum"]
+        t = v["gpu__time_duration.sum"] / 1000.0
+        rows.append(f"| {M}x{N}x{K} | {cfg} | {t:.1f} | {rd / 1e6:.1f} | {wr / 1e6:.1f} | "
+                    f"{2 * (M * K + N * K) / 1e6:.1f} | {4 * M * N / 1e6:.1f} |")
+        traffic.append({"kernel_src": digest, "config": cfg, "shape": f"{M}x{N}x{K}",
+                        "dram_bytes": int(rd + wr),
+                        "source": (f"profiles/dram_sweep.md (dram__bytes_read.sum {int(rd):,} B + "
+                                   f"dram__bytes_write.sum {int(wr):,} B, one launch)")})
+    with open(os.path.join(PROFILES, "traffic.json"), "w") as f:
+        json.dump(traffic, f, indent=1)
+    p = os.path.join(PROFILES, "dram_sweep.md")
+    text = open(p).read()
+    header = ("| shape | configuration | µs (ncu) | DRAM read MB | DRAM write MB | "
+              "compulsory A+B MB | C MB |\n|---|---|---|---|---|---|---|\n")
+    text = _set_digest(_replace_table(text, header, rows), digest)
+    open(p, "w").write(text)
+    print("\n".join(rows))
+
+
+def roofline(csv_path: str, bench_json: str) -> None:
+    b = _bench()
+    by = read_ncu_csv(csv_path)
+    with open(bench_json) as f:
+        line = [l for l in f.read().splitlines() if l.startswith("{")][-1]
+    d = json.loads(line)
+    if len(by) != len(d["shapes"]):
+        raise SystemExit(f"{len(by)} launches, {len(d['shapes'])} shapes")
+    rows = []
+    for s, v in zip(d["shapes"], by.values()):
+        M, N, K = (int(x) for x in s["shape"].split("x"))
+        t = v["gpu__time_duration.sum"] / 1000.0
+        active = 100.0 * v["sm__cycles_active.avg"] / v["gpc__cycles_elapsed.max"]
+        rows.append(
+            f"| {M}×{N}×{K} | {s['config']} | {s['mode']} | {s['us_median']:.3f} | {s['tflops']} | "
+            f"{s['tensor_frac']} | {t:.1f} | {2 * M * N * K / t / 1e6:.1f} | "
+            f"{v['sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed']:.1f} | "
+            f"{active:.1f} | {v['dram__bytes_read.sum'] / 1e6:.1f} | "
+            f"{v['dram__bytes_write.sum'] / 1e6:.1f} | {s['hbm_frac']} |")
+    p = os.path.join(PROFILES, "roofline_all_shapes.md")
+    text = open(p).read()
+    header = ("| M×N×K | configuration | mode | bench µs (median) | bench TFLOP/s | tensor frac "
+              "(bench) | ncu µs | ncu TFLOP/s | tensor pipe active % (ncu) | SM active % (ncu) | "
+              "DRAM read MB | DRAM write MB | HBM frac (bench, compulsory bytes) |\n"
+              "|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
+    text = _set_digest(_replace_table(text, header, rows), b.kernel_source_digest())
+    open(p, "w").write(text)
+    print("\n".join(rows))
+
+
+def _config_of_kernel(kernel: str) -> str:
+    """The configuration name of a launched kernel, from its Cfg<...> arguments."""
+    m = re.search(r"Cfg<([0-9, ]+)>", kernel)
+    if not m:
+        return kernel
+    args = tuple(int(x) for x in m.group(1).split(","))
+    sys.path.insert(0, ROOT)
+    from dense_fp16_gemm_02_gb300 import build, wgemm
+    build.build()
+    for name in wgemm.config_names():
+        if _entry_args(name) == args:
+            return name
+    return kernel
+
+
+def _entry_args(name: str):
+    """The Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE> arguments
+    of a configuration, rebuilt from its name."""
+    m = re.match(r"g(\d)(?:m(\d))?_(\d+)x(\d+)_s(\d+)_a(\d)_(tma|direct)(_clc)?(?:_ab(\d))?(_h)?$",
+                 name)
+    if not m:
+        return None
+    cg = int(m.group(1))
+    mc = int(m.group(2) or 1)
+    cols, rows = int(m.group(3)), int(m.group(4))
+    reps = cols // (128 * cg * mc)
+    return (cg, reps, rows, int(m.group(5)), int(m.group(6)), 1 if m.group(7) == "tma" else 0,
+            mc, 1 if m.group(8) else 0, 1 if m.group(10) else 0, int(m.group(9) or 0))
+
+
+def main(argv=None) -> int:
+    argv = sys.argv[1:] if argv is None else argv
+    if len(argv) >= 2 and argv[0] == "dram":
+        dram(argv[1])
+    elif len(argv) >= 3 and argv[0] == "roofline":
+        roofline(argv[1], argv[2])
+    else:
+        print(__doc__)
+        return 2
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
