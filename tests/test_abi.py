@@ -184,3 +184,22 @@ def test_tensor_peak_microbenchmark_compiles():
     from dense_fp16_gemm_02_gb300 import peak
     exe = peak.build_peak()
     assert os.path.exists(exe) and os.access(exe, os.X_OK)
+
+
+def test_ncu_summary_maps_every_configuration_to_its_template_arguments(tmp_path):
+    from dense_fp16_gemm_02_gb300 import ncu_summary
+    names = wgemm.config_names()
+    args = [ncu_summary._entry_args(n) for n in names]
+    assert all(a is not None and len(a) == 10 for a in args)
+    assert len(set(args)) == len(names)  # one configuration per template instantiation
+    kernel = "void wgemm_kernel<Cfg<%s>>(KParams)" % ", ".join(str(x) for x in args[0])
+    assert ncu_summary._config_of_kernel(kernel) == names[0]
+    csv_text = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+                '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
+                '"Metric Value"\n'
+                '"0","1","python","h","%s","1","7","(256, 1, 1)","(152, 1, 1)","0","10.3","",'
+                '"gpu__time_duration.sum","ns","13,312"\n' % kernel)
+    p = tmp_path / "x.csv"
+    p.write_text("==PROF== preamble\n" + csv_text)
+    by = ncu_summary.read_ncu_csv(str(p))
+    assert by["0"]["gpu__time_duration.sum"] == 13312.0 and by["0"]["kernel"] == kernel
