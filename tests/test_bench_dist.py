@@ -87,3 +87,17 @@ def test_kernel_digest_ignores_comments_and_whitespace():
     assert bench._code_only(code) != bench._code_only(other)
     assert '"a // b"' in bench._code_only(code)  # string literals are kept whole
     assert len(bench.kernel_source_digest()) == 16
+
+
+def test_peak_follows_the_power_cap():
+    """The roofline's tensor peak is the measured burst figure unless the
+    timed region ran under the power cap, then the sustained one."""
+    sys.path.insert(0, ROOT)
+    import json
+    import bench
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        d = json.load(f)
+    t, hbm, src = bench.peaks()
+    assert (t, hbm) == (d["bf16_tflops"], d["hbm_gbs"]) and "burst" in src
+    t, hbm, src = bench.peaks(power_capped=True)
+    assert (t, hbm) == (d["bf16_tflops_sustained"], d["hbm_gbs"]) and "sustained" in src
