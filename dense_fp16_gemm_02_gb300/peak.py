@@ -6,6 +6,14 @@ shared memory, with no global traffic in the timed loop. Prints one JSON line
 per MMA shape, then one with the SM clock seen during the run.
 
     python -m dense_fp16_gemm_02_gb300.peak [iterations]
+
+With `--interference` it builds and runs `peak/mma_interference.cu`
+instead: the pair M256 N224 MMA loop while four more warps of every CTA
+make one kind of traffic (global stores, the register-store epilogue's
+pattern, shared-memory stores or loads, TMEM loads, bulk copies into shared
+memory), one JSON line per kind with the MMA rate and the traffic's rate.
+
+    python -m dense_fp16_gemm_02_gb300.peak --interference [iterations]
 """
 from __future__ import annotations
 
@@ -18,24 +26,30 @@ from . import build as _build
 from .clocks import ClockSampler
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SRC = os.path.join(HERE, "peak", "tensor_peak.cu")
-EXE = os.path.join(_build.BUILD, "tensor_peak")
+PROGRAMS = ("tensor_peak", "mma_interference")
 
 
-def build_peak() -> str:
+def build_peak(name: str = "tensor_peak") -> str:
+    """Compile peak/<name>.cu for sm_103a (when stale); returns the executable."""
+    assert name in PROGRAMS
+    src = os.path.join(HERE, "peak", name + ".cu")
+    exe = os.path.join(_build.BUILD, name)
     os.makedirs(_build.BUILD, exist_ok=True)
-    deps = [SRC, os.path.join(HERE, "csrc", "sm103", "ptx.cuh"),
+    deps = [src, os.path.join(HERE, "csrc", "sm103", "ptx.cuh"),
             os.path.join(HERE, "csrc", "sm103", "umma_desc.h")]
-    if os.path.exists(EXE) and os.path.getmtime(EXE) >= max(os.path.getmtime(d) for d in deps):
-        return EXE
-    cmd = [_build.NVCC, *_build.ARCH, "-O3", "-std=c++17", "-o", EXE, SRC]
+    if os.path.exists(exe) and os.path.getmtime(exe) >= max(os.path.getmtime(d) for d in deps):
+        return exe
+    cmd = [_build.NVCC, *_build.ARCH, "-O3", "-std=c++17", "-o", exe, src]
     subprocess.run(cmd, check=True)
-    return EXE
+    return exe
 
 
 def main(argv=None) -> int:
     argv = sys.argv[1:] if argv is None else argv
-    exe = build_peak()
+    name = "tensor_peak"
+    if argv and argv[0] == "--interference":
+        name, argv = "mma_interference", argv[1:]
+    exe = build_peak(name)
     with ClockSampler(0) as clocks:
         clocks.mark_start()
         out = subprocess.run([exe, *argv], check=True, capture_output=True, text=True).stdout

@@ -179,10 +179,11 @@ def test_pdl_switch(lib):
     assert lib.wgemm_set_pdl(prev) == 0
 
 
-def test_tensor_peak_microbenchmark_compiles():
-    """The tensor-pipe microbenchmark (peak/tensor_peak.cu) builds for sm_103a."""
+@pytest.mark.parametrize("name", ["tensor_peak", "mma_interference"])
+def test_peak_microbenchmarks_compile(name):
+    """The tensor-pipe microbenchmarks (peak/*.cu) build for sm_103a."""
     from dense_fp16_gemm_02_gb300 import peak
-    exe = peak.build_peak()
+    exe = peak.build_peak(name)
     assert os.path.exists(exe) and os.access(exe, os.X_OK)
 
 
