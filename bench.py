@@ -83,7 +83,7 @@ def peaks(power_capped: bool = False):
 
 KERNEL_SOURCES = ["wgemm_kernel.cuh", "wgemm_plan.h", "wgemm_configs.h", "inst_single.cu",
                   "inst_pair.cu", "inst_pair2.cu", "inst_multicast.cu", "inst_clc.cu",
-                  "inst_out16_a.cu", "inst_out16_b.cu", "inst_fused.cu", "sm103/ptx.cuh",
+                  "inst_out16_a.cu", "inst_out16_b.cu", "inst_fused.cu", "inst_rowmc.cu", "sm103/ptx.cuh",
                   "sm103/umma_desc.h"]
 
 

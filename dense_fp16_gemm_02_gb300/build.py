@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libwgemm.so")
 SOURCES = ["wgemm_host.cu", "inst_single.cu", "inst_pair.cu", "inst_pair2.cu",
            "inst_multicast.cu", "inst_clc.cu", "inst_out16_a.cu", "inst_out16_b.cu",
-           "inst_fused.cu"]
+           "inst_fused.cu", "inst_rowmc.cu"]
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-DNDEBUG", "-Xcompiler", "-fPIC",

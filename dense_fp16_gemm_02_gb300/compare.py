@@ -1,0 +1,124 @@
+"""The library beside cuBLAS on the same shapes: a comparison, not a product path.
+
+For every shape of a bench workload, the product call (`wgemm_f16f32`,
+fp16 A and B, fp32 C) and cuBLAS through `torch.mm(A, Bᵀ, out_dtype=float32)`
+(fp16 in, fp32 accumulate and out; the same contraction) are timed call by
+call, interleaved as W, ref, ref, W. Every call follows the bench's L2
+flush (a 256 MiB write) and GPU-side gate, and is bracketed by CUDA events
+on the launching stream. Where this torch has no `out_dtype` for mm, the
+cuBLAS arm writes fp16 C (two bytes less per element) and says so.
+
+    python -m dense_fp16_gemm_02_gb300.compare [--workload all] [--rounds 20]
+
+Prints one JSON line per shape (medians, TFLOP/s of both, and the ratio)
+and one summary line. The same checks as the bench guard the comparison:
+both arms' results on the shape are compared on a sample of rows.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--workload", default="all")
+    ap.add_argument("--rounds", type=int, default=20)
+    args = ap.parse_args(argv)
+
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
+    from dense_fp16_gemm_02_gb300.clocks import ClockSampler
+
+    build.build()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    h = stream.cuda_stream
+    flush = torch.empty(bench.FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    try:
+        probe = torch.zeros((8, 8), dtype=torch.float16, device="cuda")
+        torch.mm(probe, probe.t(), out_dtype=torch.float32)
+        ref_out = "f32"
+    except (TypeError, RuntimeError):
+        ref_out = "f16"
+
+    rows = []
+    with ClockSampler(0) as clocks:
+        clocks.mark_start()
+        for idx, (M, N, K) in enumerate(bench.WORKLOADS[args.workload]):
+            A, B = inputs.gemm_operands(M, N, K, seed=1000 + idx, kind="uniform")
+            dA = torch.from_numpy(A).cuda()
+            dB = torch.from_numpy(B).cuda()
+            del A, B
+            C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            Bt = dB.t()
+
+            def ours():
+                rc = wgemm.wgemm_f16f32(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, K,
+                                        K, N, h)
+                if rc != 0:
+                    raise RuntimeError(wgemm.status_string(rc))
+
+            def ref():
+                if ref_out == "f32":
+                    return torch.mm(dA, Bt, out_dtype=torch.float32)
+                return torch.mm(dA, Bt)
+
+            def timed(fn):
+                flush.fill_(0.0)
+                torch.cuda._sleep(bench.GATE_CYCLES)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                out = fn()
+                e1.record(stream)
+                return (e0, e1), out
+
+            for _ in range(3):  # warm-up, both arms
+                timed(ours)
+                timed(ref)
+            ev = {"ours": [], "ref": []}
+            for _ in range(args.rounds):  # W, ref, ref, W
+                for arm, fn in (("ours", ours), ("ref", ref), ("ref", ref), ("ours", ours)):
+                    e, _ = timed(fn)
+                    ev[arm].append(e)
+            torch.cuda.synchronize()
+            if wgemm.wgemm_check(h) != 0:
+                raise RuntimeError(f"device status: {wgemm.wgemm_last_device_error()}")
+            # The two arms compute the same contraction: compare a sample of rows.
+            rsel = torch.linspace(0, M - 1, steps=min(M, 64)).long().cuda()
+            Cr = ref().float()
+            scale = (dA[rsel].float().abs() @ dB.float().abs().t())
+            err = float(((C[rsel] - Cr[rsel]).abs() / (scale + 1e-6)).max())
+            us = {a: statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev[a])
+                  for a in ev}
+            fl = 2.0 * M * N * K
+            row = {"shape": f"{M}x{N}x{K}", "ours_us": round(us["ours"], 3),
+                   "cublas_us": round(us["ref"], 3),
+                   "ours_tflops": round(fl / us["ours"] / 1e6, 1),
+                   "cublas_tflops": round(fl / us["ref"] / 1e6, 1),
+                   "speedup": round(us["ref"] / us["ours"], 3),
+                   "max_rel_diff_vs_abs_product": err}
+            rows.append(row)
+            print(json.dumps(row), flush=True)
+            del dA, dB, Bt, C, Cr
+            torch.cuda.empty_cache()
+        clocks.mark_stop()
+    ratios = [r["speedup"] for r in rows]
+    print(json.dumps({"summary": {
+        "workload": args.workload, "rounds": args.rounds, "cublas_output": ref_out,
+        "geomean_speedup": round(statistics.geometric_mean(ratios), 3),
+        "shapes_faster": sum(1 for x in ratios if x > 1.0), "shapes": len(ratios),
+        "torch": torch.__version__, "clocks": clocks.summary()}}), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -9,7 +9,8 @@ namespace wg {
 struct KernelEntry {
   const char* name;
   int cg, reps, bn, stages, acc, epi;
-  int mc;                    // MMA groups per cluster sharing the A tile
+  int mc;                    // MMA groups per cluster side by side along C's columns (sharing A)
+  int mr;                    // MMA groups per cluster stacked along C's rows (sharing B)
   int sched;                 // 0: static persistent grid, 1: cluster launch control
   int tile_rows, tile_cols;  // C rows / columns of one worker tile
   int out;                   // 0: fp32 C; 1: 16-bit C (fp16 or bf16), data parallel only
@@ -35,21 +36,30 @@ extern const KernelEntry kEntriesOut16B[];
 extern const int kNumEntriesOut16B;
 extern const KernelEntry kEntriesFused[];
 extern const int kNumEntriesFused;
+extern const KernelEntry kEntriesRowMc[];
+extern const int kNumEntriesRowMc;
 
 }  // namespace wg
 
 // Builds the entry of one configuration (only in .cu files that include the
-// kernel template). MC = MMA groups per cluster sharing the A tile; SCHED =
-// kSchedStatic or kSchedClc; OUT = kOut32 or kOut16; FUSE = 0 or 1.
-#define WG_ENTRY_ANY(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE)                \
-  wg::KernelEntry {                                                                             \
-    NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED,                                            \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE>::kTileRows,               \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE>::kTileCols, OUT, FUSE,    \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE>::kSmemBytes,              \
-        reinterpret_cast<const void*>(                                                          \
-            &wg::wgemm_kernel<wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE>>)   \
+// kernel template). MC = MMA groups per cluster side by side along C's
+// columns (sharing the A tile), MR = groups stacked along C's rows (sharing
+// the B tile); SCHED = kSchedStatic or kSchedClc; OUT = kOut32 or kOut16;
+// FUSE = 0 or the Cin ring depth.
+#define WG_ENTRY_GEN(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR)                \
+  wg::KernelEntry {                                                                                 \
+    NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, MR, SCHED,                                            \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR>::kTileRows,               \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR>::kTileCols, OUT, FUSE,    \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR>::kSmemBytes,              \
+        reinterpret_cast<const void*>(                                                              \
+            &wg::wgemm_kernel<wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR>>)   \
   }
+#define WG_ENTRY_ANY(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE) \
+  WG_ENTRY_GEN(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, 1)
+// MR groups stacked along C's rows sharing the B tile (fp32 C).
+#define WG_ENTRY_MR(NAME, CG, REPS, BN, STAGES, ACC, EPI, MR, SCHED) \
+  WG_ENTRY_GEN(NAME, CG, REPS, BN, STAGES, ACC, EPI, 1, SCHED, wg::kOut32, 0, MR)
 #define WG_ENTRY_OUT(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT) \
   WG_ENTRY_ANY(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, 0)
 #define WG_ENTRY_FULL(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED) \

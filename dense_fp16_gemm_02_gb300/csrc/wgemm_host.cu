@@ -91,6 +91,7 @@ struct Registry {
     for (int i = 0; i < kNumEntriesOut16A; ++i) entries.push_back(&kEntriesOut16A[i]);
     for (int i = 0; i < kNumEntriesOut16B; ++i) entries.push_back(&kEntriesOut16B[i]);
     for (int i = 0; i < kNumEntriesFused; ++i) entries.push_back(&kEntriesFused[i]);
+    for (int i = 0; i < kNumEntriesRowMc; ++i) entries.push_back(&kEntriesRowMc[i]);
   }
 };
 
@@ -194,12 +195,12 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t
 cudaLaunchConfig_t launch_config(const KernelEntry& e, int workers, cudaStream_t stream,
                                  cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(workers * e.cg * e.mc), 1, 1);
+  cfg.gridDim = dim3((unsigned)(workers * e.cg * e.mc * e.mr), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = e.smem_bytes;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)(e.cg * e.mc);
+  attr[0].val.clusterDim.x = (unsigned)(e.cg * e.mc * e.mr);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -218,7 +219,7 @@ int max_workers(DeviceState& st, int id) {
     return WGEMM_ERR_LAUNCH;
   }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_config(e, st.sm_count / (e.cg * e.mc), nullptr, attr);
+  cudaLaunchConfig_t cfg = launch_config(e, st.sm_count / (e.cg * e.mc * e.mr), nullptr, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, e.func, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
@@ -351,7 +352,8 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
       }
     };
     consider(kDataParallel, 1);
-    const bool ksplit = e.epi == kEpiTma && e.mc == 1 && e.sched == 0 && e.out == 0 && !e.fuse;
+    const bool ksplit =
+        e.epi == kEpiTma && e.mc == 1 && e.mr == 1 && e.sched == 0 && e.out == 0 && !e.fuse;
     const int64_t tiles = (int64_t)((M + e.tile_rows - 1) / e.tile_rows) *
                           ((N + e.tile_cols - 1) / e.tile_cols);
     const int kblocks = (K + kBK - 1) / kBK;
@@ -432,7 +434,7 @@ int make_plan(const KernelEntry& e, int M, int N, int K, int mode, int splits, i
   p->splits = 1;
   p->group = raster_group();
   if (mode != kDataParallel &&
-      (e.epi != kEpiTma || e.mc != 1 || e.sched != 0 || e.out != 0 || e.fuse != 0))
+      (e.epi != kEpiTma || e.mc != 1 || e.mr != 1 || e.sched != 0 || e.out != 0 || e.fuse != 0))
     return WGEMM_ERR_CONFIG;
   p->sched = e.sched;
   if (mode == kDataParallel && e.sched == 1) {
@@ -538,7 +540,7 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
   KParams params;
   std::memset(&params, 0, sizeof(params));
   if ((rc = make_plan(e, M, N, K, mode, splits, mw, &params.plan)) != WGEMM_OK) return rc;
-  const int brows_a = e.bn / e.cg / e.mc, rows_b = 128 * e.reps;
+  const int brows_a = e.bn / e.cg / e.mc, rows_b = 128 * e.reps / e.mr;
   if (!encode_2d(&params.tmA, tma_type(ab_type), A, (uint64_t)K, (uint64_t)M, (uint64_t)lda * 2,
                  kBK, (uint32_t)brows_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&params.tmB, tma_type(ab_type), B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb * 2,
@@ -565,7 +567,7 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
   params.trace_ctas = g_debug_trace_ctas;
   if (params.plan.mode != kDataParallel) {
     Workspace* ws;
-    const size_t words = (size_t)params.plan.num_tiles * e.cg * e.mc * params.plan.splits;
+    const size_t words = (size_t)params.plan.num_tiles * e.cg * e.mc * e.mr * params.plan.splits;
     if ((rc = workspace(dev, stream, words, &ws)) != WGEMM_OK) return rc;
     params.flags = ws->flags;
     params.flag_words = (int32_t)(ws->bytes / sizeof(uint32_t));
@@ -578,7 +580,7 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
                  params.plan.num_tiles);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_config(e, params.plan.workers, stream, attr);
-  if (e.cg * e.mc == 1) cfg.numAttrs = 0;  // no cluster: a plain launch
+  if (e.cg * e.mc * e.mr == 1) cfg.numAttrs = 0;  // no cluster: a plain launch
   if (g_pdl) {
     // May start (set-up only; loads wait) while the previous kernel on the
     // stream finishes, once that kernel allows its dependents to launch.
@@ -936,7 +938,7 @@ int run_noalloc(const uint16_t* A, const uint16_t* B, float* C, int M, int N, in
   if ((rc = make_plan(e, M, N, K, kSplitK, splits, mw, &params.plan)) != WGEMM_OK) return rc;
   const size_t words = (size_t)params.plan.num_tiles * e.cg * params.plan.splits;
   if (words > kNoAllocFlagWords) return WGEMM_ERR_NOALLOC_TOO_LARGE;
-  const int brows_a = e.bn / e.cg / e.mc, rows_b = 128 * e.reps;
+  const int brows_a = e.bn / e.cg / e.mc, rows_b = 128 * e.reps / e.mr;
   if (!encode_2d(&params.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
                  (uint64_t)lda * 2, kBK, (uint32_t)brows_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&params.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)K, (uint64_t)N,

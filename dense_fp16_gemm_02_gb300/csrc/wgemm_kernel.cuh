@@ -143,7 +143,7 @@ enum SchedMode : int { kSchedStatic = 0, kSchedClc = 1 };
 enum OutWidth : int { kOut32 = 0, kOut16 = 1 };
 
 template <int CG_, int REPS_, int BN_, int STAGES_, int ACC_, int EPI_, int MC_ = 1,
-          int SCHED_ = kSchedStatic, int OUT_ = kOut32, int FUSE_ = 0>
+          int SCHED_ = kSchedStatic, int OUT_ = kOut32, int FUSE_ = 0, int MR_ = 1>
 struct Cfg {
   static constexpr int OUT = OUT_;        // OutWidth: fp32 C, or 16-bit C (data parallel only)
   // FUSE > 0: alpha/beta/bias epilogue (data parallel only) whose Cin ring
@@ -151,7 +151,8 @@ struct Cfg {
   static constexpr int FUSE = FUSE_;
   static constexpr int SCHED = SCHED_;    // SchedMode
   static constexpr int CG = CG_;          // CTAs per MMA: 1, or 2 (pair)
-  static constexpr int MC = MC_;          // MMA groups per cluster sharing the A tile
+  static constexpr int MC = MC_;          // MMA groups per cluster side by side along C's columns
+  static constexpr int MR = MR_;          // MMA groups per cluster stacked along C's rows
   static constexpr int REPS = REPS_;      // stacked MMA atoms per CTA (C columns 128·REPS)
   static constexpr int BN = BN_;          // MMA N = C rows of a tile
   static constexpr int STAGES = STAGES_;  // ring depth
@@ -161,14 +162,18 @@ struct Cfg {
   static constexpr int kCtaCols = 128 * REPS;       // C columns per CTA
   static constexpr int kGroupCols = kCtaCols * CG;  // C columns per MMA group (CTA or pair)
   static constexpr int kTileCols = kGroupCols * MC; // C columns per worker (cluster) tile
-  static constexpr int kTileRows = BN;              // C rows per worker tile
-  static constexpr int kClusterSize = CG * MC;
+  static constexpr int kTileRows = BN * MR;         // C rows per worker tile
+  static constexpr int kGroups = MC * MR;           // MMA groups per cluster
+  static constexpr int kClusterSize = CG * kGroups;
   static constexpr int kArows = 128 * REPS;         // MMA-A rows (of B) per CTA stage
   static constexpr int kBrows = BN / CG;            // MMA-B rows (of A) per CTA stage
   // With MC groups side by side along C's columns, the groups of a cluster
   // need the same rows of A: each CTA loads 1/MC of its A slice and multicasts
   // it to the CTA in the same position of every group.
   static constexpr int kBrowsPart = kBrows / MC;
+  // With MR groups stacked along C's rows, the groups need the same rows of
+  // B: each CTA loads 1/MR of its B slice and multicasts it the same way.
+  static constexpr int kArowsPart = kArows / MR;
   static constexpr uint32_t kAbytes = kArows * 128;
   static constexpr uint32_t kBbytes = kBrows * 128;
   static constexpr uint32_t kStageBytes = kAbytes + kBbytes;
@@ -205,7 +210,7 @@ struct Cfg {
   // full barrier (bytes of the response) and an empty barrier (releases of
   // every consumer in the cluster, gathered in the cluster leader).
   static constexpr int kClcDepth = SCHED == kSchedClc ? 4 : 0;
-  static constexpr uint32_t kClcConsumers = kClusterSize * 6 + MC;
+  static constexpr uint32_t kClcConsumers = kClusterSize * 6 + kGroups;
   static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 2 + 2 * kClcDepth + 4 * kCinSlots;
   static constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
   static constexpr uint32_t kOffResp = (kOffMisc + 16 + 15) / 16 * 16;
@@ -219,7 +224,9 @@ struct Cfg {
   static_assert(!FUSE || SCHED == kSchedStatic, "the Cin ring prefetches the next unit");
   static_assert(FUSE >= 0 && FUSE <= 8, "Cin ring depth");
   static_assert(MC == 1 || MC == 2, "MC");
-  static_assert(kBrowsPart % 8 == 0, "multicast part in 8-row groups");
+  static_assert(MR == 1 || MR == 2, "MR");
+  static_assert(MC == 1 || MR == 1, "one multicast direction per configuration");
+  static_assert(kBrowsPart % 8 == 0 && kArowsPart % 8 == 0, "multicast part in 8-row groups");
   static_assert(REPS == 1 || REPS == 2, "REPS");
   static_assert(BN % 32 == 0 && BN % (16 * CG) == 0 && BN >= 32 && BN <= 256, "MMA N");
   static_assert(kBrows % 8 == 0, "operand rows in 8-row groups");
@@ -458,9 +465,12 @@ struct Kernel {
   __device__ static uint16_t same_rank_mask(uint32_t rank) {
     uint16_t m = 0;
 #pragma unroll
-    for (int q = 0; q < K::MC; ++q) m |= (uint16_t)(1u << (q * K::CG + rank));
+    for (int q = 0; q < K::kGroups; ++q) m |= (uint16_t)(1u << (q * K::CG + rank));
     return m;
   }
+  // The group's position along C's columns and along C's rows.
+  __device__ static int32_t col_group(uint32_t grp) { return K::MR == 1 ? (int32_t)grp : 0; }
+  __device__ static int32_t row_group(uint32_t grp) { return K::MR == 1 ? 0 : (int32_t)grp; }
   __device__ static uint16_t group_mask(uint32_t grp) {
     return (uint16_t)(((1u << K::CG) - 1u) << (grp * K::CG));
   }
@@ -470,6 +480,24 @@ struct Kernel {
                                     int32_t b_row0, int32_t a_row0, uint32_t rank, uint32_t grp) {
     const uint32_t full = bar_full(base, s);
     const uint32_t a_dst = stage_b(base, s) + grp * K::kBrowsPart * 128;
+    if constexpr (K::MR > 1) {
+      // Part grp of the B slice goes to this rank of every group; the A rows
+      // are this CTA's own. b_row0 is the slice's first row.
+      const uint32_t b_dst = stage_a(base, s) + grp * K::kArowsPart * 128;
+      const int32_t b_part = b_row0 + (int32_t)grp * K::kArowsPart;
+      if constexpr (K::CG == 1) {
+        mbar_arrive_expect_tx(full, K::kStageBytes);
+        tma_load_2d_multicast(b_dst, &p.tmB, full, kb * kBK, b_part, same_rank_mask(rank));
+        tma_load_2d(stage_b(base, s), &p.tmA, full, kb * kBK, a_row0);
+      } else {
+        if (rank == 0) mbar_arrive_expect_tx(full, 2 * K::kStageBytes);
+        const uint32_t full_leader = mapa_shared(full, group_leader(grp));
+        tma_load_2d_pair_multicast(b_dst, &p.tmB, full_leader, kb * kBK, b_part,
+                                   same_rank_mask(rank));
+        tma_load_2d_pair(stage_b(base, s), &p.tmA, full_leader, kb * kBK, a_row0);
+      }
+      return;
+    }
     if constexpr (K::CG == 1) {
       mbar_arrive_expect_tx(full, K::kStageBytes);
       tma_load_2d(stage_a(base, s), &p.tmB, full, kb * kBK, b_row0);
@@ -530,10 +558,11 @@ struct Kernel {
       Unit u;
       if (!next_unit(p, base, worker, i, true, false, u, ok, abort_flag, kSiteClcFull)) break;
       if (!unit_ok(p, u)) { ok = false; break; }
-      const int32_t b_row0 = u.tn * K::kTileCols + (int32_t)grp * K::kGroupCols +
+      const int32_t b_row0 = u.tn * K::kTileCols + col_group(grp) * K::kGroupCols +
                              (int32_t)rank * K::kCtaCols;                     // rows of B
-      const int32_t a_row0 = u.tm * K::kTileRows + (int32_t)rank * K::kBrows +
-                             (int32_t)grp * K::kBrowsPart;                    // rows of A
+      const int32_t a_row0 = u.tm * K::kTileRows + row_group(grp) * K::BN +
+                             (int32_t)rank * K::kBrows +
+                             (K::MC > 1 ? (int32_t)grp * K::kBrowsPart : 0);  // rows of A
       for (int32_t kb = u.kb_begin + (i == 0 ? (int32_t)prefilled : 0); kb < u.kb_end; ++kb) {
         if (!wait_bar(bar_empty(base, s), ph ^ 1, abort_flag, p.status, kSiteProducerEmpty)) {
           ok = false;
@@ -605,7 +634,7 @@ struct Kernel {
                             (kb > u.kb_begin || j > 0) ? 1u : 0u);
           }
         }
-        if constexpr (K::CG == 1 && K::MC == 1) umma_commit(bar_empty(base, s));
+        if constexpr (K::kClusterSize == 1) umma_commit(bar_empty(base, s));
         else if constexpr (K::CG == 1) umma_commit_multicast(bar_empty(base, s), kAllCtas);
         else umma_commit_pair_multicast(bar_empty(base, s), kAllCtas);
         if (++s == (uint32_t)K::STAGES) { s = 0; ph ^= 1; }
@@ -662,8 +691,8 @@ struct Kernel {
     if (!plan_unit(p.plan, worker, i, u)) return g;
     const int32_t M = p.plan.M, N = p.plan.N;
     constexpr int kChunks = K::BN / 32;
-    g.col_cta = u.tn * K::kTileCols + (int32_t)grp * K::kGroupCols + (int32_t)rank * K::kCtaCols;
-    g.row0 = u.tm * K::kTileRows;
+    g.col_cta = u.tn * K::kTileCols + col_group(grp) * K::kGroupCols + (int32_t)rank * K::kCtaCols;
+    g.row0 = u.tm * K::kTileRows + row_group(grp) * K::BN;
     const int32_t rows = M - g.row0;
     g.lc = rows <= 0 ? 0 : ((rows + 31) / 32 < kChunks ? (rows + 31) / 32 : kChunks);
     int32_t atoms = 0;
@@ -941,8 +970,8 @@ struct Kernel {
       tcgen05_fence_after();
       if (!unit_ok(p, u)) { ok = false; break; }
       const int32_t col_cta =
-          u.tn * K::kTileCols + (int32_t)grp * K::kGroupCols + (int32_t)rank * K::kCtaCols;
-      const int32_t row0 = u.tm * K::kTileRows;
+          u.tn * K::kTileCols + col_group(grp) * K::kGroupCols + (int32_t)rank * K::kCtaCols;
+      const int32_t row0 = u.tm * K::kTileRows + row_group(grp) * K::BN;
       const bool add = u.kind == kUnitAddAfterOwner || u.kind == kUnitAddAfterZero;
       if constexpr (K::EPI == kEpiTma) {
         if (add && lane == 0) {
@@ -1058,12 +1087,13 @@ struct Kernel {
       Unit u;
       if (!plan_unit(p.plan, worker, i, u)) break;
       int32_t r0, r1;
-      plan_zero_rows(K::kTileRows, p.plan.splits, u.split, r0, r1);
-      const int32_t row_begin = u.tm * K::kTileRows + r0;
-      int32_t row_end = u.tm * K::kTileRows + r1;
+      plan_zero_rows(K::BN, p.plan.splits, u.split, r0, r1);
+      const int32_t group_row0 = u.tm * K::kTileRows + row_group(grp) * K::BN;
+      const int32_t row_begin = group_row0 + r0;
+      int32_t row_end = group_row0 + r1;
       if (row_end > M) row_end = M;
       const int32_t col_begin =
-          u.tn * K::kTileCols + (int32_t)grp * K::kGroupCols + (int32_t)rank * K::kCtaCols;
+          u.tn * K::kTileCols + col_group(grp) * K::kGroupCols + (int32_t)rank * K::kCtaCols;
       int32_t col_end = col_begin + K::kCtaCols;
       if (col_end > N) col_end = N;
       if (row_begin >= row_end || col_begin >= col_end) continue;
@@ -1119,7 +1149,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     if (K::EPI == kEpiTma) prefetch_tensormap(&p.tmC);
     for (int s = 0; s < K::STAGES; ++s) {
       mbar_init(Kernel<K>::bar_full(base, s), 1);
-      mbar_init(Kernel<K>::bar_empty(base, s), K::MC);  // one release per MMA group
+      mbar_init(Kernel<K>::bar_empty(base, s), K::kGroups);  // one release per MMA group
     }
     for (int a = 0; a < K::ACC; ++a) {
       mbar_init(Kernel<K>::bar_accf(base, a), 1);

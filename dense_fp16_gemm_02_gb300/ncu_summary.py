@@ -124,6 +124,8 @@ def _config_of_kernel(kernel: str) -> str:
     if not m:
         return kernel
     args = tuple(int(x) for x in m.group(1).split(","))
+    if len(args) == 10:  # captures from before the MR argument existed
+        args += (1,)
     sys.path.insert(0, ROOT)
     from dense_fp16_gemm_02_gb300 import build, wgemm
     build.build()
@@ -134,18 +136,21 @@ def _config_of_kernel(kernel: str) -> str:
 
 
 def _entry_args(name: str):
-    """The Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE> arguments
-    of a configuration, rebuilt from its name."""
-    m = re.match(r"g(\d)(?:m(\d))?_(\d+)x(\d+)_s(\d+)_a(\d)_(tma|direct)(_clc)?(?:_ab(\d))?(_h)?$",
-                 name)
+    """The Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR>
+    arguments of a configuration, rebuilt from its name (g<CG>[m<MC>|r<MR>]_
+    <tile columns>x<tile rows>_s<STAGES>_a<ACC>_<epilogue>[_clc][_ab<FUSE>][_h])."""
+    m = re.match(r"g(\d)(?:m(\d))?(?:r(\d))?_(\d+)x(\d+)_s(\d+)_a(\d)_(tma|direct)(_clc)?"
+                 r"(?:_ab(\d))?(_h)?$", name)
     if not m:
         return None
     cg = int(m.group(1))
     mc = int(m.group(2) or 1)
-    cols, rows = int(m.group(3)), int(m.group(4))
+    mr = int(m.group(3) or 1)
+    cols, rows = int(m.group(4)), int(m.group(5))
     reps = cols // (128 * cg * mc)
-    return (cg, reps, rows, int(m.group(5)), int(m.group(6)), 1 if m.group(7) == "tma" else 0,
-            mc, 1 if m.group(8) else 0, 1 if m.group(10) else 0, int(m.group(9) or 0))
+    return (cg, reps, rows // mr, int(m.group(6)), int(m.group(7)),
+            1 if m.group(8) == "tma" else 0, mc, 1 if m.group(9) else 0,
+            1 if m.group(11) else 0, int(m.group(10) or 0), mr)
 
 
 def main(argv=None) -> int:

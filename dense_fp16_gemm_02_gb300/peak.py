@@ -14,6 +14,13 @@ pattern, shared-memory stores or loads, TMEM loads, bulk copies into shared
 memory), one JSON line per kind with the MMA rate and the traffic's rate.
 
     python -m dense_fp16_gemm_02_gb300.peak --interference [iterations]
+
+With `--copies` it measures the host-device copy engines instead, the bound
+of the bench's end-to-end figure: pinned host memory to the device, back,
+and both directions at once on two streams, for 32, 128 and 256 MiB (CUDA
+events, median of ten after two warm-ups), one JSON line per size.
+
+    python -m dense_fp16_gemm_02_gb300.peak --copies
 """
 from __future__ import annotations
 
@@ -44,8 +51,63 @@ def build_peak(name: str = "tensor_peak") -> str:
     return exe
 
 
+def copy_rates(sizes_mib=(32, 128, 256), reps=10):
+    """Host-device copy bandwidths (GB/s) with pinned host buffers."""
+    import torch
+    dev = torch.device("cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    out = []
+    for mib in sizes_mib:
+        n = mib << 20
+        h_in = torch.empty(n, dtype=torch.uint8).pin_memory()
+        h_out = torch.empty(n, dtype=torch.uint8).pin_memory()
+        d_in = torch.empty(n, dtype=torch.uint8, device=dev)
+        d_out = torch.empty(n, dtype=torch.uint8, device=dev)
+
+        def timed(fn):
+            ts = []
+            for _ in range(reps + 2):
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            ts = sorted(ts[2:])
+            return ts[len(ts) // 2] * 1e-3  # s
+
+        def both():
+            cur = torch.cuda.current_stream()
+            start = torch.cuda.Event()
+            start.record(cur)
+            s1.wait_event(start)
+            s2.wait_event(start)
+            with torch.cuda.stream(s1):
+                d_in.copy_(h_in, non_blocking=True)
+            with torch.cuda.stream(s2):
+                h_out.copy_(d_out, non_blocking=True)
+            for s in (s1, s2):
+                e = torch.cuda.Event()
+                e.record(s)
+                cur.wait_event(e)
+
+        out.append({
+            "mib": mib,
+            "h2d_gbs": round(n / timed(lambda: d_in.copy_(h_in, non_blocking=True)) / 1e9, 1),
+            "d2h_gbs": round(n / timed(lambda: h_out.copy_(d_out, non_blocking=True)) / 1e9, 1),
+            "both_directions_gbs": round(2 * n / timed(both) / 1e9, 1),
+        })
+    return out
+
+
 def main(argv=None) -> int:
     argv = sys.argv[1:] if argv is None else argv
+    if argv and argv[0] == "--copies":
+        for row in copy_rates():
+            print(json.dumps(row))
+        return 0
     name = "tensor_peak"
     if argv and argv[0] == "--interference":
         name, argv = "mma_interference", argv[1:]

@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import sys
 
@@ -50,7 +51,7 @@ def candidates(M, N, K, names, workers_pair, workers_single):
         tiles = -(-M // rows) * -(-N // cols)
         workers = workers_pair if cg == 2 else workers_single
         out.append((cid, 0, 1))
-        if not name.endswith("_tma") or kb < 8 or "m2_" in name:
+        if not name.endswith("_tma") or kb < 8 or re.match(r"g\d[mr]2_", name):
             continue
         if tiles < 2 * workers:
             out.append((cid, 2, 1))
@@ -215,12 +216,13 @@ def _time_calls(wgemm, torch, bufs, M, N, K, fn, flush, reps=7, warm=2):
 RATE_POINTS = [(1, 1024), (1, 4096), (2, 1024), (2, 4096), (3, 2048), (4, 3072)]
 
 
-def rates(out_path, points=RATE_POINTS):
+def rates(out_path, points=RATE_POINTS, only=None):
     """Per data-parallel configuration: time whole waves of tiles (as many
     tiles per wave as co-resident workers) at several K and wave counts and
     fit t = t0 + waves · (a + b · kblocks) by least squares; once with operand
     rows on 32-byte sectors (pitch a multiple of 16 elements) and once with
-    rows 16 bytes off them (pitch ≡ 8 mod 16)."""
+    rows 16 bytes off them (pitch ≡ 8 mod 16). `only`: a regular expression
+    the configuration names must match (default: all)."""
     import numpy as np
     import torch
 
@@ -237,6 +239,8 @@ def rates(out_path, points=RATE_POINTS):
     pitches = {"": Kmax + 16, "u": Kmax + 8}  # the buffers hold Kmax + 16 per row
     out = []
     for cid, name in enumerate(names):
+        if only and not re.search(only, name):
+            continue
         W = lib.wgemm_debug_max_workers(cid)
         cols, rows = (int(v) for v in name.split("_")[1].split("x"))
         tn = max(d for d in range(1, 9) if W % d == 0)
@@ -281,16 +285,24 @@ def rates(out_path, points=RATE_POINTS):
                   indent=1)
 
 
-def emit_rates(json_path, inc_path=RATES_INC):
-    with open(json_path) as f:
-        d = json.load(f)
+def emit_rates(json_paths, inc_path=RATES_INC):
+    """Writes the rates table from one or more `--rates` outputs; a
+    configuration measured in a later file replaces its earlier row."""
+    if isinstance(json_paths, str):
+        json_paths = [json_paths]
+    merged, d = {}, {}
+    for path in json_paths:
+        with open(path) as f:
+            d = json.load(f)
+        for r in d["rates"]:
+            merged[r["config"]] = r
     lines = [
         "// Measured per-configuration rates (generated by dense_fp16_gemm_02_gb300/tune.py",
         f"// --rates on {d.get('gpu', 'a GB300')}; do not edit by hand). {{configuration,",
         "// t0 µs, a µs per wave, b µs per wave per k-block: rows on 32-byte sectors; the",
         "// same three with rows 16 bytes off}.",
     ]
-    for r in d["rates"]:
+    for r in merged.values():
         lines.append(f'{{"{r["config"]}", {r["t0_us"]:.3f}, {r["a_us"]:.3f}, {r["b_us"]:.5f}, '
                      f'{r["t0u_us"]:.3f}, {r["au_us"]:.3f}, {r["bu_us"]:.5f}}},')
     with open(inc_path, "w") as f:
@@ -415,7 +427,9 @@ def main(argv=None):
     ap.add_argument("--shapes", default="all")
     ap.add_argument("--emit", metavar="JSON", help="write csrc/wgemm_tuned.inc from a sweep")
     ap.add_argument("--rates", metavar="JSON", help="measure per-configuration rates")
-    ap.add_argument("--emit-rates", metavar="JSON", help="write csrc/wgemm_rates.inc")
+    ap.add_argument("--emit-rates", metavar="JSON", nargs="+",
+                    help="write csrc/wgemm_rates.inc (later files override earlier rows)")
+    ap.add_argument("--only", metavar="REGEX", help="--rates: configurations matching REGEX")
     ap.add_argument("--validate", metavar="JSON", help="check the rule on off-table shapes")
     ap.add_argument("--pdl-report", metavar="JSON",
                     help="back-to-back calls with programmatic dependent launch off and on")
@@ -427,7 +441,7 @@ def main(argv=None):
         print(emit_rates(args.emit_rates))
         return 0
     if args.rates:
-        rates(args.rates)
+        rates(args.rates, only=args.only)
         return 0
     if args.validate:
         validate(args.validate)

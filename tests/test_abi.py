@@ -2,6 +2,7 @@
 encoders match the PTX ISA field layouts and the pages' worked example.
 No GPU is used: only host functions and argument checks are called."""
 import os
+import re
 
 import pytest
 
@@ -119,7 +120,7 @@ def test_rule_predictions_from_measured_rates(lib):
     n = lib.wgemm_num_configs()
     for cid in range(n):
         name = lib.wgemm_config_name(cid).decode()
-        w = 36 if "m2_" in name else (152 if name.startswith("g1_") else 76)
+        w = 36 if re.match(r"g2[mr]2_", name) else (152 if name.startswith("g1_") else 76)
         p = lambda M, N, K, ld=None, mode=0, s=1: lib.wgemm_debug_predict_us(
             M, N, K, ld or K, ld or K, cid, mode, s, w)
         assert p(4096, 4096, 2048) > 0, name
@@ -191,10 +192,17 @@ def test_ncu_summary_maps_every_configuration_to_its_template_arguments(tmp_path
     from dense_fp16_gemm_02_gb300 import ncu_summary
     names = wgemm.config_names()
     args = [ncu_summary._entry_args(n) for n in names]
-    assert all(a is not None and len(a) == 10 for a in args)
+    assert all(a is not None and len(a) == 11 for a in args)
     assert len(set(args)) == len(names)  # one configuration per template instantiation
     kernel = "void wgemm_kernel<Cfg<%s>>(KParams)" % ", ".join(str(x) for x in args[0])
     assert ncu_summary._config_of_kernel(kernel) == names[0]
+    # A row-multicast configuration, and a name captured before the eleventh
+    # template argument existed.
+    rm = [n for n in names if "r2_" in n][0]
+    k_rm = "void wgemm_kernel<Cfg<%s>>(KParams)" % ", ".join(str(x) for x in args[names.index(rm)])
+    assert ncu_summary._config_of_kernel(k_rm) == rm
+    old = "void wgemm_kernel<Cfg<%s>>(KParams)" % ", ".join(str(x) for x in args[0][:10])
+    assert ncu_summary._config_of_kernel(old) == names[0]
     csv_text = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
                 '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
                 '"Metric Value"\n'

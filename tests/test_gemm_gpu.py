@@ -13,6 +13,8 @@ span several tiles with ragged edges; the full-size cases of the workloads run
 the default per-shape choice (the launch the bench times) and are checked on
 sampled rows and columns the oracle computes one by one.
 """
+import re
+
 import numpy as np
 import pytest
 import torch
@@ -88,16 +90,21 @@ def configs(suffix=""):
             if n.endswith(suffix) and not n.endswith("_h") and "_ab" not in n]
 
 
+def is_multicast(name: str) -> bool:
+    """A cluster of MMA groups sharing an operand tile (g?m2_ or g?r2_)."""
+    return re.match(r"g\d[mr]2_", name) is not None
+
+
 def k_split_configs():
-    """Configurations that run split-K and stream-K (TMA epilogue, no A multicast)."""
-    return [n for n in configs("_tma") if "m2_" not in n]
+    """Configurations that run split-K and stream-K (TMA epilogue, no multicast)."""
+    return [n for n in configs("_tma") if not is_multicast(n)]
 
 
 # ---------------------------------------------------------------- every configuration
 
 
 @pytest.mark.parametrize("kind", ["int", "uniform"])
-@pytest.mark.parametrize("cfg", range(32))
+@pytest.mark.parametrize("cfg", range(48))
 def test_every_config_ragged(cfg, kind):
     names = configs()
     if cfg >= len(names):
@@ -109,7 +116,7 @@ def test_every_config_ragged(cfg, kind):
     check_full(A, B, K, kind, f"{names[cfg]} {kind}", config=names[cfg], mode=DP)
 
 
-@pytest.mark.parametrize("cfg", range(32))
+@pytest.mark.parametrize("cfg", range(48))
 def test_every_config_multi_round(cfg):
     # More tiles than co-resident workers for every configuration (≥ 2 tiles
     # per worker even for the 512×256 pair tile: 11 × 14 = 154 tiles over at

@@ -8,6 +8,7 @@ finish without a worker waiting forever ("SASS-Level Kernel Generation for
 Blackwell", paragraph "Stream-K and split-K, added in the L2").
 """
 import ctypes
+import re
 from collections import defaultdict
 
 import numpy as np
@@ -63,7 +64,8 @@ def test_data_parallel_covers_each_tile_once(lib, M, N, K, workers):
 
 def tma_configs(lib):
     """Configurations that run split-K and stream-K (TMA epilogue, no A multicast)."""
-    return [i for i, n in enumerate(wgemm.config_names()) if n.endswith("_tma") and "m2_" not in n]
+    return [i for i, n in enumerate(wgemm.config_names())
+            if n.endswith("_tma") and not re.match(r"g\d[mr]2_", n)]
 
 
 def direct_configs(lib):
@@ -71,7 +73,7 @@ def direct_configs(lib):
 
 
 def multicast_configs(lib):
-    return [i for i, n in enumerate(wgemm.config_names()) if "m2_" in n]
+    return [i for i, n in enumerate(wgemm.config_names()) if re.match(r"g\d[mr]2_", n)]
 
 
 def coverage(units, tm, tn, kb):
