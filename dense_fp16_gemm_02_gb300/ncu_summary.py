@@ -4,10 +4,12 @@ of the eleven shapes.
 
     python -m dense_fp16_gemm_02_gb300.ncu_summary dram DRAM_CSV
     python -m dense_fp16_gemm_02_gb300.ncu_summary roofline ROOFLINE_CSV BENCH_JSON
+    python -m dense_fp16_gemm_02_gb300.ncu_summary launches LAUNCHES_CSV
 
 DRAM_CSV is the `--csv --log-file` output of the dram command in
 profiles/dram_sweep.md; ROOFLINE_CSV and BENCH_JSON are those of
-profiles/roofline_all_shapes.md. The files under profiles/ are rewritten
+profiles/roofline_all_shapes.md; LAUNCHES_CSV that of
+profiles/launches_sweep.md (every launch with gpu__time_duration.sum). The files under profiles/ are rewritten
 (their prose is kept; the tables and the kernel-source digest are replaced).
 """
 from __future__ import annotations
@@ -118,6 +120,32 @@ def roofline(csv_path: str, bench_json: str) -> None:
     print("\n".join(rows))
 
 
+def launches(csv_path: str) -> None:
+    """Per kernel of a launch list: launches, total device time and shares."""
+    by = read_ncu_csv(csv_path)
+    agg = OrderedDict()
+    for v in by.values():
+        a = agg.setdefault(v["kernel"], [0, 0.0])
+        a[0] += 1
+        a[1] += v["gpu__time_duration.sum"] / 1000.0
+    total = sum(a[1] for a in agg.values())
+    gemm = sum(a[1] for k, a in agg.items() if "wgemm_kernel" in k)
+    rows = []
+    for k, (n, us) in agg.items():
+        name = k if len(k) <= 90 else k[:87] + "..."
+        cfg = _config_of_kernel(k) if "wgemm_kernel" in k else "—"
+        g = 100.0 * us / gemm if "wgemm_kernel" in k and gemm > 0 else 0.0
+        rows.append(f"| `{name}` | {cfg} | {n} | {us:.1f} | {100.0 * us / total:.1f} % | "
+                    f"{g:.1f} % |")
+    p = os.path.join(PROFILES, "launches_sweep.md")
+    text = open(p).read()
+    header = ("| kernel | configuration | launches | total µs | share of all | share of wgemm |\n"
+              "|---|---|---|---|---|---|\n")
+    text = _set_digest(_replace_table(text, header, rows), _bench().kernel_source_digest())
+    open(p, "w").write(text)
+    print("\n".join(rows))
+
+
 def _config_of_kernel(kernel: str) -> str:
     """The configuration name of a launched kernel, from its Cfg<...> arguments."""
     m = re.search(r"Cfg<([0-9, ]+)>", kernel)
@@ -159,6 +187,8 @@ def main(argv=None) -> int:
         dram(argv[1])
     elif len(argv) >= 3 and argv[0] == "roofline":
         roofline(argv[1], argv[2])
+    elif len(argv) >= 2 and argv[0] == "launches":
+        launches(argv[1])
     else:
         print(__doc__)
         return 2
