@@ -1,0 +1,35 @@
+"""The measurement tools beside the bench run on the GPU and report sane
+figures: the cuBLAS comparison (the two arms agree on the contraction) and
+the copy-engine measurement."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_compare_with_cublas_on_1024():
+    r = subprocess.run([sys.executable, "-m", "dense_fp16_gemm_02_gb300.compare",
+                        "--workload", "c1", "--rounds", "2"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    shape, summary = lines[0], lines[-1]["summary"]
+    assert shape["shape"] == "1024x1024x1024"
+    assert shape["ours_us"] > 0 and shape["cublas_us"] > 0
+    # Both arms accumulate in fp32 over K = 1024: far inside the parity bound.
+    assert shape["max_rel_diff_vs_abs_product"] < 1e-5
+    assert summary["shapes"] == 1 and summary["geomean_speedup"] > 0
+
+
+def test_copy_engine_rates():
+    from dense_fp16_gemm_02_gb300 import peak
+    rows = peak.copy_rates(sizes_mib=(8,), reps=2)
+    assert len(rows) == 1
+    assert rows[0]["h2d_gbs"] > 1.0 and rows[0]["d2h_gbs"] > 1.0
+    assert rows[0]["both_directions_gbs"] > 1.0
