@@ -245,6 +245,24 @@ def test_padding_past_k_never_read():
         check_full(A, B, K, "uniform", name, config=name, mode=DP)
 
 
+@pytest.mark.parametrize("extra_rows", [0, 17])
+def test_row_multicast_second_group_past_m(extra_rows):
+    """Row multicast: the second MMA group of a cluster tile needs no rows of
+    C when M ends inside (or at the end of) the first group's rows, but its
+    producer still loads and multicasts its half of the B slice, which the
+    first group reads. M = one group's rows (+ a ragged 17 more rows, which
+    puts the second group of the last tile partly in range), N ragged over
+    several cluster tiles, K several k-blocks with a ragged tail; exact on
+    integers."""
+    names = [n for n in configs() if re.match(r"g\dr2_", n)]
+    assert names, "row-multicast configurations are compiled"
+    for name in names:
+        bn = int(name.split("_")[1].split("x")[1]) // 2  # tile rows = 2 groups of BN
+        M, N, K = bn + extra_rows, 900, 200
+        A, B = operands(M, N, K, 41, "int")
+        check_full(A, B, K, "int", f"{name} M={M}", config=name, mode=DP)
+
+
 def test_unaligned_c_rows_use_register_stores():
     # N = 53: rows of a contiguous C are not 16-byte aligned; the default
     # choice stores from registers and the result is still exact.
