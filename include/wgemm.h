@@ -192,7 +192,19 @@ int wgemm_bf16bf16(const wgemm_bf16_t* A, const wgemm_bf16_t* B, wgemm_bf16_t* C
  */
 int wgemm_set_pdl(int enable);
 
-/* Number of compiled kernel configurations, and the name of one ("" if out of range). */
+/*
+ * Number of compiled kernel configurations, and the name of one ("" if out
+ * of range). A name reads g<G>[m2|r2]_<C>x<R>_s<S>_a<A>_<E>[_clc][_ab<F>][_h]:
+ * G CTAs per MMA (1, or 2 for a CTA pair); m2 = two MMA groups per cluster
+ * side by side along C's columns sharing the A tile, r2 = two groups stacked
+ * along C's rows sharing the B tile; C × R the C columns × rows of one
+ * worker (cluster) tile; S ring stages; A TMEM accumulators; E the epilogue
+ * (direct: stores from registers, tma: staged TMA stores); _clc tiles taken
+ * by cluster launch control (else a static persistent schedule); _ab<F> the
+ * fused alpha/beta/bias epilogue with an F-block Cin ring; _h a 16-bit C.
+ * Split-K and stream-K run on the static, fp32, unfused "tma" configurations
+ * without m2 or r2.
+ */
 int wgemm_num_configs(void);
 const char* wgemm_config_name(int config_id);
 
