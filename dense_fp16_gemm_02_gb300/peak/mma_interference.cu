@@ -13,6 +13,8 @@
 //   sts       shared-memory stores, 128 B per warp instruction
 //   lds       shared-memory loads, 128 B per warp instruction
 //   tmem_ld   tcgen05.ld 32x32b.x32 from TMEM columns the MMAs do not use
+//   tmem_x16  the same bytes in 32x32b.x16 loads (half the columns per load)
+//   tmem_x64  the same bytes in 32x32b.x64 loads (twice the columns per load)
 //   bulk      cp.async.bulk global → shared, 16 KB copies, four in flight
 //             per CTA (what the TMA producer does in the k-loop)
 //
@@ -53,9 +55,42 @@ constexpr int kEpiColBlocks = 8;               // 32-column blocks cycled throug
 constexpr int kBulkBytes = 16 * 1024;
 constexpr int kBulkSrcBytes = 1 << 20;
 
-enum Mode { kNone, kGst, kGstV4, kEpi, kSts, kLds, kTmemLd, kBulk, kModes };
-const char* const kModeNames[kModes] = {"none", "gst", "gst_v4", "epi",
-                                        "sts",  "lds", "tmem_ld", "bulk"};
+enum Mode { kNone, kGst, kGstV4, kEpi, kSts, kLds, kTmemLd, kBulk, kTmemX16, kTmemX64, kModes };
+const char* const kModeNames[kModes] = {"none", "gst",  "gst_v4",   "epi",     "sts",
+                                        "lds",  "tmem_ld", "bulk", "tmem_x16", "tmem_x64"};
+
+// 32 lanes × 16 / 64 consecutive 32-bit columns per thread (cf. the x32 load).
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_x64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]),
+        "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+        "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+        "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),
+        "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
 
 __device__ bool wait_parity(uint32_t bar, uint32_t parity) {
   const unsigned long long w0 = global_timer_ns();
@@ -192,6 +227,25 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) acc += __uint_as_float(r[e]);
           n += 32 * 128;
+          break;
+        }
+        case kTmemX16: {  // two x16 loads per iteration: the bytes of one x32
+          uint32_t r16a[16], r16b[16];
+          tmem_ld_x16(taddr + (it % 8u) * 32u, r16a);
+          tmem_ld_x16(taddr + (it % 8u) * 32u + 16u, r16b);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc += __uint_as_float(r16a[e]) + __uint_as_float(r16b[e]);
+          n += 32 * 128;
+          break;
+        }
+        case kTmemX64: {  // one x64 load per iteration: the bytes of two x32
+          uint32_t r64[64];
+          tmem_ld_x64(taddr + (it % 4u) * 64u, r64);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 64; ++e) acc += __uint_as_float(r64[e]);
+          n += 64 * 128;
           break;
         }
         case kBulk: {
