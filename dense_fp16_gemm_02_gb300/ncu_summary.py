@@ -103,18 +103,22 @@ def roofline(csv_path: str, bench_json: str) -> None:
         M, N, K = (int(x) for x in s["shape"].split("x"))
         t = v["gpu__time_duration.sum"] / 1000.0
         active = 100.0 * v["sm__cycles_active.avg"] / v["gpc__cycles_elapsed.max"]
+        grid = int(v.get("launch__grid_size", 0))
         rows.append(
-            f"| {M}×{N}×{K} | {s['config']} | {s['mode']} | {s['us_median']:.3f} | {s['tflops']} | "
+            f"| {M}×{N}×{K} | {s['config']} | {s['mode']} | {grid} | "
+            f"{_waves(s['config'], M, N, grid, s['mode'], s.get('splits', 1))} | "
+            f"{s['us_median']:.3f} | {s['tflops']} | "
             f"{s['tensor_frac']} | {t:.1f} | {2 * M * N * K / t / 1e6:.1f} | "
             f"{v['sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed']:.1f} | "
             f"{active:.1f} | {v['dram__bytes_read.sum'] / 1e6:.1f} | "
             f"{v['dram__bytes_write.sum'] / 1e6:.1f} | {s['hbm_frac']} |")
     p = os.path.join(PROFILES, "roofline_all_shapes.md")
     text = open(p).read()
-    header = ("| M×N×K | configuration | mode | bench µs (median) | bench TFLOP/s | tensor frac "
-              "(bench) | ncu µs | ncu TFLOP/s | tensor pipe active % (ncu) | SM active % (ncu) | "
-              "DRAM read MB | DRAM write MB | HBM frac (bench, compulsory bytes) |\n"
-              "|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
+    header = ("| M×N×K | configuration | mode | grid (CTAs) | waves | bench µs (median) | "
+              "bench TFLOP/s | tensor frac (bench) | ncu µs | ncu TFLOP/s | tensor pipe active % "
+              "(ncu) | SM active % (ncu) | DRAM read MB | DRAM write MB | HBM frac (bench, "
+              "compulsory bytes) |\n"
+              "|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
     text = _set_digest(_replace_table(text, header, rows), b.kernel_source_digest())
     open(p, "w").write(text)
     print("\n".join(rows))
@@ -144,6 +148,28 @@ def launches(csv_path: str) -> None:
     text = _set_digest(_replace_table(text, header, rows), _bench().kernel_source_digest())
     open(p, "w").write(text)
     print("\n".join(rows))
+
+
+def _waves(config: str, M: int, N: int, grid: int, mode: str, splits: int) -> str:
+    """Worker tiles (units, for split-K) per co-resident worker: the number
+    of waves of the launch, from the configuration's tile and cluster."""
+    a = _entry_args(config)
+    if not a or grid <= 0:
+        return "—"
+    cg, reps, bn, _, _, _, mc, _, _, _, mr = a
+    tile_cols, tile_rows = 128 * reps * cg * mc, bn * mr
+    tiles = -(-M // tile_rows) * -(-N // tile_cols)
+    cluster = cg * mc * mr
+    workers = grid // cluster
+    if config.endswith("_clc"):
+        # One cluster per tile is launched; the co-resident ones take tiles
+        # from the others (GB300: 152 CTAs, 76 pairs, 36 clusters of four).
+        workers = min(workers, {1: 152, 2: 76, 4: 36}.get(cluster, workers))
+    if mode == "split-K":
+        tiles *= splits
+    elif mode == "stream-K":
+        return "1 (stream)"
+    return f"{tiles / workers:.2f}"
 
 
 def _config_of_kernel(kernel: str) -> str:
