@@ -286,6 +286,14 @@ const RateRow* rate_of(const char* name) {
 // Operand rows of both A and B start on 32-byte sectors.
 bool rows_on_sectors(int lda, int ldb) { return lda % 16 == 0 && ldb % 16 == 0; }
 
+// Configurations that may run split-K or stream-K plans: TMA epilogue (the
+// reduce-adds), static schedule and no multicast (every worker resident and
+// owning its own tiles), fp32 C and no fused epilogue. The kernel compiles
+// its split-K and stream-K paths for exactly these (Cfg::kKSplit).
+bool can_split_k(const KernelEntry& e) {
+  return e.epi == kEpiTma && e.mc == 1 && e.mr == 1 && e.sched == 0 && e.out == 0 && !e.fuse;
+}
+
 // Predicted microseconds of a configuration and K-decomposition from the
 // measured rates, with `workers` co-resident workers; < 0 if not modelled.
 double predict_us(const KernelEntry& e, int M, int N, int K, bool aligned, int mode, int splits,
@@ -352,8 +360,7 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
       }
     };
     consider(kDataParallel, 1);
-    const bool ksplit =
-        e.epi == kEpiTma && e.mc == 1 && e.mr == 1 && e.sched == 0 && e.out == 0 && !e.fuse;
+    const bool ksplit = can_split_k(e);
     const int64_t tiles = (int64_t)((M + e.tile_rows - 1) / e.tile_rows) *
                           ((N + e.tile_cols - 1) / e.tile_cols);
     const int kblocks = (K + kBK - 1) / kBK;
@@ -433,9 +440,7 @@ int make_plan(const KernelEntry& e, int M, int N, int K, int mode, int splits, i
   p->mode = mode;
   p->splits = 1;
   p->group = raster_group();
-  if (mode != kDataParallel &&
-      (e.epi != kEpiTma || e.mc != 1 || e.mr != 1 || e.sched != 0 || e.out != 0 || e.fuse != 0))
-    return WGEMM_ERR_CONFIG;
+  if (mode != kDataParallel && !can_split_k(e)) return WGEMM_ERR_CONFIG;
   p->sched = e.sched;
   if (mode == kDataParallel && e.sched == 1) {
     p->workers = p->num_tiles;  // one cluster per tile; running clusters take the rest
@@ -858,7 +863,8 @@ int wgemm_debug_plan(int M, int N, int K, int config_id, int mode, int splits, i
   for (int w = 0; w < p.workers; ++w) {
     for (int i = 0;; ++i) {
       Unit u;
-      if (!plan_unit(p, w, i, u)) break;
+      // The unit walk the configuration's kernel compiles (Cfg::kKSplit).
+      if (!(can_split_k(e) ? plan_unit(p, w, i, u) : plan_unit_dp(p, w, i, u))) break;
       if (out && n < max_units) {
         int32_t* o = out + 7 * n;
         o[0] = u.tile; o[1] = u.tm; o[2] = u.tn; o[3] = u.kb_begin; o[4] = u.kb_end;

@@ -216,6 +216,11 @@ struct Cfg {
   static constexpr uint32_t kOffResp = (kOffMisc + 16 + 15) / 16 * 16;
   static constexpr uint32_t kSmemBytes = kOffResp + 16 * kClcDepth + 1024;  // + alignment slack
 
+  // The configurations the host may give a split-K or stream-K plan; every
+  // other one runs data-parallel plans only and compiles just that path.
+  static constexpr bool kKSplit =
+      EPI == kEpiTma && SCHED == kSchedStatic && MC == 1 && MR == 1 && OUT == kOut32 && FUSE == 0;
+
   static_assert(CG == 1 || CG == 2, "CG");
   static_assert(OUT == kOut32 || OUT == kOut16, "OUT");
   static_assert(!FUSE || EPI == kEpiDirect, "the fused epilogue stores from registers");
@@ -373,6 +378,12 @@ struct Kernel {
     return base + K::kOffCin + (q * K::kCinSlots + s) * K::kEpiSlotBytes;
   }
 
+  // Unit i of the worker in the plan (see plan_unit).
+  __device__ static bool unit_at(const Plan& plan, int32_t worker, int32_t i, Unit& u) {
+    if constexpr (K::kKSplit) return plan_unit(plan, worker, i, u);
+    else return plan_unit_dp(plan, worker, i, u);
+  }
+
   // Unit i of this CTA's worker (cluster). Static scheduling: the plan's
   // order. Cluster launch control: unit 0 is the worker's own tile, unit
   // i > 0 is the tile of the cluster that CLC response i−1 cancelled; the
@@ -384,7 +395,7 @@ struct Kernel {
                                    bool release, bool warp_wide, Unit& u, bool& ok,
                                    volatile uint32_t* abort_flag, int32_t site) {
     if constexpr (K::SCHED == kSchedStatic) {
-      return plan_unit(p.plan, worker, i, u);
+      return unit_at(p.plan, worker, i, u);
     } else {
       if (i == 0) {
         if (worker >= p.plan.num_tiles) return false;
@@ -535,7 +546,7 @@ struct Kernel {
         have = worker < p.plan.num_tiles;
         if (have) plan_tile_unit(p.plan, worker, u);
       } else {
-        have = plan_unit(p.plan, worker, 0, u);
+        have = unit_at(p.plan, worker, 0, u);
       }
       if (!have || !unit_ok(p, u)) return 0;
       const int32_t b_row0 = u.tn * K::kTileCols + (int32_t)rank * K::kCtaCols;
@@ -688,7 +699,7 @@ struct Kernel {
                                      int32_t worker, int32_t i) {
     CinUnit g{0, 0, 0, 0};
     Unit u;
-    if (!plan_unit(p.plan, worker, i, u)) return g;
+    if (!unit_at(p.plan, worker, i, u)) return g;
     const int32_t M = p.plan.M, N = p.plan.N;
     constexpr int kChunks = K::BN / 32;
     g.col_cta = u.tn * K::kTileCols + col_group(grp) * K::kGroupCols + (int32_t)rank * K::kCtaCols;
@@ -1006,7 +1017,7 @@ struct Kernel {
       bool tail = false;
       if constexpr (K::kTailGroups > 1) {
         Unit u_next;
-        tail = !plan_unit(p.plan, worker, i + 1, u_next);
+        tail = !unit_at(p.plan, worker, i + 1, u_next);
       }
       int32_t batch = 0;
 #pragma unroll 1
@@ -1085,7 +1096,7 @@ struct Kernel {
     const int32_t t = (int32_t)threadIdx.x - 128;  // 0..127
     for (int32_t i = 0;; ++i) {
       Unit u;
-      if (!plan_unit(p.plan, worker, i, u)) break;
+      if (!unit_at(p.plan, worker, i, u)) break;
       int32_t r0, r1;
       plan_zero_rows(K::BN, p.plan.splits, u.split, r0, r1);
       const int32_t group_row0 = u.tm * K::kTileRows + row_group(grp) * K::BN;
@@ -1115,7 +1126,7 @@ struct Kernel {
       fence_acq_rel_gpu();
       for (int32_t i = 0;; ++i) {
         Unit u;
-        if (!plan_unit(p.plan, worker, i, u)) break;
+        if (!unit_at(p.plan, worker, i, u)) break;
         const int32_t fi = (u.tile * K::kClusterSize + crank) * p.plan.splits + u.split;
         if (WG_CHECK(p.status, fi < p.flag_words, kCheckFlag, fi))
           st_release_gpu(p.flags + fi, p.epoch);

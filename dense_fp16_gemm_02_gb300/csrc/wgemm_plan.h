@@ -132,6 +132,20 @@ WG_PLAN_HD bool plan_unit(const Plan& p, int32_t w, int32_t i, Unit& u) {
   return true;
 }
 
+// plan_unit for kernels that never split K (the host gives them data-parallel
+// plans only): the same units without the split-K and stream-K arithmetic.
+WG_PLAN_HD bool plan_unit_dp(const Plan& p, int32_t w, int32_t i, Unit& u) {
+  if (p.sched == 1) {
+    if (i > 0 || w >= p.num_tiles) return false;
+    plan_tile_unit(p, w, u);
+    return true;
+  }
+  const int32_t idx = w + i * p.workers;
+  if (idx >= p.num_tiles) return false;
+  plan_tile_unit(p, idx, u);
+  return true;
+}
+
 // Rows [r0, r1) of a tile's `tile_rows` that split `s` of `S` zeroes.
 WG_PLAN_HD void plan_zero_rows(int32_t tile_rows, int32_t S, int32_t s, int32_t& r0, int32_t& r1) {
   const int32_t per = (tile_rows + S - 1) / S;
