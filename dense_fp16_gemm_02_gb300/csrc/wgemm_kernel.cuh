@@ -934,7 +934,7 @@ struct Kernel {
           const int32_t row_c = row0 + (c0 + b) * 32;
           // 16-bit C is written by data-parallel units only: partial sums
           // are never rounded to 16 bits before they are added.
-          if (K::OUT == kOut32 && add) tma_reduce_add_2d(&p.tmC, sbuf, col_warp, row_c);
+          if (K::kKSplit && add) tma_reduce_add_2d(&p.tmC, sbuf, col_warp, row_c);
           else tma_store_2d(&p.tmC, sbuf, col_warp, row_c);
         }
         bulk_commit_group();
@@ -954,7 +954,7 @@ struct Kernel {
     bool ok = true;
     uint32_t sync_phase = 0;
 
-    if constexpr (K::EPI == kEpiTma && K::OUT == kOut32) {
+    if constexpr (K::kKSplit) {
       if (p.plan.mode == kSplitK)
         ok = zero_slices(p, base, rank, grp, worker, sync_phase, abort_flag);
     }
@@ -983,8 +983,10 @@ struct Kernel {
       const int32_t col_cta =
           u.tn * K::kTileCols + col_group(grp) * K::kGroupCols + (int32_t)rank * K::kCtaCols;
       const int32_t row0 = u.tm * K::kTileRows + row_group(grp) * K::BN;
-      const bool add = u.kind == kUnitAddAfterOwner || u.kind == kUnitAddAfterZero;
-      if constexpr (K::EPI == kEpiTma) {
+      // Only K-split units add into C (data-parallel units store).
+      const bool add =
+          K::kKSplit && (u.kind == kUnitAddAfterOwner || u.kind == kUnitAddAfterZero);
+      if constexpr (K::kKSplit) {
         if (add && lane == 0) {
           if (u.kind == kUnitAddAfterOwner) {
             ok = WG_CHECK(p.status, (int32_t)(u.tile * K::kClusterSize + crank) < p.flag_words, kCheckFlag,
@@ -1050,7 +1052,7 @@ struct Kernel {
         if (!ok) break;
       }
       if (!ok) break;
-      if constexpr (K::EPI == kEpiTma) {
+      if constexpr (K::kKSplit) {
         if (u.kind == kUnitStoreRaise) {
           // Owner of the tile's first k-block: make the stores complete and
           // visible, then raise the flag for the CTAs that add to this tile.
