@@ -172,21 +172,66 @@ def sweep(shapes, out_path):
                   indent=1)
 
 
-def emit(json_path, inc_path=TUNED_INC):
-    """Writes the measured winners as a C table the library compiles in."""
-    with open(json_path) as f:
-        d = json.load(f)
+def _score(c):
+    """A candidate's time in one sweep: its interleaved time if it was a
+    finalist, else its screen median."""
+    return c.get("us_interleaved", c["us"])
+
+
+def combine(sweeps):
+    """Per shape, the candidate (configuration, mode, splits) with the lowest
+    mean time relative to each sweep's best, over the sweeps that timed it.
+    Sweeps on different boxes rank near-equal cluster configurations
+    differently (each chip groups its SMs differently), so one box's winner
+    is not taken on its own; relative times remove the boxes' overall speed.
+    Returns {shape: (candidate dict with "us" = mean time, relative score)}."""
+    per_shape = {}
+    for d in sweeps:
+        for r in d["results"]:
+            shape = tuple(r["shape"])
+            best = min(_score(c) for c in r["candidates"])
+            acc = per_shape.setdefault(shape, {})
+            for c in r["candidates"]:
+                key = (c["config"], c["mode"], c["splits"])
+                rel, us = acc.get(key, ([], []))
+                rel.append(_score(c) / best)
+                us.append(_score(c))
+                acc[key] = (rel, us)
+    out = {}
+    for shape, acc in per_shape.items():
+        n = max(len(v[0]) for v in acc.values())
+        # Candidates timed in every sweep only (a candidate that failed on a
+        # box, or was not compiled there, does not win by absence).
+        full = {k: v for k, v in acc.items() if len(v[0]) == n}
+        key, (rel, us) = min(full.items(), key=lambda kv: sum(kv[1][0]) / len(kv[1][0]))
+        out[shape] = ({"config": key[0], "mode": key[1], "splits": key[2],
+                       "us": sum(us) / len(us)}, sum(rel) / len(rel))
+    return out
+
+
+def emit(json_paths, inc_path=TUNED_INC):
+    """Writes the measured winners as a C table the library compiles in, from
+    one sweep or several (see combine)."""
+    if isinstance(json_paths, str):
+        json_paths = [json_paths]
+    sweeps = []
+    for path in json_paths:
+        with open(path) as f:
+            sweeps.append(json.load(f))
+    d = sweeps[0]
+    boxes = f"{len(sweeps)} sweep" + ("s" if len(sweeps) > 1 else "")
     lines = [
-        "// Measured per-shape winners (generated by dense_fp16_gemm_02_gb300/tune.py on",
-        f"// {d.get('gpu', 'a GB300')} with {d.get('sm_count')} SMs; do not edit by hand).",
+        "// Measured per-shape winners (generated by dense_fp16_gemm_02_gb300/tune.py from",
+        f"// {boxes} on {d.get('gpu', 'a GB300')} with {d.get('sm_count')} SMs; do not edit by hand).",
         "// {M, N, K, configuration name, mode (0 data parallel, 1 split-K, 2 stream-K),",
-        "//  splits, measured µs per call}",
+        "//  splits, measured µs per call (mean over the sweeps)}",
     ]
+    chosen = combine(sweeps)
     for r in d["results"]:
         M, N, K = r["shape"]
-        b = r["best"]
+        b, _ = chosen[(M, N, K)]
         lines.append(f'{{{M}, {N}, {K}, "{b["config"]}", {b["mode"]}, {b["splits"]}, '
-                     f'{b.get("us_interleaved", b["us"]):.3f}}},')
+                     f'{b["us"]:.3f}}},')
     with open(inc_path, "w") as f:
         f.write("\n".join(lines) + "\n")
     return inc_path
@@ -425,7 +470,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--out", default="tune.json")
     ap.add_argument("--shapes", default="all")
-    ap.add_argument("--emit", metavar="JSON", help="write csrc/wgemm_tuned.inc from a sweep")
+    ap.add_argument("--emit", metavar="JSON", nargs="+",
+                    help="write csrc/wgemm_tuned.inc from one or more sweeps (several boxes)")
     ap.add_argument("--rates", metavar="JSON", help="measure per-configuration rates")
     ap.add_argument("--emit-rates", metavar="JSON", nargs="+",
                     help="write csrc/wgemm_rates.inc (later files override earlier rows)")

@@ -13,14 +13,23 @@ def test_mid_mean_trims_a_quarter_each_end():
     assert tune._mid_mean([20.5, 21.5] * 10) == 21.0
 
 
+def _sweep(shape, cands):
+    return {"gpu": "test GPU", "sm_count": 152, "results": [
+        {"shape": list(shape), "best": cands[0], "candidates": cands}]}
+
+
+def _c(config, us, inter=None, mode=0, splits=1):
+    c = {"config": config, "mode": mode, "splits": splits, "us": us}
+    if inter is not None:
+        c["us_interleaved"] = inter
+    return c
+
+
 def test_emit_prefers_the_interleaved_time(tmp_path):
-    d = {"gpu": "test GPU", "sm_count": 152, "results": [
-        {"shape": [64, 128, 256],
-         "best": {"config": "g1_128x64_s8_a2_direct", "mode": 0, "splits": 1, "us": 9.0,
-                  "us_interleaved": 8.5}},
-        {"shape": [1024, 1024, 65536],
-         "best": {"config": "g2_512x256_s4_a1_tma", "mode": 1, "splits": 9, "us": 96.25}},
-    ]}
+    d = _sweep((64, 128, 256), [_c("g1_128x64_s8_a2_direct", 9.0, 8.5),
+                                _c("g1_128x128_s6_a2_tma", 8.9, 8.8)])
+    d["results"].append({"shape": [1024, 1024, 65536], "candidates": [
+        _c("g2_512x256_s4_a1_tma", 96.25, mode=1, splits=9)]})
     js = tmp_path / "t.json"
     js.write_text(json.dumps(d))
     inc = tmp_path / "t.inc"
@@ -29,6 +38,23 @@ def test_emit_prefers_the_interleaved_time(tmp_path):
     assert rows == ['{64, 128, 256, "g1_128x64_s8_a2_direct", 0, 1, 8.500},',
                     '{1024, 1024, 65536, "g2_512x256_s4_a1_tma", 1, 9, 96.250},']
     assert "do not edit by hand" in inc.read_text()
+
+
+def test_combine_takes_the_best_mean_over_boxes():
+    # X wins box 1 by 2 % but loses box 2 by 10 %; Y is steady. Box 2 is 5 %
+    # faster overall, which the relative scores remove.
+    shape = (1536, 1536, 1536)
+    box1 = _sweep(shape, [_c("X", 15.0, 15.0), _c("Y", 15.3, 15.3)])
+    box2 = _sweep(shape, [_c("Y", 14.5, 14.5), _c("X", 15.95, 15.95)])
+    got, score = tune.combine([box1, box2])[shape]
+    assert got["config"] == "Y" and abs(got["us"] - 14.9) < 1e-9
+    assert abs(score - (15.3 / 15.0 + 1.0) / 2) < 1e-12
+    # One sweep alone keeps its own winner.
+    assert tune.combine([box1])[shape][0]["config"] == "X"
+    # A candidate missing from a sweep cannot win by absence.
+    box3 = _sweep(shape, [_c("Z", 10.0, 10.0), _c("Y", 15.0, 15.0)])
+    box4 = _sweep(shape, [_c("Y", 15.0, 15.0)])
+    assert tune.combine([box3, box4])[shape][0]["config"] == "Y"
 
 
 def _rows(*us):
