@@ -372,8 +372,10 @@ def run_ours(args):
     by_config = {}
     for i, (M, N, K) in enumerate(shapes):
         us = times[:, i] * 1e3
-        cfg, mode, splits = wgemm.wgemm_select(M, N, K, c_type=c_type,
-                                               fused=args.epilogue == "fused")
+        # The fused bench call is in place with beta = 1: with fp32 D it may
+        # also take the reduce-add kernels (fused kind 2).
+        fused_kind = 0 if args.epilogue != "fused" else (2 if c_type == wgemm.WGEMM_F32 else 1)
+        cfg, mode, splits = wgemm.wgemm_select(M, N, K, c_type=c_type, fused=fused_kind)
         med = float(np.median(us))
         tf = flops[i] / (med * 1e-6) / 1e12
         c_rw = (2 if args.epilogue == "fused" else 1) * c_bytes * M * N  # C written (and read)

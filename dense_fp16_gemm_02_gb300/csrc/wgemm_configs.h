@@ -77,6 +77,12 @@ extern const int kNumEntriesRowMc;
 #define WG_ENTRY_AB(NAME, CG, REPS, BN, STAGES, ACC, SLOTS) \
   WG_ENTRY_ANY(NAME "_ab" #SLOTS, CG, REPS, BN, STAGES, ACC, wg::kEpiDirect, 1, wg::kSchedStatic, \
                wg::kOut32, SLOTS)
+// The in-place form D += alpha·A·Bᵀ + bias (beta = 1, Cin = D, fp32 D) with
+// the TMA epilogue: its stores are reduce-adds into D and it reads no Cin.
+// "_ab1" after a "_tma" name.
+#define WG_ENTRY_AB_RED(NAME, CG, REPS, BN, STAGES, ACC) \
+  WG_ENTRY_ANY(NAME "_ab1", CG, REPS, BN, STAGES, ACC, wg::kEpiTma, 1, wg::kSchedStatic, \
+               wg::kOut32, 1)
 #define WG_ENTRY_AB_H(NAME, CG, REPS, BN, STAGES, ACC, SLOTS) \
   WG_ENTRY_ANY(NAME "_ab" #SLOTS "_h", CG, REPS, BN, STAGES, ACC, wg::kEpiDirect, 1, \
                wg::kSchedStatic, wg::kOut16, SLOTS)

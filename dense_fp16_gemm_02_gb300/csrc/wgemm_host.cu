@@ -286,6 +286,19 @@ const RateRow* rate_of(const char* name) {
 // Operand rows of both A and B start on 32-byte sectors.
 bool rows_on_sectors(int lda, int ldb) { return lda % 16 == 0 && ldb % 16 == 0; }
 
+// The fused epilogue of a configuration: 0 none, 1 the Cin ring (register
+// stores; any alpha, beta, Cin), 2 the reduce-add form (TMA epilogue; only
+// D += alpha·A·Bᵀ + bias in place, fp32).
+int fuse_kind(const KernelEntry& e) { return e.fuse == 0 ? 0 : (e.epi == kEpiTma ? 2 : 1); }
+
+// Whether a configuration serves a call whose epilogue is `fuse` (0 plain, 1
+// general fused, 2 fused in place with beta = 1 and fp32 D, which either
+// fused form can compute).
+bool fuse_fits(const KernelEntry& e, int fuse) {
+  const int k = fuse_kind(e);
+  return fuse == 2 ? k != 0 : k == fuse;
+}
+
 // Configurations that may run split-K or stream-K plans: TMA epilogue (the
 // reduce-adds), static schedule and no multicast (every worker resident and
 // owning its own tiles), fp32 C and no fused epilogue. The kernel compiles
@@ -346,8 +359,7 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
   double best_us = 0.0, best_split_us = 0.0;
   for (int id = 0; id < (int)es.size(); ++id) {
     const KernelEntry& e = *es[id];
-    if (e.out != out || (e.fuse != 0) != (fuse != 0) || (e.epi == kEpiTma && !c_tma_ok))
-      continue;
+    if (e.out != out || !fuse_fits(e, fuse) || (e.epi == kEpiTma && !c_tma_ok)) continue;
     const int w = max_workers(st, id);
     if (w <= 0) continue;
     auto consider = [&](int mode, int splits) {
@@ -492,7 +504,11 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
         const EpiArgs& ep = EpiArgs()) {
   if (!ab_type_ok(ab_type) || !c_type_ok(c_type)) return WGEMM_ERR_INVALID_ARG;
   const int cb = c_bytes(c_type), out = c_type == WGEMM_F32 ? 0 : 1;
-  const int fuse = ep.fused ? 1 : 0;
+  // D += alpha·A·Bᵀ + bias in place (Cin = D, beta = 1, fp32 D) may also
+  // run the reduce-add kernels.
+  const bool in_place = ep.fused && ep.beta == 1.f && ep.cin == C && ep.ldcin == ldc &&
+                        c_type == WGEMM_F32;
+  const int fuse = ep.fused ? (in_place ? 2 : 1) : 0;
   int rc = check_args(A, B, C, M, N, K, lda, ldb, ldc, cb);
   if (rc != WGEMM_OK) return rc;
   const bool load_cin = ep.fused && ep.beta != 0.f;
@@ -527,7 +543,7 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
   }
   if (config_id < 0 || config_id >= (int)es.size()) return WGEMM_ERR_CONFIG;
   const KernelEntry& e = *es[config_id];
-  if (e.out != out || (e.fuse != 0) != (fuse != 0)) return WGEMM_ERR_CONFIG;
+  if (e.out != out || !fuse_fits(e, fuse)) return WGEMM_ERR_CONFIG;
   if (e.epi == kEpiTma && !c_ok) return WGEMM_ERR_ALIGNMENT;
   if (mode < 0) {
     Choice c = choose(*st, M, N, K, lda, ldb, c_ok, out, fuse);
@@ -562,8 +578,9 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
     params.alpha = ep.alpha;
     params.beta = ep.beta;
     params.bias = ep.bias;
-    params.load_cin = load_cin ? 1 : 0;
-    if (load_cin && !encode_2d(&params.tmCin, tma_type(c_type), ep.cin, (uint64_t)N, (uint64_t)M,
+    // The reduce-add form adds into D's old values in L2: no Cin read.
+    params.load_cin = load_cin && fuse_kind(e) == 1 ? 1 : 0;
+    if (params.load_cin && !encode_2d(&params.tmCin, tma_type(c_type), ep.cin, (uint64_t)N, (uint64_t)M,
                                (uint64_t)ep.ldcin * cb, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
       return WGEMM_ERR_LAUNCH;
   }
@@ -696,8 +713,8 @@ const char* wgemm_config_name(int id) {
 
 int wgemm_select(int M, int N, int K, int lda, int ldb, int c_type, int fused, int* config_id,
                  int* mode, int* splits) {
-  if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || !c_type_ok(c_type) ||
-      (fused != 0 && fused != 1))
+  if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || !c_type_ok(c_type) || fused < 0 ||
+      fused > 2 || (fused == 2 && c_type != WGEMM_F32))
     return WGEMM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
   int dev;

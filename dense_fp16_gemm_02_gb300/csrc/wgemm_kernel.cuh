@@ -146,8 +146,10 @@ template <int CG_, int REPS_, int BN_, int STAGES_, int ACC_, int EPI_, int MC_ 
           int SCHED_ = kSchedStatic, int OUT_ = kOut32, int FUSE_ = 0, int MR_ = 1>
 struct Cfg {
   static constexpr int OUT = OUT_;        // OutWidth: fp32 C, or 16-bit C (data parallel only)
-  // FUSE > 0: alpha/beta/bias epilogue (data parallel only) whose Cin ring
-  // has FUSE slots per epilogue warp.
+  // FUSE > 0: alpha/beta/bias epilogue (data parallel only). With register
+  // stores its Cin ring has FUSE slots per epilogue warp; with the TMA
+  // epilogue (fp32 D) it is the in-place form D += alpha·acc + bias, added
+  // into D by TMA reduce-adds, with no Cin ring.
   static constexpr int FUSE = FUSE_;
   static constexpr int SCHED = SCHED_;    // SchedMode
   static constexpr int CG = CG_;          // CTAs per MMA: 1, or 2 (pair)
@@ -198,7 +200,8 @@ struct Cfg {
   static constexpr uint32_t kTailWarpBytes = kTailGroups * kEpiBatch * kEpiSlotBytes;
   // Fused epilogue: each epilogue warp prefetches its 32×32 blocks of Cin
   // with TMA into a private ring of kCinSlots slots.
-  static constexpr int kCinSlots = FUSE;
+  static constexpr bool kFuseReduce = FUSE > 0 && EPI == kEpiTma;
+  static constexpr int kCinSlots = kFuseReduce ? 0 : FUSE;
   static constexpr uint32_t kCinBytes = 4 * kCinSlots * kEpiSlotBytes;
 
   // Shared-memory layout (offsets from a 1024-byte-aligned base).
@@ -223,7 +226,8 @@ struct Cfg {
 
   static_assert(CG == 1 || CG == 2, "CG");
   static_assert(OUT == kOut32 || OUT == kOut16, "OUT");
-  static_assert(!FUSE || EPI == kEpiDirect, "the fused epilogue stores from registers");
+  static_assert(!FUSE || EPI == kEpiDirect || OUT == kOut32,
+                "the reduce-add fused epilogue writes fp32 D");
   static_assert(kTailGroups >= 1 && 4 * kTailWarpBytes <= STAGES * kStageBytes,
                 "tail staging inside the stage ring");
   static_assert(!FUSE || SCHED == kSchedStatic, "the Cin ring prefetches the next unit");
@@ -731,16 +735,19 @@ struct Kernel {
     f.t = 0;
     f.cur_issued = i == 0 ? 0 : f.pre;  // issued while the previous unit drained
     f.pre = 0;
-    if (!p.load_cin) return;
-    // The slots were last read by this warp's generic loads: order those
-    // reads before the TMA writes that refill them.
-    fence_proxy_async_shared();
-    __syncwarp();
-    // Fill the ring: at most kCinSlots loads in flight.
-    while (f.cur_issued < f.cur.nblk && f.issued - f.consumed < (uint32_t)K::kCinSlots) {
-      if (lane == 0) cin_issue(p, base, q, f.cur, f.issued, f.cur_issued);
-      ++f.issued;
-      ++f.cur_issued;
+    // The reduce-add form reads no Cin: D's old values are added in L2.
+    if constexpr (K::kCinSlots > 0) {
+      if (!p.load_cin) return;
+      // The slots were last read by this warp's generic loads: order those
+      // reads before the TMA writes that refill them.
+      fence_proxy_async_shared();
+      __syncwarp();
+      // Fill the ring: at most kCinSlots loads in flight.
+      while (f.cur_issued < f.cur.nblk && f.issued - f.consumed < (uint32_t)K::kCinSlots) {
+        if (lane == 0) cin_issue(p, base, q, f.cur, f.issued, f.cur_issued);
+        ++f.issued;
+        ++f.cur_issued;
+      }
     }
   }
 
@@ -759,37 +766,41 @@ struct Kernel {
       if (b >= nb) break;
       const int32_t c = c0 + b;
       if (c >= f.cur.lc) break;  // rows past M: nothing of this chunk is stored
-      if (p.load_cin) {
-        const uint32_t slot = f.consumed % (uint32_t)K::kCinSlots;
-        if (!wait_bar(bar_cin(base, q, slot), (f.consumed / (uint32_t)K::kCinSlots) & 1u,
-                      abort_flag, p.status, kSiteEpiCinFull))
-          return false;
-        const uint8_t* sp = smem + (cin_slot(base, q, slot) - base);
+      bool with_cin = false;
+      if constexpr (K::kCinSlots > 0) with_cin = p.load_cin != 0;
+      if (with_cin) {
+        if constexpr (K::kCinSlots > 0) {
+          const uint32_t slot = f.consumed % (uint32_t)K::kCinSlots;
+          if (!wait_bar(bar_cin(base, q, slot), (f.consumed / (uint32_t)K::kCinSlots) & 1u,
+                        abort_flag, p.status, kSiteEpiCinFull))
+            return false;
+          const uint8_t* sp = smem + (cin_slot(base, q, slot) - base);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float cin;
-          if constexpr (K::OUT == kOut16) {
-            const uint16_t h = reinterpret_cast<const uint16_t*>(sp)[e * 32 + lane];
-            cin = p.c_bf16 ? __bfloat162float(__ushort_as_bfloat16(h))
-                           : __half2float(__ushort_as_half(h));
-          } else {
-            cin = reinterpret_cast<const float*>(sp)[e * 32 + lane];
+          for (int e = 0; e < 32; ++e) {
+            float cin;
+            if constexpr (K::OUT == kOut16) {
+              const uint16_t h = reinterpret_cast<const uint16_t*>(sp)[e * 32 + lane];
+              cin = p.c_bf16 ? __bfloat162float(__ushort_as_bfloat16(h))
+                             : __half2float(__ushort_as_half(h));
+            } else {
+              cin = reinterpret_cast<const float*>(sp)[e * 32 + lane];
+            }
+            v[b][e] = __float_as_uint(fmaf(alpha, __uint_as_float(v[b][e]), fmaf(beta, cin, bias)));
           }
-          v[b][e] = __float_as_uint(fmaf(alpha, __uint_as_float(v[b][e]), fmaf(beta, cin, bias)));
-        }
-        ++f.consumed;
-        fence_proxy_async_shared();
-        __syncwarp();
-        // The freed slot takes the next block in consumption order: this
-        // unit's, else the next unit's.
-        if (f.cur_issued < f.cur.nblk) {
-          if (lane == 0) cin_issue(p, base, q, f.cur, f.issued, f.cur_issued);
-          ++f.issued;
-          ++f.cur_issued;
-        } else if (f.pre < f.next.nblk) {
-          if (lane == 0) cin_issue(p, base, q, f.next, f.issued, f.pre);
-          ++f.issued;
-          ++f.pre;
+          ++f.consumed;
+          fence_proxy_async_shared();
+          __syncwarp();
+          // The freed slot takes the next block in consumption order: this
+          // unit's, else the next unit's.
+          if (f.cur_issued < f.cur.nblk) {
+            if (lane == 0) cin_issue(p, base, q, f.cur, f.issued, f.cur_issued);
+            ++f.issued;
+            ++f.cur_issued;
+          } else if (f.pre < f.next.nblk) {
+            if (lane == 0) cin_issue(p, base, q, f.next, f.issued, f.pre);
+            ++f.issued;
+            ++f.pre;
+          }
         }
       } else {
 #pragma unroll
@@ -934,7 +945,8 @@ struct Kernel {
           const int32_t row_c = row0 + (c0 + b) * 32;
           // 16-bit C is written by data-parallel units only: partial sums
           // are never rounded to 16 bits before they are added.
-          if (K::kKSplit && add) tma_reduce_add_2d(&p.tmC, sbuf, col_warp, row_c);
+          // K-split partial sums, and the in-place fused form, add into C.
+          if ((K::kKSplit && add) || K::kFuseReduce) tma_reduce_add_2d(&p.tmC, sbuf, col_warp, row_c);
           else tma_store_2d(&p.tmC, sbuf, col_warp, row_c);
         }
         bulk_commit_group();
@@ -1075,7 +1087,7 @@ struct Kernel {
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
     }
-    if constexpr (K::FUSE) {
+    if constexpr (K::kCinSlots > 0) {
       // Aborted: let this warp's Cin loads in flight land before exit.
       if (!ok && p.load_cin && lane == 0)
         for (uint32_t j = fs.consumed; j != fs.issued; ++j)
@@ -1174,8 +1186,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
       mbar_init(Kernel<K>::bar_clc_full(base, j), 1);
       mbar_init(Kernel<K>::bar_clc_empty(base, j), K::kClcConsumers);
     }
-    for (int j = 0; j < 4 * K::kCinSlots; ++j)
-      mbar_init(Kernel<K>::bar_cin(base, j / K::kCinSlots, j % K::kCinSlots), 1);
+    if constexpr (K::kCinSlots > 0) {
+      for (int j = 0; j < 4 * K::kCinSlots; ++j)
+        mbar_init(Kernel<K>::bar_cin(base, j / K::kCinSlots, j % K::kCinSlots), 1);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
     // Programmatic dependent launch: everything above touches no global

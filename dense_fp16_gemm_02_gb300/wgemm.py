@@ -224,13 +224,15 @@ def wgemm_f16f32_splitk_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, 
 
 
 def wgemm_select(M: int, N: int, K: int, lda: int | None = None, ldb: int | None = None,
-                 c_type: int = WGEMM_F32, fused: bool = False) -> tuple[int, int, int]:
+                 c_type: int = WGEMM_F32, fused: int = 0) -> tuple[int, int, int]:
     """(configuration id, mode, splits) that the library runs for this shape,
-    these row pitches (K when omitted), this C type and epilogue."""
+    these row pitches (K when omitted), this C type and epilogue: fused 0
+    (plain), 1 (alpha/beta/bias) or 2 (in place with beta = 1, fp32 D; a
+    bool True counts as 1)."""
     lda = K if lda is None else lda
     ldb = K if ldb is None else ldb
     c, m, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    rc = load().wgemm_select(M, N, K, lda, ldb, c_type, 1 if fused else 0, ctypes.byref(c),
+    rc = load().wgemm_select(M, N, K, lda, ldb, c_type, int(fused), ctypes.byref(c),
                              ctypes.byref(m), ctypes.byref(s))
     if rc != WGEMM_OK:
         raise WgemmError(rc, "wgemm_select")

@@ -148,12 +148,18 @@ int wgemm_gemm_config(const void* A, const void* B, void* C, int ab_type, int c_
  *   alpha, beta: finite fp32 scalars (WGEMM_ERR_INVALID_ARG otherwise).
  * A, B, types and alignment as wgemm_gemm. K == 0 gives D = beta·Cin + bias.
  * alpha = 1, beta = 0 and bias = NULL is exactly wgemm_gemm (any kernel);
- * otherwise the call runs one of the fused configurations (names ending in
- * "_ab", or "_ab_h" for a 16-bit D), data parallel; each epilogue warp
- * prefetches its blocks of Cin with TMA while the unit's main loop runs.
+ * otherwise the call runs one of the fused configurations (names containing
+ * "_ab"), data parallel. In the register-store ones ("_direct_ab<F>") each
+ * epilogue warp prefetches its blocks of Cin with TMA while the unit's main
+ * loop runs. The in-place form D += alpha·A·Bᵀ + bias (Cin == D, ldcin == ldd,
+ * beta == 1, fp32 D) may also run the reduce-add ones ("_tma_ab1"): they
+ * add alpha·sum + bias (one fmaf) into D's old values with TMA reduce-adds
+ * in L2 and read no Cin, so D's element is rounded twice (the fmaf and the
+ * add), as in the general form.
  * wgemm_gemm_ex_config forces a fused configuration (config_id ≥ 0), or
- * chooses (-1); WGEMM_ERR_CONFIG for a configuration that is not fused or is
- * of the other D width.
+ * chooses (-1); WGEMM_ERR_CONFIG for a configuration that is not fused, is
+ * of the other D width, or is a reduce-add one for a call that is not of
+ * the in-place form.
  */
 int wgemm_gemm_ex(const void* A, const void* B, void* D, const void* Cin, const float* bias,
                   float alpha, float beta, int ab_type, int c_type,
@@ -201,7 +207,8 @@ int wgemm_set_pdl(int enable);
  * worker (cluster) tile; S ring stages; A TMEM accumulators; E the epilogue
  * (direct: stores from registers, tma: staged TMA stores); _clc tiles taken
  * by cluster launch control (else a static persistent schedule); _ab<F> the
- * fused alpha/beta/bias epilogue with an F-block Cin ring; _h a 16-bit C.
+ * fused alpha/beta/bias epilogue (direct: with an F-block Cin ring; tma_ab1:
+ * the in-place reduce-add form); _h a 16-bit C.
  * Split-K and stream-K run on the static, fp32, unfused "tma" configurations
  * without m2 or r2.
  */
@@ -211,7 +218,9 @@ const char* wgemm_config_name(int config_id);
 /*
  * The choice wgemm_f16f32 (c_type WGEMM_F32, fused 0), wgemm_gemm (any
  * c_type; the operand type does not enter) or wgemm_gemm_ex (fused 1: among
- * the fused configurations) makes for a shape and operand row pitches
+ * the fused configurations; fused 2: the in-place form with beta = 1 and
+ * fp32 D, which may also take the reduce-add ones) makes for a shape and
+ * operand row pitches
  * (lda, ldb, in elements) on the current device: for fp32 C, the measured
  * per-shape table if the shape is in it and both pitches are multiples of 16
  * elements (rows on 32-byte sectors, as the table was measured); else the
@@ -222,7 +231,8 @@ const char* wgemm_config_name(int config_id);
  * only when it predicts at least 20% less time than the best data-parallel
  * configuration. Writes the configuration id, mode and splits (any pointer
  * may be NULL). Returns WGEMM_OK, WGEMM_ERR_INVALID_ARG (negative size, a
- * pitch below K, an unknown c_type, fused not 0 or 1) or a device error.
+ * pitch below K, an unknown c_type, fused not 0, 1 or 2, fused 2 with a
+ * 16-bit c_type) or a device error.
  */
 int wgemm_select(int M, int N, int K, int lda, int ldb, int c_type, int fused, int* config_id,
                  int* mode, int* splits);

@@ -11,6 +11,10 @@ oracle's sum and its epilogue definition on the same seeded inputs:
   each), plus half a unit in the last place of a 16-bit D.
 Also: D computed in place over Cin, beta = 0 with no Cin, no bias, K = 0,
 many tiles per worker, and the argument checks of the fused entry point.
+The reduce-add configurations ("_tma_ab1") serve only the in-place form
+D += alpha·A·Bᵀ + bias (beta = 1, fp32 D): they add alpha·sum + bias into
+D's old values with TMA reduce-adds, two fp32 roundings as in the general
+form, so the same bounds hold.
 """
 import numpy as np
 import pytest
@@ -40,8 +44,14 @@ def ceil8(k):
 
 
 def fused_names(width):
-    names = [n for n in wgemm.config_names() if "_ab" in n]
+    """The Cin-ring fused configurations of one D width."""
+    names = [n for n in wgemm.config_names() if "_direct_ab" in n]
     return [n for n in names if n.endswith("_h") == (width == 16)]
+
+
+def reduce_names():
+    """The reduce-add fused configurations (in place, beta = 1, fp32 D)."""
+    return [n for n in wgemm.config_names() if "_tma_ab" in n]
 
 
 def upload(x: np.ndarray, ab: str) -> torch.Tensor:
@@ -211,3 +221,71 @@ def test_fused_argument_checks():
     assert wgemm.wgemm_f16f32_config(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), M, N, K, K, K,
                                      N, wgemm.config_id(fused_names(32)[0]), 0, 1, None) == -6
     assert wgemm.wgemm_check(None) == 0
+
+
+@pytest.mark.parametrize("idx", range(6))
+def test_every_reduce_config_in_place(idx):
+    names = reduce_names()
+    if idx >= len(names):
+        pytest.skip("fewer reduce-add configurations compiled")
+    M, N, K = 600, 1100, 300
+    for ab in ("f16", "bf16"):
+        for kind in ("int", "uniform"):
+            A, B = inputs.gemm_operands(M, N, K, seed=80 + idx, kind=kind, lda=ceil8(K),
+                                        ldb=ceil8(K), pad="nan", dtype=ab)
+            cin, bias, alpha, _ = epilogue_operands(M, N, kind, 81 + idx, "f32")
+            for b in (bias, None):
+                D = run_fused(A, B, K, ab, "f32", alpha, 1.0, cin, b, config=names[idx],
+                              in_place=True)
+                check(D, A, B, K, kind, "f32", alpha, 1.0, cin, b,
+                      f"{names[idx]} {ab} {kind} bias={b is not None}")
+
+
+@pytest.mark.parametrize("idx", range(6))
+def test_reduce_multi_round(idx):
+    # More tiles than workers, ragged edges: every tile is added exactly once.
+    names = reduce_names()
+    if idx >= len(names):
+        pytest.skip("fewer reduce-add configurations compiled")
+    M, N, K = 2600, 7000, 136
+    A, B = inputs.gemm_operands(M, N, K, seed=90 + idx, kind="int", lda=ceil8(K), ldb=ceil8(K))
+    cin, bias, alpha, _ = epilogue_operands(M, N, "int", 91 + idx, "f32")
+    D = run_fused(A, B, K, "f16", "f32", alpha, 1.0, cin, bias, config=names[idx], in_place=True)
+    check(D, A, B, K, "int", "f32", alpha, 1.0, cin, bias, f"{names[idx]} multi-round")
+
+
+def test_reduce_configs_only_in_place_with_unit_beta():
+    M, N, K = 256, 256, 64
+    dA = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    dB = torch.zeros((N, K), dtype=torch.float16, device="cuda")
+    D = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    other = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    F16, F32 = wgemm.WGEMM_F16, wgemm.WGEMM_F32
+    cid = wgemm.config_id(reduce_names()[0])
+    a = (dA.data_ptr(), dB.data_ptr(), D.data_ptr())
+    # beta != 1, Cin elsewhere, and no Cin: not the in-place form
+    assert wgemm.wgemm_gemm_ex_config(*a, D.data_ptr(), None, 1.0, 2.0, F16, F32, M, N, K, K, K,
+                                      N, N, cid, None) == -6
+    assert wgemm.wgemm_gemm_ex_config(*a, other.data_ptr(), None, 1.0, 1.0, F16, F32, M, N, K,
+                                      K, K, N, N, cid, None) == -6
+    assert wgemm.wgemm_gemm_ex_config(*a, None, None, 2.0, 0.0, F16, F32, M, N, K, K, K, N, N,
+                                      cid, None) == -6
+    # a 16-bit D
+    Dh = torch.zeros((M, N), dtype=torch.float16, device="cuda")
+    assert wgemm.wgemm_gemm_ex_config(dA.data_ptr(), dB.data_ptr(), Dh.data_ptr(),
+                                      Dh.data_ptr(), None, 1.0, 1.0, F16, wgemm.WGEMM_F16, M, N,
+                                      K, K, K, N, N, cid, None) == -6
+    # the in-place form runs
+    assert wgemm.wgemm_gemm_ex_config(*a, D.data_ptr(), None, 1.0, 1.0, F16, F32, M, N, K, K, K,
+                                      N, N, cid, None) == 0
+    assert wgemm.wgemm_check(None) == 0
+
+
+def test_in_place_default_choice():
+    M, N, K = 1000, 1500, 520
+    A, B = inputs.gemm_operands(M, N, K, seed=95, kind="int")
+    cin, bias, alpha, _ = epilogue_operands(M, N, "int", 96, "f32")
+    D = run_fused(A, B, K, "f16", "f32", alpha, 1.0, cin, bias, in_place=True)
+    check(D, A, B, K, "int", "f32", alpha, 1.0, cin, bias, "in place, default choice")
+    cid, mode, splits = wgemm.wgemm_select(M, N, K, c_type=wgemm.WGEMM_F32, fused=2)
+    assert wgemm.config_fused(cid) == 1 and mode == 0 and splits == 1
