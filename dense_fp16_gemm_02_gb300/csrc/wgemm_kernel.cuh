@@ -252,8 +252,11 @@ __device__ __forceinline__ uint16_t to_c16(uint32_t bits, bool bf16) {
               : __half_as_ushort(__float2half_rn(f));
 }
 
-__device__ __forceinline__ void record_error(DeviceStatus* st, int32_t code, int32_t site,
-                                             uint32_t parity) {
+// Out of line: it runs only when a wait has given up, and every bounded wait
+// site would otherwise carry its own copy (less code ahead of the first loads
+// measured faster on small shapes).
+static __device__ __noinline__ void record_error(DeviceStatus* st, int32_t code, int32_t site,
+                                                 uint32_t parity) {
   if (atomicCAS(&st->code, 0, code) == 0) {
     st->block = (int32_t)blockIdx.x;
     st->warp = (int32_t)(threadIdx.x / 32);
