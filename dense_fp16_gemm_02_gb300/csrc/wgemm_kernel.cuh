@@ -299,9 +299,10 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
 
 // Bounded wait used after an abort: waits for this CTA's own operations in
 // flight (copies, responses) to land before the CTA exits, ignoring the
-// abort flag; gives up after the same time limit.
-__device__ __forceinline__ bool wait_bar_final(uint32_t bar, uint32_t parity, DeviceStatus* st,
-                                               int32_t site) {
+// abort flag; gives up after the same time limit. Out of line: only abort
+// paths call it.
+static __device__ __noinline__ bool wait_bar_final(uint32_t bar, uint32_t parity,
+                                                   DeviceStatus* st, int32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t n = 1;; ++n) {
