@@ -50,6 +50,7 @@ WORKLOADS = {
 }
 WORKLOADS["all"] = (WORKLOADS["c1"] + WORKLOADS["sweep"] + WORKLOADS["large"]
                     + WORKLOADS["streamk"] + WORKLOADS["splitk"])
+MODE_NAMES = ["data-parallel", "split-K", "stream-K", "data-parallel + stream-K tail"]
 FLUSH_BYTES = 256 << 20  # > the 129 MB L2
 GATE_CYCLES = 400_000    # ≈ 0.2 ms of GPU spin ahead of each timed call
 FALLBACK_TFLOPS = 1900.0
@@ -386,7 +387,7 @@ def run_ours(args):
             "tflops": round(tf, 1), "tensor_frac": round(tf / peak_tflops, 4),
             "hbm_gbs": round(bytes_min / (med * 1e-6) / 1e9, 1),
             "hbm_frac": round(bytes_min / (med * 1e-6) / 1e9 / peak_hbm, 4),
-            "config": names[cfg], "mode": ["data-parallel", "split-K", "stream-K"][mode],
+            "config": names[cfg], "mode": MODE_NAMES[mode],
             "splits": splits})
         agg = by_config.setdefault(names[cfg], {"flops": 0.0, "ms": 0.0, "launches": 0,
                                                 "shape": (M, N, K), "shape_ms": 0.0})

@@ -465,6 +465,22 @@ int make_plan(const KernelEntry& e, int M, int N, int K, int mode, int splits, i
   } else if (mode == kStreamK) {
     p->total_iters = (int64_t)p->num_tiles * p->kblocks;
     p->workers = (int32_t)std::min<int64_t>(p->total_iters, max_w);
+  } else if (mode == kHybridK) {
+    // Whole waves of tiles data parallel; the partial last wave and the
+    // `splits` − 1 full waves before it by stream-K over all workers. Fewer
+    // tiles than workers leaves no whole wave: plain stream-K.
+    if (splits < 1) return WGEMM_ERR_CONFIG;
+    p->mode = kStreamK;
+    if (p->num_tiles < max_w) {
+      p->total_iters = (int64_t)p->num_tiles * p->kblocks;
+      p->workers = (int32_t)std::min<int64_t>(p->total_iters, max_w);
+    } else {
+      p->workers = max_w;
+      const int32_t waves = p->num_tiles / max_w;
+      const int32_t dp_waves = std::max(0, waves - (splits - 1));
+      p->dp_tiles = dp_waves * max_w;
+      p->total_iters = (int64_t)(p->num_tiles - p->dp_tiles) * p->kblocks;
+    }
   } else {
     return WGEMM_ERR_CONFIG;
   }
@@ -648,7 +664,7 @@ int wgemm_gemm_config(const void* A, const void* B, void* C, int ab_type, int c_
                       int K, int lda, int ldb, int ldc, int config_id, int mode, int splits,
                       wgemm_stream_t stream) {
   if (config_id < 0 || config_id >= (int)registry().entries.size()) return WGEMM_ERR_CONFIG;
-  if (mode < -1 || mode > 2) return WGEMM_ERR_CONFIG;
+  if (mode < -1 || mode > kHybridK) return WGEMM_ERR_CONFIG;
   return run(A, B, C, ab_type, c_type, M, N, K, lda, ldb, ldc, config_id, mode, splits,
              reinterpret_cast<cudaStream_t>(stream));
 }

@@ -4,7 +4,7 @@
 // units, and the host tests check that the units cover every (tile, k-block)
 // exactly once.
 //
-// Three modes, following "SASS-Level Kernel Generation for Blackwell"
+// Three modes (and a mix of two), following "SASS-Level Kernel Generation for Blackwell"
 // (sections "The numbers" and "Inside the kernels", paragraph "Stream-K and
 // split-K, added in the L2"):
 //  * data parallel: one unit per output tile, tiles taken by stride in
@@ -17,7 +17,13 @@
 //    tile's first k-block stores it and raises the tile's flag, the others add
 //    to it once the flag is up. A worker walks its range from the end, so its
 //    first unit is the one that owns a tile start: no owner waits behind a
-//    unit that waits.
+//    unit that waits;
+//  * data-parallel waves with a stream-K tail: the leading `dp_tiles` tiles
+//    (whole waves, one tile per worker per wave) run data parallel, and the
+//    tiles left over are shared out by stream-K over the same workers, after
+//    their data-parallel units. The pages' stream-K spreads all tiles; this
+//    mix splits only the partial last wave (or the last few waves), so that
+//    the reduce-adds stay few when tiles outnumber workers.
 #pragma once
 #include <stdint.h>
 
@@ -29,7 +35,8 @@
 
 namespace wg {
 
-enum PlanMode : int32_t { kDataParallel = 0, kSplitK = 1, kStreamK = 2 };
+// kHybridK is a host-side request: its plan runs as kStreamK with dp_tiles > 0.
+enum PlanMode : int32_t { kDataParallel = 0, kSplitK = 1, kStreamK = 2, kHybridK = 3 };
 
 // What the epilogue does with a unit's accumulator.
 enum UnitKind : int32_t {
@@ -50,7 +57,8 @@ struct Plan {
   int32_t group;        // raster group (tile rows per group)
   int32_t workers;      // persistent workers in the grid (clusters launched, with CLC)
   int32_t sched;        // 0: static stride; 1: cluster launch control (tiles taken at run time)
-  int64_t total_iters;  // stream-K: num_tiles · kblocks
+  int32_t dp_tiles;     // stream-K: leading tiles run data parallel (a multiple of workers)
+  int64_t total_iters;  // stream-K: (num_tiles − dp_tiles) · kblocks
 };
 
 struct Unit {
@@ -97,6 +105,13 @@ WG_PLAN_HD bool plan_unit(const Plan& p, int32_t w, int32_t i, Unit& u) {
     return true;
   }
   if (p.mode == kStreamK) {
+    // Data-parallel waves first: worker w's tiles w, w + P, … below dp_tiles.
+    const int32_t dp_waves = p.dp_tiles / p.workers;
+    if (i < dp_waves) {
+      plan_tile_unit(p, w + i * p.workers, u);
+      return true;
+    }
+    i -= dp_waves;
     const int64_t T = p.total_iters, P = p.workers;
     const int64_t b = (T * w) / P, e = (T * (w + 1)) / P;
     if (e <= b) return false;
@@ -105,7 +120,7 @@ WG_PLAN_HD bool plan_unit(const Plan& p, int32_t w, int32_t i, Unit& u) {
     if (t < 0 || (t + 1) * kb <= b) return false;
     const int64_t s0 = t * kb > b ? t * kb : b;
     const int64_t s1 = (t + 1) * kb < e ? (t + 1) * kb : e;
-    u.tile = (int32_t)t;
+    u.tile = p.dp_tiles + (int32_t)t;
     plan_tile_coords(p, u.tile, u.tm, u.tn);
     u.kb_begin = (int32_t)(s0 - t * kb);
     u.kb_end = (int32_t)(s1 - t * kb);

@@ -169,6 +169,8 @@ def _waves(config: str, M: int, N: int, grid: int, mode: str, splits: int) -> st
         tiles *= splits
     elif mode == "stream-K":
         return "1 (stream)"
+    elif mode == "data-parallel + stream-K tail":
+        return f"{tiles / workers:.2f} (stream-K tail)"
     return f"{tiles / workers:.2f}"
 
 

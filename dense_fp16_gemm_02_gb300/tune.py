@@ -55,6 +55,11 @@ def candidates(M, N, K, names, workers_pair, workers_single):
             continue
         if tiles < 2 * workers:
             out.append((cid, 2, 1))
+        if tiles >= workers and tiles % workers:
+            # whole waves data parallel, the partial wave (and one more) by stream-K
+            out.append((cid, 3, 1))
+            if tiles >= 2 * workers:
+                out.append((cid, 3, 2))
         if tiles * 2 <= workers:
             for s in sorted({2, 3, 4, 6, 8, 9, 12, 16, workers // max(1, tiles)}):
                 if 2 <= s <= kb // 4 and tiles * s <= workers:
@@ -223,7 +228,8 @@ def emit(json_paths, inc_path=TUNED_INC):
     lines = [
         "// Measured per-shape winners (generated by dense_fp16_gemm_02_gb300/tune.py from",
         f"// {boxes} on {d.get('gpu', 'a GB300')} with {d.get('sm_count')} SMs; do not edit by hand).",
-        "// {M, N, K, configuration name, mode (0 data parallel, 1 split-K, 2 stream-K),",
+        "// {M, N, K, configuration name, mode (0 data parallel, 1 split-K, 2 stream-K,",
+        "//  3 data-parallel waves + stream-K tail),",
         "//  splits, measured µs per call (mean over the sweeps)}",
     ]
     chosen = combine(sweeps)

@@ -23,6 +23,9 @@ STATUS_NAMES = {
     -7: "WGEMM_ERR_WORKSPACE", -8: "WGEMM_ERR_NOALLOC_TOO_LARGE",
 }
 MODE_DATA_PARALLEL, MODE_SPLIT_K, MODE_STREAM_K = 0, 1, 2
+# Whole waves of tiles data parallel, the rest (partial last wave and `splits` − 1
+# full waves before it) by stream-K.
+MODE_HYBRID = 3
 WGEMM_F32, WGEMM_F16, WGEMM_BF16 = 0, 1, 2
 
 

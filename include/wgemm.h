@@ -92,8 +92,10 @@ int wgemm_f16f32(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
  * As wgemm_f16f32, but with the kernel configuration `config_id`
  * (0 ≤ config_id < wgemm_num_configs()) and the K-decomposition forced:
  * mode 0 = data parallel, 1 = split-K into `splits` ways (splits ≥ 1),
- * 2 = stream-K, -1 = what the configuration table picks. Used by the tests
- * and the per-shape sweep. WGEMM_ERR_CONFIG if the combination cannot run.
+ * 2 = stream-K, 3 = whole waves of tiles data parallel and the rest (the
+ * partial last wave and `splits` − 1 full waves before it, splits ≥ 1) by
+ * stream-K, -1 = what the configuration table picks. Used by the tests and
+ * the per-shape sweep. WGEMM_ERR_CONFIG if the combination cannot run.
  */
 int wgemm_f16f32_config(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
                         int M, int N, int K, int lda, int ldb, int ldc,

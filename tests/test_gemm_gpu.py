@@ -25,7 +25,7 @@ from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
 pytestmark = pytest.mark.gpu
 
 RTOL, ATOL = 2e-3, 1e-6
-DP, SPLIT, STREAM = 0, 1, 2
+DP, SPLIT, STREAM, HYBRID = 0, 1, 2, 3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -152,13 +152,29 @@ def test_stream_k_every_tma_config():
             check_full(A, B, K, kind, f"{name} stream-K {kind}", config=name, mode=STREAM)
 
 
+@pytest.mark.parametrize("held", [1, 2])
+def test_hybrid_every_tma_config(held):
+    # Whole waves of tiles data parallel and the rest by stream-K: more tiles
+    # than workers for the pair 256-wide tiles (11 × 12 = 132 over 76 pairs)
+    # and the single-CTA ones (21 × 12 over 152); ragged edges, K not a
+    # multiple of 64. Fewer tiles than workers (the 512-wide pair tiles) runs
+    # plain stream-K. Twice, to cross the flag epochs.
+    M, N, K = 2600, 3000, 700
+    for kind in ("int", "uniform"):
+        A, B = operands(M, N, K, 31 + held, kind)
+        for name in k_split_configs():
+            for _ in range(2):
+                check_full(A, B, K, kind, f"{name} hybrid {held} {kind}", config=name,
+                           mode=HYBRID, splits=held)
+
+
 def test_split_and_stream_equal_data_parallel_on_integers():
     # Exact arithmetic: every decomposition of K gives the same C, bit for bit.
     M, N, K = 256, 512, 4096
     A, B = inputs.gemm_operands(M, N, K, seed=5, kind="int")
     name = "g2_512x256_s4_a1_tma"
     base = run(A, B, K, config=name, mode=DP).cpu().numpy()
-    for mode, s in ((SPLIT, 2), (SPLIT, 9), (STREAM, 1)):
+    for mode, s in ((SPLIT, 2), (SPLIT, 9), (STREAM, 1), (HYBRID, 1)):
         other = run(A, B, K, config=name, mode=mode, splits=s).cpu().numpy()
         assert np.array_equal(base, other), (mode, s)
 

@@ -17,7 +17,7 @@ import pytest
 from dense_fp16_gemm_02_gb300 import build, wgemm
 
 KIND_STORE, KIND_RAISE, KIND_ADD_OWNER, KIND_ADD_ZERO = 0, 1, 2, 3
-DP, SPLIT, STREAM = 0, 1, 2
+DP, SPLIT, STREAM, HYBRID = 0, 1, 2, 3
 
 
 @pytest.fixture(scope="module")
@@ -184,6 +184,67 @@ def test_stream_k_protocol_finishes(lib, M, N, K, workers):
         assert simulate_stream_k(lists)
 
 
+def hybrid_lists(units, workers, dp_waves, tail_tiles, kb):
+    """Per-worker unit lists of a data-parallel + stream-K-tail plan, cut from
+    the worker-major listing by the plan's definition: dp_waves whole tiles
+    per worker, then one unit per tail tile that the worker's near-equal range
+    [⌊T·w/P⌋, ⌊T·(w+1)/P⌋) of the T = tail_tiles·kb tail iterations touches."""
+    T, lists, pos = tail_tiles * kb, [], 0
+    for w in range(workers):
+        b, e = T * w // workers, T * (w + 1) // workers
+        n_tail = 0 if e <= b else (e - 1) // kb - b // kb + 1
+        lists.append(units[pos:pos + dp_waves + n_tail])
+        pos += dp_waves + n_tail
+    assert pos == len(units)
+    return lists
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (8192, 2048, 4096), (4096, 4096, 1024),
+                                   (2600, 3000, 700), (257, 513, 4097), (300, 520, 200)])
+@pytest.mark.parametrize("workers", [3, 74, 76, 152])
+@pytest.mark.parametrize("held", [1, 2, 5])
+def test_hybrid_waves_and_stream_k_tail(lib, M, N, K, workers, held):
+    # Whole waves of tiles run data parallel, one tile per worker per wave in
+    # tile order; the partial last wave (and held − 1 full waves before it)
+    # goes to stream-K. Every (tile, k-block) once, one owner per tail tile,
+    # and the flag protocol finishes.
+    for cfg in tma_configs(lib):
+        units, tr, tc = plan(lib, M, N, K, cfg, HYBRID, held, workers)
+        tm, tn = tile_grid(M, N, tr, tc)
+        tiles, kb = tm * tn, -(-K // 64)
+        hits = coverage(units, tm, tn, kb)
+        assert len(hits) == tiles * kb and set(hits.values()) == {1}
+        if tiles < workers:
+            continue  # no whole wave: plain stream-K, covered above
+        dp_waves = max(0, tiles // workers - (held - 1))
+        dp_tiles = dp_waves * workers
+        lists = hybrid_lists(units, workers, dp_waves, tiles - dp_tiles, kb)
+        for w, lst in enumerate(lists):
+            for i in range(dp_waves):
+                u = lst[i]
+                assert u[0] == w + i * workers and u[3] == 0 and u[4] == kb
+                assert u[5] == KIND_STORE
+            tail = lst[dp_waves:]
+            assert all(u[0] >= dp_tiles for u in tail)
+            # The tail walks its range downwards: an owner unit comes first.
+            assert all(u[5] != KIND_RAISE for u in tail[1:])
+            assert len(tail) == 0 or tail[0][5] != KIND_ADD_OWNER or len(tail) == 1
+        starts = defaultdict(int)
+        for u in units:
+            if u[3] == 0:
+                starts[int(u[0])] += 1
+        assert len(starts) == tiles and set(starts.values()) == {1}
+        assert simulate_stream_k(lists)
+
+
+def test_hybrid_rejects_bad_arguments(lib):
+    cfg = tma_configs(lib)[0]
+    assert lib.wgemm_debug_plan(4096, 4096, 4096, cfg, HYBRID, 0, 76, None, 0, None, None) == -6
+    for c in direct_configs(lib) + multicast_configs(lib):
+        assert lib.wgemm_debug_plan(4096, 4096, 4096, c, HYBRID, 1, 76, None, 0, None,
+                                    None) == -6
+
+
 @pytest.mark.parametrize("M,N,K,S", [(1024, 1024, 65536, 9), (300, 520, 200, 3),
                                      (257, 513, 4097, 5)])
 def test_split_k_zero_slices_partition_rows(lib, M, N, K, S):
@@ -218,6 +279,6 @@ def test_16bit_output_and_fused_configs_are_data_parallel_only(lib):
         if not name.endswith("_h") and "_ab" not in name:
             continue
         assert lib.wgemm_debug_plan(1024, 1024, 4096, cfg, DP, 1, 76, None, 0, None, None) > 0
-        for mode, sp in ((SPLIT, 4), (STREAM, 1)):
+        for mode, sp in ((SPLIT, 4), (STREAM, 1), (HYBRID, 1)):
             assert lib.wgemm_debug_plan(1024, 1024, 4096, cfg, mode, sp, 76, None, 0, None,
                                         None) == -6
