@@ -180,7 +180,7 @@ def test_pdl_switch(lib):
     assert lib.wgemm_set_pdl(prev) == 0
 
 
-@pytest.mark.parametrize("name", ["tensor_peak", "mma_interference"])
+@pytest.mark.parametrize("name", ["tensor_peak", "mma_interference", "l2_reduce"])
 def test_peak_microbenchmarks_compile(name):
     """The tensor-pipe microbenchmarks (peak/*.cu) build for sm_103a."""
     from dense_fp16_gemm_02_gb300 import peak
