@@ -333,6 +333,7 @@ double predict_us(const KernelEntry& e, int M, int N, int K, bool aligned, int m
     // after the other (measured ≈6 µs on GB300).
     return t0 + 6.0 + a + b * (double)per_worker;
   }
+  if (mode != kDataParallel) return -1.0;  // the waves + stream-K tail mix is not modelled
   const int64_t waves = (tiles + workers - 1) / workers;
   return t0 + waves * (a + b * (double)kblocks);
 }

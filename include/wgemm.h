@@ -346,7 +346,8 @@ int wgemm_debug_trace_build(void);
  * error). wgemm_debug_predict_us: the time the rule predicts for a shape,
  * configuration and K-decomposition with `workers` workers and operand row
  * pitches lda, ldb, from the measured per-configuration rates compiled into
- * the library (-1 if the configuration has none or an argument is invalid).
+ * the library (-1 if the configuration has none, the mode is not modelled
+ * (3, the data-parallel + stream-K tail mix) or an argument is invalid).
  * Host arithmetic only.
  */
 int wgemm_debug_max_workers(int config_id);

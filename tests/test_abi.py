@@ -130,6 +130,9 @@ def test_rule_predictions_from_measured_rates(lib):
         assert p(4096, 4096, 2048, ld=1024) == -1.0, name  # pitch below K
     assert lib.wgemm_debug_predict_us(64, 64, 64, 64, 64, n, 0, 1, 76) == -1.0
     assert lib.wgemm_debug_predict_us(64, 64, 64, 64, 64, -1, 0, 1, 76) == -1.0
+    # The waves + stream-K tail mix is not modelled.
+    cid = wgemm.config_id("g2_256x256_s6_a2_tma")
+    assert lib.wgemm_debug_predict_us(4096, 4096, 4096, 4096, 4096, cid, 3, 1, 76) == -1.0
 
 
 def test_rule_charges_rows_off_sectors(lib):
