@@ -12,7 +12,13 @@
 //                block order (a tile's nine split-K units)
 //   add_rot9     as add_shared9, each of the nine starting at a different
 //                block (rotated by its index in the group)
+//   red_v4       no bulk copies: warps 1–3 add their blocks from registers
+//                with red.global.add.v4.f32 (16 bytes per lane), every CTA
+//                into its own region
+//   add_mixed    both paths at once: lane 0 of warp 0 bulk-adds the blocks
+//                b ≡ 0 (mod 4), warps 1–3 red-add the others from registers
 //
+// In red_v4 and add_mixed the block size is 4 KB and `issuers` is ignored.
 // Each CTA covers its region `passes` times; its issuing warps take its
 // blocks in turn. Usage: l2_reduce [passes] [block bytes] [issuing warps]
 // [CTAs] (default: every SM, in whole groups of nine).
@@ -38,8 +44,32 @@ constexpr int kSrcBytes = 64 * 1024;      // shared-memory source
 constexpr int kGroup = 9;                 // CTAs adding into one region
 constexpr float kValue = 1.0f;
 
-enum Mode { kStore, kAdd, kAddShared9, kAddRot9, kModes };
-const char* const kModeNames[kModes] = {"store", "add", "add_shared9", "add_rot9"};
+enum Mode { kStore, kAdd, kAddShared9, kAddRot9, kRedV4, kAddMixed, kModes };
+const char* const kModeNames[kModes] = {"store",    "add",    "add_shared9",
+                                        "add_rot9", "red_v4", "add_mixed"};
+
+// Warps 1–3 add 4 KB blocks of the value from registers: every lane adds 16
+// bytes per instruction, a warp covers a block in 8 instructions. With `all`
+// set, block b goes to warp 1 + b mod 3; otherwise blocks b ≡ w (mod 4) go
+// to warp w and the blocks b ≡ 0 are left to the bulk path.
+__device__ void red_blocks(unsigned char* base, int passes, int warp, bool all) {
+  const int lane = (int)threadIdx.x % 32;
+  constexpr int kBlk = 4096, kBlocksR = kRegionBytes / kBlk;
+  for (int p = 0; p < passes; ++p) {
+    for (int b = 0; b < kBlocksR; ++b) {
+      const int owner = all ? 1 + b % 3 : b % 4;
+      if (owner != warp) continue;
+      float* blk = reinterpret_cast<float*>(base + (size_t)b * kBlk);
+#pragma unroll
+      for (int i = 0; i < kBlk / 512; ++i) {
+        float* d = blk + (i * 32 + lane) * 4;
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                     :: "l"(__cvta_generic_to_global(d)), "f"(kValue), "f"(kValue),
+                        "f"(kValue), "f"(kValue) : "memory");
+      }
+    }
+  }
+}
 
 #define CHECK(x)                                                                   \
   do {                                                                             \
@@ -63,6 +93,27 @@ __global__ void __launch_bounds__(128) bulk_kernel(float* dst, int mode, int pas
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
   const int warp = (int)threadIdx.x / 32;
+  if (mode == kRedV4 || mode == kAddMixed) {
+    unsigned char* own = reinterpret_cast<unsigned char*>(dst) + (size_t)blockIdx.x * kRegionBytes;
+    if (warp >= 1) {
+      red_blocks(own, passes, warp, mode == kRedV4);
+      return;
+    }
+    if (mode == kRedV4 || threadIdx.x != 0) return;
+    // Lane 0 of warp 0: bulk reduce-adds of the blocks b ≡ 0 (mod 4).
+    for (int p = 0; p < passes; ++p) {
+      for (int b = 0; b < kRegionBytes / 4096; b += 4) {
+        const uint32_t s = smem_addr(smem + (b % (kSrcBytes / 4096)) * 4096);
+        const size_t d = __cvta_generic_to_global(own + (size_t)b * 4096);
+        asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
+                     :: "l"(d), "r"(s), "r"(4096) : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 15;" ::: "memory");
+      }
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    return;
+  }
   if (threadIdx.x % 32 != 0 || warp >= issuers) return;
   const int blocks = kRegionBytes / block_bytes;
   const int src_blocks = kSrcBytes / block_bytes;
@@ -134,7 +185,7 @@ int main(int argc, char** argv) {
         const int regions = shared9 ? grid / kGroup : grid;
         const float want = mode == kStore ? kValue
                            : shared9     ? kValue * (float)(kGroup * passes)
-                                         : kValue * (float)passes;
+                                         : kValue * (float)passes;  // every block once per pass
         for (size_t i = 0; i < (size_t)regions * kRegionBytes / 4; ++i)
           if (host[i] != want) {
             ok = false;

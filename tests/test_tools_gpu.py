@@ -41,7 +41,8 @@ def test_l2_reduce_microbenchmark_moves_the_bytes():
     r = subprocess.run([exe, "1"], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     rows = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
-    assert [x["mode"] for x in rows] == ["store", "add", "add_shared9", "add_rot9"]
+    assert [x["mode"] for x in rows] == ["store", "add", "add_shared9", "add_rot9", "red_v4",
+                                         "add_mixed"]
     # Every mode leaves C holding the expected values (stores, or the sums of
     # the adds), so the timed kernels did the work they report.
     assert all(x["result_ok"] for x in rows)
