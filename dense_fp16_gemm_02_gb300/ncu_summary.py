@@ -5,12 +5,15 @@ of the eleven shapes.
     python -m dense_fp16_gemm_02_gb300.ncu_summary dram DRAM_CSV
     python -m dense_fp16_gemm_02_gb300.ncu_summary roofline ROOFLINE_CSV BENCH_JSON
     python -m dense_fp16_gemm_02_gb300.ncu_summary launches LAUNCHES_CSV
+    python -m dense_fp16_gemm_02_gb300.ncu_summary warm WARM_CSV COMPARE_JSONL
 
 DRAM_CSV is the `--csv --log-file` output of the dram command in
 profiles/dram_sweep.md; ROOFLINE_CSV and BENCH_JSON are those of
 profiles/roofline_all_shapes.md; LAUNCHES_CSV that of
 profiles/launches_sweep.md (every launch with gpu__time_duration.sum). The files under profiles/ are rewritten
 (their prose is kept; the tables and the kernel-source digest are replaced).
+`warm` prints the table of profiles/warm_l2_kernel_times.md from the launch
+list of `compare --warm` and that command's output.
 """
 from __future__ import annotations
 
@@ -19,6 +22,7 @@ import io
 import json
 import os
 import re
+import statistics
 import sys
 from collections import OrderedDict
 
@@ -150,6 +154,50 @@ def launches(csv_path: str) -> None:
     print("\n".join(rows))
 
 
+def warm(csv_path: str, compare_jsonl: str) -> None:
+    """Kernel-only times of `compare --warm` from its ncu launch list (taken
+    with --cache-control none): per shape, the library's launches come first
+    and cuBLAS's after them; a cuBLAS call may launch several kernels, whose
+    times are summed per call. Medians of the timed calls (the warm-up calls
+    dropped). Prints the table rows."""
+    with open(compare_jsonl) as f:
+        lines = [json.loads(l) for l in f if l.startswith("{")]
+    shapes = [d for d in lines if "shape" in d]
+    rounds = [d for d in lines if "summary" in d][0]["summary"]["rounds"]
+    calls = 3 + rounds
+    by = list(read_ncu_csv(csv_path).values())
+    # Runs of consecutive launches, library (wgemm) or not; skip what comes
+    # before the first library launch (the start-up probe).
+    runs = []
+    for v in by:
+        ours = "wgemm_kernel" in v["kernel"]
+        if not runs and not ours:
+            continue
+        if runs and runs[-1][0] == ours:
+            runs[-1][1].append(v["gpu__time_duration.sum"] / 1000.0)
+        else:
+            runs.append((ours, [v["gpu__time_duration.sum"] / 1000.0]))
+    if len(runs) != 2 * len(shapes):
+        raise SystemExit(f"{len(runs)} launch runs for {len(shapes)} shapes")
+    out = []
+    for i, d in enumerate(shapes):
+        M, N, K = (int(x) for x in d["shape"].split("x"))
+        (o1, t_ours), (o2, t_ref) = runs[2 * i], runs[2 * i + 1]
+        if not (o1 and not o2) or len(t_ours) != calls or len(t_ref) % calls:
+            raise SystemExit(f"{d['shape']}: {len(t_ours)} and {len(t_ref)} launches")
+        k = len(t_ref) // calls
+        ref_calls = [sum(t_ref[j * k:(j + 1) * k]) for j in range(calls)]
+        us_o = statistics.median(t_ours[3:])
+        us_r = statistics.median(ref_calls[3:])
+        fl = 2.0 * M * N * K
+        out.append(f"| {M}×{N}×{K} | {us_o:.2f} | {us_r:.2f} | {us_r / us_o:.3f} | "
+                   f"{fl / us_o / 1e6:.1f} | {k} | {d['ours_us']:.2f} | {d['cublas_us']:.2f} |")
+    print("| M×N×K | wgemm kernel µs | cuBLAS kernel µs (per call) | cuBLAS ÷ wgemm | "
+          "wgemm TFLOP/s | cuBLAS kernels per call | wgemm event µs | cuBLAS event µs |")
+    print("|---|---|---|---|---|---|---|---|")
+    print("\n".join(out))
+
+
 def _waves(config: str, M: int, N: int, grid: int, mode: str, splits: int) -> str:
     """Worker tiles (units, for split-K) per co-resident worker: the number
     of waves of the launch, from the configuration's tile and cluster."""
@@ -217,6 +265,8 @@ def main(argv=None) -> int:
         roofline(argv[1], argv[2])
     elif len(argv) >= 2 and argv[0] == "launches":
         launches(argv[1])
+    elif len(argv) >= 3 and argv[0] == "warm":
+        warm(argv[1], argv[2])
     else:
         print(__doc__)
         return 2

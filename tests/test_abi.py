@@ -215,3 +215,39 @@ def test_ncu_summary_maps_every_configuration_to_its_template_arguments(tmp_path
     p.write_text("==PROF== preamble\n" + csv_text)
     by = ncu_summary.read_ncu_csv(str(p))
     assert by["0"]["gpu__time_duration.sum"] == 13312.0 and by["0"]["kernel"] == kernel
+
+
+def test_ncu_summary_warm_groups_launches_by_arm_and_call(tmp_path, capsys):
+    # compare --warm runs, per shape, the library's calls and then cuBLAS's;
+    # a cuBLAS call may launch several kernels, summed per call; the first
+    # three calls of each arm are warm-up. A start-up probe before the first
+    # library launch is skipped.
+    from dense_fp16_gemm_02_gb300 import ncu_summary
+    head = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+            '"Block Size","Grid Size","Device","CC","Metric Name","Metric Unit","Metric Value"')
+    rows, n = [], 0
+
+    def add(kernel, us):
+        nonlocal n
+        rows.append(f'"{n}","1","python","h","{kernel}","1","7","(256, 1, 1)","(1, 1, 1)",'
+                    f'"0","10.3","gpu__time_duration.sum","ns","{int(us * 1000)}"')
+        n += 1
+
+    add("nvjet_probe", 50.0)
+    for s in range(2):
+        for c in range(5):  # 3 warm-up + 2 timed library calls
+            add("void wg::wgemm_kernel<wg::Cfg<1>>(wg::KParams)", 100.0 if c < 3 else 10.0 + s)
+        for c in range(5):  # cuBLAS: two kernels per call
+            add("nvjet_main", 100.0 if c < 3 else 5.0 + s)
+            add("nvjet_reduce", 1.0)
+    (tmp_path / "w.csv").write_text(head + "\n" + "\n".join(rows) + "\n")
+    (tmp_path / "c.jsonl").write_text(
+        '{"shape": "64x64x64", "ours_us": 12.0, "cublas_us": 9.0}\n'
+        '{"shape": "128x64x64", "ours_us": 13.0, "cublas_us": 10.0}\n'
+        '{"summary": {"rounds": 2}}\n')
+    ncu_summary.warm(str(tmp_path / "w.csv"), str(tmp_path / "c.jsonl"))
+    out = [l for l in capsys.readouterr().out.splitlines() if l.startswith("| 6") or
+           l.startswith("| 1")]
+    assert out[0].startswith("| 64×64×64 | 10.00 | 6.00 | 0.600 |")
+    assert out[1].startswith("| 128×64×64 | 11.00 | 7.00 | 0.636 |")
+    assert "| 2 |" in out[0]
