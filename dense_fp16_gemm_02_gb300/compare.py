@@ -14,8 +14,9 @@ Prints one JSON line per shape (medians, TFLOP/s of both, and the ratio)
 and one summary line. The same checks as the bench guard the comparison:
 both arms' results on the shape are compared on a sample of rows.
 
-With `--warm` the calls run the way the pages timed theirs: no L2 flush and
-no gate, each call followed by a device synchronisation, per shape first
+With `--warm` the calls run the way "SASS-Level Kernel Generation for
+Blackwell" (section "How we measured") timed its own: no L2 flush and no
+gate, each call followed by a device synchronisation, per shape first
 3 + `rounds` calls of the library and then 3 + `rounds` of cuBLAS, and no
 other kernel in between (the row check is skipped). Event times then
 include the launch; kernel-only times come from an ncu launch list of the
@@ -38,7 +39,7 @@ def main(argv=None) -> int:
     ap.add_argument("--workload", default="all")
     ap.add_argument("--rounds", type=int, default=20)
     ap.add_argument("--warm", action="store_true",
-                    help="warm L2, synchronised calls, arms in blocks (the pages' protocol)")
+                    help="warm L2, synchronised calls, arms in blocks")
     args = ap.parse_args(argv)
 
     import torch

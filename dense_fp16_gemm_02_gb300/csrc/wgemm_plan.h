@@ -21,7 +21,7 @@
 //  * data-parallel waves with a stream-K tail: the leading `dp_tiles` tiles
 //    (whole waves, one tile per worker per wave) run data parallel, and the
 //    tiles left over are shared out by stream-K over the same workers, after
-//    their data-parallel units. The pages' stream-K spreads all tiles; this
+//    their data-parallel units. The page's stream-K spreads all tiles; this
 //    mix splits only the partial last wave (or the last few waves), so that
 //    the reduce-adds stay few when tiles outnumber workers.
 #pragma once
