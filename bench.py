@@ -1,18 +1,28 @@
 """Benchmark of the dense GEMM C = A·Bᵀ (fp16 in, fp32 accumulate and out).
 
-One step = one call of each shape of the workload, each call timed alone with
-CUDA events on the launching stream, an L2 flush (a 256 MiB write) between
-calls, nothing overlapping ("SASS-Level Kernel Generation for Blackwell",
-section "How we measured": every call runs alone). Inputs are seeded
-synthetic uniform[-1, 1] fp16 matrices, resident in HBM before timing starts.
+One step = a pass over every shape of the workload. Each shape is called
+several times per step (more often for small shapes, as the pages time
+400 calls of a small shape and a dozen of the largest), every call timed
+alone with CUDA events on the launching stream, after an L2 flush (a
+256 MiB write) and a GPU-side gate, nothing overlapping ("SASS-Level Kernel
+Generation for Blackwell", section "How we measured": every call runs
+alone). Inputs are seeded synthetic uniform[-1, 1] fp16 matrices, resident
+in HBM before timing starts.
 
-Default workload: the square and near-square sweep (1536³, 2048³, 4096³,
-3072×1280×2048, 4096×4096×1024, 8192×2048×4096). Other workloads: c1
-(1024³), splitk (1024×1024×65536), streamk (2048×2048×16384), large (8192³,
-16384³), all.
+Default workload: all eleven shapes of the pages' table ("The numbers"):
+1024³, the square and near-square sweep (1536³, 2048³, 4096³,
+3072×1280×2048, 4096×4096×1024, 8192×2048×4096), 8192³, 16384³, the stream-K
+case 2048×2048×16384 and the split-K case 1024×1024×65536. Named subsets:
+c1, sweep, large, streamk, splitk.
 
-Prints one JSON line (rank 0). `value` = Σ 2·M·N·K over the step's calls ÷
-Σ their GPU times, in TFLOP/s, over all ranks (replicas for N > 1).
+After the timed steps, a second pass records every call's GPU kernel time
+with CUPTI (the pages' measure: kernel time, median over the calls), once
+with the L2 flushed before each call and once with a warm L2 and a device
+synchronisation after each call (the pages' protocol).
+
+Prints one JSON line. `value` = Σ 2·M·N·K over a step's calls ÷ the step's
+summed GPU event time, in TFLOP/s. One GPU only: the library's cluster
+kernels multicast TMA loads within a cluster, which stays a one-GPU feature.
 
 `--impl reference` times the CPU oracle (the plain fp64 triple loop) on the
 host cores, on a bounded row sample of the same shapes, in the same unit.
@@ -24,7 +34,6 @@ import hashlib
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -50,7 +59,26 @@ WORKLOADS = {
 }
 WORKLOADS["all"] = (WORKLOADS["c1"] + WORKLOADS["sweep"] + WORKLOADS["large"]
                     + WORKLOADS["streamk"] + WORKLOADS["splitk"])
-MODE_NAMES = ["data-parallel", "split-K", "stream-K", "data-parallel + stream-K tail"]
+MODE_NAMES = ["data-parallel", "split-K", "stream-K", "data-parallel + stream-K tail",
+              "owners + tail split"]
+
+
+def calls_per_step(M: int, N: int, K: int) -> int:
+    """Calls of a shape in one step: the pages time 400 calls of the small
+    shapes, 200 of the ~75 µs ones, 40 at 8192³ and 12 at 16384³ ("How we
+    measured"); a step holds three times a twentieth of that (so 20 steps
+    hold three times the pages' count), which keeps the timed region several
+    seconds long, for a clock record with many samples under load."""
+    flops = 2.0 * M * N * K
+    if flops >= 4e12:
+        return 2
+    if flops >= 5e11:
+        return 6
+    if flops >= 1e11:
+        return 30
+    return 60
+
+
 FLUSH_BYTES = 256 << 20  # > the 129 MB L2
 GATE_CYCLES = 400_000    # ≈ 0.2 ms of GPU spin ahead of each timed call
 FALLBACK_TFLOPS = 1900.0
@@ -62,24 +90,35 @@ def shape_name(s):
     return "x".join(str(v) for v in s)
 
 
-def peaks(power_capped: bool = False):
-    """(tensor TFLOP/s, HBM GB/s, source). The tensor figure is the measured
-    cuBLAS bf16 rate (fp16 runs at the same nominal rate): the burst figure,
-    or the sustained one when the timed region ran under the power cap (a
-    long run of back-to-back large GEMMs), since that is the regime the
-    sustained figure was measured in."""
+def peaks():
+    """(tensor TFLOP/s burst, tensor TFLOP/s sustained, HBM GB/s, source). The
+    tensor figures are the measured cuBLAS bf16 rates (fp16 runs at the same
+    nominal rate). Every call is timed alone, so the burst figure is the
+    denominator; the sustained one (a seconds-long loop under the power cap)
+    is reported beside it."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        if power_capped and "bf16_tflops_sustained" in d:
-            return (float(d["bf16_tflops_sustained"]), float(d["hbm_gbs"]),
-                    "measured: bf16 cuBLAS sustained (timed region under sw_power_cap)")
-        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured: bf16 cuBLAS burst"
+        return (float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                float(d["hbm_gbs"]), "measured: bf16 cuBLAS burst")
     except (OSError, KeyError, ValueError):
-        if power_capped:
-            return FALLBACK_TFLOPS_SUSTAINED, FALLBACK_HBM_GBS, "fallback: sustained"
-        return FALLBACK_TFLOPS, FALLBACK_HBM_GBS, "fallback: burst"
+        return FALLBACK_TFLOPS, FALLBACK_TFLOPS_SUSTAINED, FALLBACK_HBM_GBS, "fallback: burst"
+
+
+def pipe_ceiling():
+    """(TFLOP/s, description) of the tensor pipe on its own: the largest rate
+    of the tcgen05.mma microbenchmark (dense_fp16_gemm_02_gb300/peak.py),
+    back-to-back MMAs on operands resident in shared memory, all SMs, from
+    the committed profiles/tensor_pipe_ceiling.json; None if absent."""
+    path = os.path.join(ROOT, "profiles", "tensor_pipe_ceiling.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        best = max(d["shapes"], key=lambda r: r["tflops"])
+        return float(best["tflops"]), f"tcgen05.mma microbenchmark, {best['mma']} (the largest)"
+    except (OSError, KeyError, ValueError):
+        return None, None
 
 
 KERNEL_SOURCES = ["wgemm_kernel.cuh", "wgemm_plan.h", "wgemm_configs.h", "inst_single.cu",
@@ -141,29 +180,23 @@ def committed_traffic(config_name: str, shape):
     return None
 
 
-def max_over_ranks(values, device=None):
-    """Element-wise maximum of a list of floats over all ranks (identity with
-    one process). Every rank's timed region is bracketed by barriers, so the
-    slowest rank's time is the job's time."""
-    import torch
-    import torch.distributed as dist
-    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
-        return [float(v) for v in values]
-    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return [float(v) for v in t.tolist()]
+def job_value(flops_per_step: float, step_ms: float) -> float:
+    """Throughput in TFLOP/s: a step's flops over the step's time."""
+    return flops_per_step / (step_ms * 1e-3) / 1e12
 
 
-def job_value(flops_per_rank_step: float, world: int, step_ms: float) -> float:
-    """Whole-job throughput in TFLOP/s: every rank's flops over the slowest time."""
-    return world * flops_per_rank_step / (step_ms * 1e-3) / 1e12
-
-
-def dist_setup(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return world, rank, local
+def workload_config(args, shapes):
+    """The workload description, the same for both arms."""
+    ab, c = TYPES[args.types]
+    return {
+        "workload": args.workload + ": " + ", ".join(shape_name(s) for s in shapes),
+        "inputs": (f"uniform[-1,1] rounded to {ab}" if args.values == "uniform" else
+                   "integers in {-2..2}") + ", seeded SplitMix64",
+        "accumulate": "f32", "output": c,
+        "epilogue": ("D = A·Bᵀ + D + bias (fused; C read back in place)"
+                     if args.epilogue == "fused" else "C = A·Bᵀ"),
+        "parallelism": "single GPU",
+    }
 
 
 _B_CACHE = {}
@@ -229,10 +262,18 @@ def oracle_sample_rate(shapes, seconds_total: float, nthreads: int = 0, ab: str 
     return total_flops / total_t / 1e12, threads, "; ".join(desc), work
 
 
+def single_gpu_only(args) -> str | None:
+    """The reason this run cannot go ahead, or None. The bench runs one GPU:
+    its cluster kernels multicast TMA loads within a cluster, which is kept to
+    one-GPU runs, and the path has no exchange step to measure."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != 1 or world != 1:
+        return (f"one GPU only (asked for --gpus {args.gpus}, WORLD_SIZE {world}): the GEMM "
+                "runs on one GPU and its cluster kernels multicast TMA loads within a cluster")
+    return None
+
+
 def run_reference(args):
-    world, rank, _ = dist_setup(args)
-    if rank != 0:
-        return 0
     shapes = WORKLOADS[args.workload]
     # About 150 s of oracle work over the whole run, however many steps.
     budget = max(0.02 * len(shapes), min(60.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -250,9 +291,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": tflop_per_step / value * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload + ": " + ", ".join(shape_name(s) for s in shapes),
-                   "types": args.types,
-                   "oracle": "plain fp64 triple loop in C (oracle/wgemm_oracle.c)",
+        "config": workload_config(args, shapes),
+        "timing": {"oracle": "plain fp64 triple loop in C (oracle/wgemm_oracle.c), host cores",
                    "sample": ("row sample per shape; each full call estimated as the "
                               "calibrated fixed cost (decoding B) plus the sample's "
                               "per-row time times M")},
@@ -265,21 +305,22 @@ def run_reference(args):
     return 0
 
 
+def _median(xs):
+    return float(statistics.median(xs)) if xs else None
+
+
 def run_ours(args):
     import numpy as np
     import torch
 
-    from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
+    from dense_fp16_gemm_02_gb300 import build, inputs, ktime, wgemm
 
-    world, rank, local = dist_setup(args)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
-    torch.cuda.set_device(local)
-    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
     build.build()
     wgemm.load()
     shapes = WORKLOADS[args.workload]
+    reps = [args.calls or calls_per_step(*s) for s in shapes]
     stream = torch.cuda.current_stream()
     h = stream.cuda_stream
     ab, c = TYPES[args.types]
@@ -322,19 +363,22 @@ def run_ours(args):
         if rc != 0:
             raise RuntimeError(f"wgemm call failed: {rc}")
 
+    # The calls of one step, in order: every shape `reps` times in a row.
+    order = [i for i in range(len(shapes)) for _ in range(reps[i])]
+
     def one_step(events):
-        for i in range(len(shapes)):
-            flush.fill_(float(i))  # evict L2
+        for j, i in enumerate(order):
+            flush.fill_(float(j))  # evict L2
             # Keep the GPU busy while the host enqueues the start event and the
             # call, so the event pair brackets the kernel, not host latency.
             torch.cuda._sleep(GATE_CYCLES)
-            e0, e1 = events[i]
+            e0, e1 = events[j]
             e0.record(stream)
             call(i)
             e1.record(stream)
 
     mk = lambda: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in shapes]
+                  for _ in order]
     for _ in range(args.warmup):
         one_step(mk())
     rc = wgemm.wgemm_check(h)
@@ -342,10 +386,8 @@ def run_ours(args):
         raise RuntimeError(f"device status {rc}: {wgemm.wgemm_last_device_error()}")
 
     per_step_events = [mk() for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(0) as clocks:
         clocks.mark_start()
         t_wall = time.perf_counter()
         for s in range(args.steps):
@@ -353,26 +395,69 @@ def run_ours(args):
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
         clocks.mark_stop()
-    if world > 1:
-        dist.barrier()
     rc = wgemm.wgemm_check(h)
     if rc != 0:
         raise RuntimeError(f"device status {rc}: {wgemm.wgemm_last_device_error()}")
-    gpu_launches = args.steps * len(shapes)
+    gpu_launches = args.steps * len(order)  # one GEMM kernel per call (K > 0)
 
     times = np.array([[e0.elapsed_time(e1) for (e0, e1) in ev] for ev in per_step_events])  # ms
     step_ms = float(np.median(times.sum(axis=1)))
     flops = np.array([2.0 * M * N * K for (M, N, K) in shapes])
-    step_ms = max_over_ranks([step_ms], dev)[0]
-    value = job_value(float(flops.sum()), world, step_ms)
+    flops_per_step = float(sum(flops[i] for i in order))
+    value = job_value(flops_per_step, step_ms)
     clk = clocks.summary()
-    peak_tflops, peak_hbm, peak_src = peaks("sw_power_cap" in clk["reasons"])
+    peak_tflops, peak_sustained, peak_hbm, peak_src = peaks()
+    ceiling, ceiling_src = pipe_ceiling()
+
+    # Kernel-only times from CUPTI, outside the timed region: per shape, calls
+    # after an L2 flush and the gate (as timed above), then the pages'
+    # protocol: a warm L2, each call followed by a device synchronisation, one
+    # untimed call first. Shapes go smallest first, so that the largest (which
+    # run into the power cap back to back) do not lower the clock of the rest.
+    ktimes, ktime_note = None, None
+    if not args.no_kernel_time:
+        try:
+            rec = ktime.KernelTimes()
+            n_k = max(5, min(20, args.steps))
+            kinds = []
+            torch.cuda.synchronize()
+            rec.start()
+            by_size = sorted(range(len(shapes)), key=lambda i: flops[i])
+            for i in by_size:
+                for r in range(n_k):
+                    flush.fill_(float(r))
+                    torch.cuda._sleep(GATE_CYCLES)
+                    call(i)
+                    kinds.append((i, "flushed"))
+                torch.cuda.synchronize()
+                for r in range(n_k + 1):
+                    call(i)
+                    torch.cuda.synchronize()
+                    kinds.append((i, "warm" if r > 0 else "skip"))
+            rec.stop()
+            recs = [r for r in rec.records() if "wgemm_" in r[0]]
+            if len(recs) != len(kinds):
+                raise ktime.KernelTimesUnavailable(
+                    f"{len(recs)} GEMM kernel records for {len(kinds)} calls "
+                    f"({rec.dropped()} dropped)")
+            ktimes = {}
+            for (i, kind), (_, t0, t1, _) in zip(kinds, recs):
+                ktimes.setdefault((i, kind), []).append((t1 - t0) * 1e-3)  # µs
+            ktime_note = (f"CUPTI CONCURRENT_KERNEL records; {n_k} calls per shape after an L2 "
+                          f"flush, and {n_k} with a warm L2 and a device synchronisation after "
+                          "each call (one untimed call first)")
+        except ktime.KernelTimesUnavailable as e:
+            ktimes, ktime_note = None, f"unavailable: {e}"
+    rc = wgemm.wgemm_check(h)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc}: {wgemm.wgemm_last_device_error()}")
 
     # Per-shape report, and the configuration each call ran.
     per_shape = []
     by_config = {}
     for i, (M, N, K) in enumerate(shapes):
-        us = times[:, i] * 1e3
+        cols = [j for j, x in enumerate(order) if x == i]
+        us = times[:, cols].ravel() * 1e3
         # The fused bench call is in place with beta = 1: with fp32 D it may
         # also take the reduce-add kernels (fused kind 2).
         fused_kind = 0 if args.epilogue != "fused" else (2 if c_type == wgemm.WGEMM_F32 else 1)
@@ -381,21 +466,35 @@ def run_ours(args):
         tf = flops[i] / (med * 1e-6) / 1e12
         c_rw = (2 if args.epilogue == "fused" else 1) * c_bytes * M * N  # C written (and read)
         bytes_min = 2.0 * (M * K + N * K) + c_rw
-        per_shape.append({
-            "shape": shape_name((M, N, K)), "us_median": round(med, 3),
+        row = {
+            "shape": shape_name((M, N, K)), "calls": int(us.size), "us_median": round(med, 3),
             "us_min": round(float(us.min()), 3), "us_max": round(float(us.max()), 3),
             "tflops": round(tf, 1), "tensor_frac": round(tf / peak_tflops, 4),
+            "pipe_frac": round(tf / ceiling, 4) if ceiling else None,
             "hbm_gbs": round(bytes_min / (med * 1e-6) / 1e9, 1),
             "hbm_frac": round(bytes_min / (med * 1e-6) / 1e9 / peak_hbm, 4),
-            "config": names[cfg], "mode": MODE_NAMES[mode],
-            "splits": splits})
+            "config": names[cfg], "mode": MODE_NAMES[mode], "splits": splits}
+        if ktimes is not None:
+            kf, kw = ktimes.get((i, "flushed"), []), ktimes.get((i, "warm"), [])
+            row.update({
+                "us_kernel_median": round(_median(kf), 3), "us_kernel_min": round(min(kf), 3),
+                "us_kernel_max": round(max(kf), 3),
+                "tflops_kernel": round(flops[i] / (_median(kf) * 1e-6) / 1e12, 1),
+                "us_kernel_warm_median": round(_median(kw), 3),
+                "tflops_kernel_warm": round(flops[i] / (_median(kw) * 1e-6) / 1e12, 1)})
+        per_shape.append(row)
         agg = by_config.setdefault(names[cfg], {"flops": 0.0, "ms": 0.0, "launches": 0,
-                                                "shape": (M, N, K), "shape_ms": 0.0})
-        agg["flops"] += flops[i] * args.steps
-        agg["ms"] += float(times[:, i].sum())
-        agg["launches"] += args.steps
-        if float(times[:, i].sum()) > agg["shape_ms"]:
-            agg["shape"], agg["shape_ms"] = (M, N, K), float(times[:, i].sum())
+                                                "shape": (M, N, K), "shape_ms": 0.0,
+                                                "kernel_us": 0.0, "kernel_flops": 0.0})
+        shape_ms = float(times[:, cols].sum())
+        agg["flops"] += flops[i] * us.size
+        agg["ms"] += shape_ms
+        agg["launches"] += int(us.size)
+        if ktimes is not None:
+            agg["kernel_us"] += _median(ktimes[(i, "flushed")])
+            agg["kernel_flops"] += flops[i]
+        if shape_ms > agg["shape_ms"]:
+            agg["shape"], agg["shape_ms"] = (M, N, K), shape_ms
     dom_name, dom = max(by_config.items(), key=lambda kv: kv[1]["ms"])
     achieved = dom["flops"] / (dom["ms"] * 1e-3) / 1e12
 
@@ -442,76 +541,78 @@ def run_ours(args):
         e1.synchronize()
         if s > 0:  # the first pass warms the copy engines
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_step_ms = max_over_ranks([statistics.median(e2e_ms)], dev)[0]
+    e2e_step_ms = statistics.median(e2e_ms)
     h2d = sum(2 * (M * K + N * K) + (c_bytes * M * N if fused else 0) for (M, N, K) in shapes)
     d2h = sum(c_bytes * M * N for (M, N, K) in shapes)
 
-    line = None
-    if rank == 0:
-        cpu = None
-        if not args.no_cpu_baseline and world == 1:
-            rate, cores, sample, secs = oracle_sample_rate(shapes, args.cpu_seconds, ab=ab)
-            cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                   "sample": (f"{sample} ({secs:.1f} s of oracle work; rows not timed "
-                              "are estimated from the sample's per-row time plus the "
-                              "calibrated fixed cost of decoding B)")}
-        line = {
-            "metric": METRIC, "value": round(float(value), 2), "unit": "TFLOP/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": ab, "data": "synthetic",
-            "config": {
-                "workload": args.workload + ": " + ", ".join(shape_name(s) for s in shapes),
-                "inputs": (f"uniform[-1,1] rounded to {ab}" if args.values == "uniform" else
-                           "integers in {-2..2}") + ", seeded SplitMix64, resident in HBM",
-                "accumulate": "f32", "output": c,
-                "epilogue": ("D = A·Bᵀ + D + bias (fused; C read back in place)"
-                             if args.epilogue == "fused" else "C = A·Bᵀ"),
-                "l2": "flushed between calls (256 MiB write), each call timed alone",
-                "timing": ("CUDA events on the launching stream around each call; a GPU-side "
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, cores, sample, secs = oracle_sample_rate(shapes, args.cpu_seconds, ab=ab)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": (f"{sample} ({secs:.1f} s of oracle work; rows not timed "
+                          "are estimated from the sample's per-row time plus the "
+                          "calibrated fixed cost of decoding B)")}
+    roofline = {
+        "bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 1),
+        "peak": peak_tflops, "unit": "TFLOP/s", "frac": round(achieved / peak_tflops, 4),
+        "peak_source": f"{peak_src} x fp16/bf16 nominal ratio 1 (of measured)",
+        "traffic": committed_traffic(dom_name, dom["shape"]),
+        "traffic_shape": shape_name(dom["shape"]),
+        "launches": dom["launches"],
+        "frac_vs_sustained": round(achieved / peak_sustained, 4),
+        "peak_sustained": peak_sustained,
+        "pipe_ceiling": ceiling, "pipe_ceiling_source": ceiling_src,
+        "frac_vs_pipe_ceiling": round(achieved / ceiling, 4) if ceiling else None,
+    }
+    if ktimes is not None and dom["kernel_us"] > 0:
+        roofline["achieved_kernel_time"] = round(
+            dom["kernel_flops"] / (dom["kernel_us"] * 1e-6) / 1e12, 1)
+    line = {
+        "metric": METRIC, "value": round(float(value), 2), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": ab, "data": "synthetic",
+        "config": workload_config(args, shapes),
+        "timing": {
+            "calls_per_step": {shape_name(s): r for s, r in zip(shapes, reps)},
+            "l2": "flushed between calls (256 MiB write), each call timed alone",
+            "events": ("CUDA events on the launching stream around each call; a GPU-side "
                        "spin ahead of the start event hides host enqueue latency"),
-                "e2e": ("every step: A and B uploaded from pinned host memory, the call, C "
-                        "downloaded; uploads and downloads on two copy streams, pipelined "
-                        "across the step's shapes; timed from the first upload to the last "
-                        "download"),
-                "parallelism": "replicas" if world > 1 else "single GPU",
-            },
-            "shapes": per_shape,
-            "roofline": {
-                "bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 1),
-                "peak": peak_tflops, "unit": "TFLOP/s", "frac": round(achieved / peak_tflops, 4),
-                "peak_source": f"{peak_src} x fp16/bf16 nominal ratio 1",
-                "traffic": committed_traffic(dom_name, dom["shape"]),
-                "traffic_shape": shape_name(dom["shape"]),
-            },
-            "cpu_baseline": cpu,
-            "e2e": {"value": round(job_value(float(flops.sum()), world, e2e_step_ms), 2),
-                    "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": gpu_launches,
-            "clocks": clk,
-            "wall_s_timed": round(t_wall, 3),
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
+            "kernel_time": ktime_note,
+            "e2e": ("every step: A and B uploaded from pinned host memory, the call, C "
+                    "downloaded; uploads and downloads on two copy streams, pipelined "
+                    "across the step's shapes; timed from the first upload to the last "
+                    "download"),
+        },
+        "shapes": per_shape,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(job_value(float(flops.sum()), e2e_step_ms), 2),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": gpu_launches,
+        "clocks": clk,
+        "wall_s_timed": round(t_wall, 3),
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("--gpus", type=int, default=1)
-    # 200 steps of the sweep take about a third of a second: with clocks
-    # sampled every 50 ms, several samples fall inside the timed region.
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--gpus", type=int, default=1, help="must be 1: the bench runs one GPU")
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="sweep")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="all")
     ap.add_argument("--shape", metavar="MxNxK",
                     help="time this one shape instead of a named workload")
+    ap.add_argument("--calls", type=int, default=0,
+                    help="calls of every shape per step (default: by shape size)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="oracle time budget of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kernel-time", action="store_true",
+                    help="skip the CUPTI kernel-time pass")
     ap.add_argument("--types", choices=sorted(TYPES), default="f16f32",
                     help="operand and C types (the measured product is f16f32)")
     ap.add_argument("--values", choices=["uniform", "int"], default="uniform",
@@ -520,6 +621,11 @@ def main(argv=None):
                     help="fused: D = A·Bᵀ + D + bias through the alpha/beta/bias epilogue")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    why = single_gpu_only(args)
+    if why:
+        ap.error(why)
+    if args.calls < 0:
+        ap.error("--calls wants a count >= 0")
     if args.shape:
         dims = tuple(int(v) for v in args.shape.lower().split("x"))
         if len(dims) != 3 or min(dims) <= 0:

@@ -8,7 +8,7 @@ flush (a 256 MiB write) and GPU-side gate, and is bracketed by CUDA events
 on the launching stream. Where this torch has no `out_dtype` for mm, the
 cuBLAS arm writes fp16 C (two bytes less per element) and says so.
 
-    python -m dense_fp16_gemm_02_gb300.compare [--workload all] [--rounds 20]
+    python compare.py [--workload all] [--rounds 20]
 
 Prints one JSON line per shape (medians, TFLOP/s of both, and the ratio)
 and one summary line. The same checks as the bench guard the comparison:
@@ -31,7 +31,7 @@ import os
 import statistics
 import sys
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 
 
 def main(argv=None) -> int:

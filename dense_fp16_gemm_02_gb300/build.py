@@ -3,11 +3,16 @@
 Each translation unit is compiled in parallel for sm_103a only, then linked
 into one shared library with the CUDA runtime linked statically. No CMake, no
 torch extension builder: plain nvcc.
+
+Beside it, when the toolkit's CUPTI is present, the bench's kernel-time
+recorder libwgemm_ktime.so (csrc/ktime_cupti.cpp, g++ against libcupti). The
+GEMM library does not depend on it.
 """
 from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import shutil
 import subprocess
 import sys
 
@@ -67,8 +72,57 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
+KTIME_SRC = os.path.join(CSRC, "ktime_cupti.cpp")
+KTIME_LIB = os.path.join(BUILD, "libwgemm_ktime.so")
+
+
+def _cuda_home() -> str:
+    home = os.environ.get("CUDA_HOME") or os.environ.get("CUDA_PATH")
+    if home:
+        return home
+    nvcc = shutil.which(NVCC)
+    if nvcc:
+        return os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
+    return "/usr/local/cuda"
+
+
+def cupti_paths():
+    """(include dir, library dir) of the toolkit's CUPTI, or None."""
+    home = _cuda_home()
+    incs = [os.path.join(home, "extras", "CUPTI", "include"), os.path.join(home, "include")]
+    libs = [os.path.join(home, "extras", "CUPTI", "lib64"), os.path.join(home, "lib64")]
+    tdir = os.path.join(home, "targets")
+    if os.path.isdir(tdir):
+        for t in sorted(os.listdir(tdir)):
+            incs.append(os.path.join(tdir, t, "include"))
+            libs.append(os.path.join(tdir, t, "lib"))
+    inc = next((d for d in incs if os.path.exists(os.path.join(d, "cupti.h"))), None)
+    lib = next((d for d in libs if os.path.exists(os.path.join(d, "libcupti.so"))), None)
+    return (inc, lib) if inc and lib else None
+
+
+def build_ktime() -> str | None:
+    """Compile the CUPTI kernel-time recorder; None when CUPTI is absent."""
+    paths = cupti_paths()
+    if paths is None:
+        return None
+    inc, lib = paths
+    os.makedirs(BUILD, exist_ok=True)
+    if not _stale(KTIME_LIB, [KTIME_SRC]):
+        return KTIME_LIB
+    tmp = KTIME_LIB + f".{os.getpid()}.tmp"
+    cmd = [os.environ.get("CXX", "g++"), "-O2", "-std=c++17", "-fPIC", "-shared", "-I", inc,
+           KTIME_SRC, "-o", tmp, "-L", lib, "-lcupti", f"-Wl,-rpath,{lib}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"kernel-time recorder build failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, KTIME_LIB)
+    return KTIME_LIB
+
+
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile every translation unit (in parallel) and link libwgemm.so."""
+    """Compile every translation unit (in parallel) and link libwgemm.so;
+    also the kernel-time recorder where CUPTI is present."""
     os.makedirs(BUILD, exist_ok=True)
     if force:
         for f in os.listdir(BUILD):
@@ -83,6 +137,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)
+    build_ktime()
     return LIB
 
 

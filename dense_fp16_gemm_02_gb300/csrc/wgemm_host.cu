@@ -208,6 +208,18 @@ cudaLaunchConfig_t launch_config(const KernelEntry& e, int workers, cudaStream_t
   return cfg;
 }
 
+// K-split grids (split-K, stream-K and their mixes) wait on flags that other
+// CTAs of the same grid raise, so every CTA must be resident at once. A
+// cooperative launch guarantees that: the grid starts only when all of its
+// CTAs fit on the GPU beside whatever else runs there (a grid that cannot fit
+// at all fails to launch). The grid never exceeds the co-resident count.
+// `attr` is the array cfg.attrs points to, with room for one more entry.
+void cooperative(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr) {
+  attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
+  attr[cfg.numAttrs].val.cooperative = 1;
+  ++cfg.numAttrs;
+}
+
 // Requires g_mu. Co-resident workers (clusters) of a configuration on this
 // device; sets the kernel's shared-memory attribute on first use.
 int max_workers(DeviceState& st, int id) {
@@ -482,6 +494,15 @@ int make_plan(const KernelEntry& e, int M, int N, int K, int mode, int splits, i
       p->dp_tiles = dp_waves * max_w;
       p->total_iters = (int64_t)(p->num_tiles - p->dp_tiles) * p->kblocks;
     }
+  } else if (mode == kTailK) {
+    // Owners and a tail split: needs fewer tiles than workers. Owner and tail
+    // shares are balanced: the owners run ceil(tiles·kblocks / workers)
+    // k-blocks of their tile, the idle workers share the rest.
+    if (p->num_tiles >= max_w) return WGEMM_ERR_CONFIG;
+    p->workers = max_w;
+    const int64_t total = (int64_t)p->num_tiles * p->kblocks;
+    p->owner_kb = (int32_t)std::min<int64_t>(p->kblocks, (total + max_w - 1) / max_w);
+    p->total_iters = (int64_t)p->num_tiles * (p->kblocks - p->owner_kb);
   } else {
     return WGEMM_ERR_CONFIG;
   }
@@ -617,9 +638,10 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
     std::fprintf(stderr, "wgemm: %dx%dx%d config %s mode %d splits %d workers %d tiles %d\n", M, N,
                  K, e.name, params.plan.mode, params.plan.splits, params.plan.workers,
                  params.plan.num_tiles);
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   cudaLaunchConfig_t cfg = launch_config(e, params.plan.workers, stream, attr);
   if (e.cg * e.mc * e.mr == 1) cfg.numAttrs = 0;  // no cluster: a plain launch
+  if (params.plan.mode != kDataParallel) cooperative(cfg, attr);
   if (g_pdl) {
     // May start (set-up only; loads wait) while the previous kernel on the
     // stream finishes, once that kernel allows its dependents to launch.
@@ -665,7 +687,7 @@ int wgemm_gemm_config(const void* A, const void* B, void* C, int ab_type, int c_
                       int K, int lda, int ldb, int ldc, int config_id, int mode, int splits,
                       wgemm_stream_t stream) {
   if (config_id < 0 || config_id >= (int)registry().entries.size()) return WGEMM_ERR_CONFIG;
-  if (mode < -1 || mode > kHybridK) return WGEMM_ERR_CONFIG;
+  if (mode < -1 || mode > kTailK) return WGEMM_ERR_CONFIG;
   return run(A, B, C, ab_type, c_type, M, N, K, lda, ldb, ldc, config_id, mode, splits,
              reinterpret_cast<cudaStream_t>(stream));
 }
@@ -993,8 +1015,9 @@ int run_noalloc(const uint16_t* A, const uint16_t* B, float* C, int M, int N, in
   params.flags = na->flags;
   params.flag_words = (int32_t)kNoAllocFlagWords;
   params.epoch = ++na->epoch;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_config(e, params.plan.workers, stream, attr);
+  cooperative(cfg, attr);
   void* args[] = {&params};
   if (cudaLaunchKernelExC(&cfg, e.func, args) != cudaSuccess) {
     cudaGetLastError();

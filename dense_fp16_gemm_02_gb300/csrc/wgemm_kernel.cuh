@@ -517,6 +517,25 @@ struct Kernel {
       }
       return;
     }
+    if constexpr (K::kKSplit) {
+      // K-split plans: each k-block of an operand has few readers, and C's
+      // lines, zeroed or stored early and reduce-added at the end, must stay
+      // in L2 meanwhile: the operand loads are marked evict-first.
+      if (p.plan.mode != kDataParallel) {
+        const uint64_t pol = l2_policy_evict_first();
+        if constexpr (K::CG == 1) {
+          mbar_arrive_expect_tx(full, K::kStageBytes);
+          tma_load_2d_hint(stage_a(base, s), &p.tmB, full, kb * kBK, b_row0, pol);
+          tma_load_2d_hint(a_dst, &p.tmA, full, kb * kBK, a_row0, pol);
+        } else {
+          if (rank == 0) mbar_arrive_expect_tx(full, 2 * K::kStageBytes);
+          const uint32_t full_leader = mapa_shared(full, group_leader(grp));
+          tma_load_2d_pair_hint(stage_a(base, s), &p.tmB, full_leader, kb * kBK, b_row0, pol);
+          tma_load_2d_pair_hint(a_dst, &p.tmA, full_leader, kb * kBK, a_row0, pol);
+        }
+        return;
+      }
+    }
     if constexpr (K::CG == 1) {
       mbar_arrive_expect_tx(full, K::kStageBytes);
       tma_load_2d(stage_a(base, s), &p.tmB, full, kb * kBK, b_row0);
@@ -971,7 +990,7 @@ struct Kernel {
     uint32_t sync_phase = 0;
 
     if constexpr (K::kKSplit) {
-      if (p.plan.mode == kSplitK)
+      if (p.plan.mode == kSplitK || p.plan.mode == kTailK)
         ok = zero_slices(p, base, rank, grp, worker, sync_phase, abort_flag);
     }
 
@@ -1000,8 +1019,8 @@ struct Kernel {
           u.tn * K::kTileCols + col_group(grp) * K::kGroupCols + (int32_t)rank * K::kCtaCols;
       const int32_t row0 = u.tm * K::kTileRows + row_group(grp) * K::BN;
       // Only K-split units add into C (data-parallel units store).
-      const bool add =
-          K::kKSplit && (u.kind == kUnitAddAfterOwner || u.kind == kUnitAddAfterZero);
+      const bool add = K::kKSplit && (u.kind == kUnitAddAfterOwner || u.kind == kUnitAddAfterZero ||
+                                      u.kind == kUnitAddAfterZeroed);
       if constexpr (K::kKSplit) {
         if (add && lane == 0) {
           if (u.kind == kUnitAddAfterOwner) {
@@ -1103,8 +1122,9 @@ struct Kernel {
   }
 
 
-  // Split-K: before any unit of this worker runs, zero this CTA's share of
-  // every tile slice it owns and raise the slice's flag.
+  // Split-K and the tail split: before any unit of this worker runs, zero
+  // this CTA's share of every tile slice its zeroing units (kind
+  // kUnitAddAfterZero) own and raise each slice's flag.
   __device__ static bool zero_slices(const KParams& p, uint32_t base, uint32_t rank, uint32_t grp,
                                      int32_t worker, uint32_t& sync_phase,
                                      volatile uint32_t* abort_flag) {
@@ -1115,6 +1135,7 @@ struct Kernel {
     for (int32_t i = 0;; ++i) {
       Unit u;
       if (!unit_at(p.plan, worker, i, u)) break;
+      if (u.kind != kUnitAddAfterZero) continue;
       int32_t r0, r1;
       plan_zero_rows(K::BN, p.plan.splits, u.split, r0, r1);
       const int32_t group_row0 = u.tm * K::kTileRows + row_group(grp) * K::BN;
@@ -1145,6 +1166,7 @@ struct Kernel {
       for (int32_t i = 0;; ++i) {
         Unit u;
         if (!unit_at(p.plan, worker, i, u)) break;
+        if (u.kind != kUnitAddAfterZero) continue;
         const int32_t fi = (u.tile * K::kClusterSize + crank) * p.plan.splits + u.split;
         if (WG_CHECK(p.status, fi < p.flag_words, kCheckFlag, fi))
           st_release_gpu(p.flags + fi, p.epoch);

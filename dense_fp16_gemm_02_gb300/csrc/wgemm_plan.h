@@ -36,14 +36,17 @@
 namespace wg {
 
 // kHybridK is a host-side request: its plan runs as kStreamK with dp_tiles > 0.
-enum PlanMode : int32_t { kDataParallel = 0, kSplitK = 1, kStreamK = 2, kHybridK = 3 };
+enum PlanMode : int32_t { kDataParallel = 0, kSplitK = 1, kStreamK = 2, kHybridK = 3,
+                          kTailK = 4 };
 
 // What the epilogue does with a unit's accumulator.
 enum UnitKind : int32_t {
   kUnitStore = 0,        // whole K of the tile: plain store
   kUnitStoreRaise = 1,   // stream-K: owns the tile's first k-block: store, then raise the flag
   kUnitAddAfterOwner = 2,// stream-K: add into C once the owner's flag is up
-  kUnitAddAfterZero = 3, // split-K: add into C once every split has zeroed its slice
+  kUnitAddAfterZero = 3, // split-K, and a tail-split owner: zero this unit's slice of the
+                         // tile first; add into C once every slice of the tile is zeroed
+  kUnitAddAfterZeroed = 4,  // tail-split tail: add into C once the tile is zeroed
 };
 
 struct Plan {
@@ -58,7 +61,9 @@ struct Plan {
   int32_t workers;      // persistent workers in the grid (clusters launched, with CLC)
   int32_t sched;        // 0: static stride; 1: cluster launch control (tiles taken at run time)
   int32_t dp_tiles;     // stream-K: leading tiles run data parallel (a multiple of workers)
-  int64_t total_iters;  // stream-K: (num_tiles − dp_tiles) · kblocks
+  int64_t total_iters;  // stream-K: (num_tiles − dp_tiles) · kblocks; tail split: tail k-blocks
+  int32_t owner_kb;     // tail split: k-blocks [0, owner_kb) of a tile run on its owner
+  int32_t pad_;
 };
 
 struct Unit {
@@ -128,6 +133,35 @@ WG_PLAN_HD bool plan_unit(const Plan& p, int32_t w, int32_t i, Unit& u) {
     if (u.kb_begin == 0 && u.kb_end == p.kblocks) u.kind = kUnitStore;
     else if (u.kb_begin == 0) u.kind = kUnitStoreRaise;
     else u.kind = kUnitAddAfterOwner;
+    return true;
+  }
+  if (p.mode == kTailK) {
+    // Worker w < num_tiles: its tile's first owner_kb k-blocks. Every other
+    // worker: its near-equal share of the tails, tile-major, in ascending order.
+    if (w < p.num_tiles) {
+      if (i > 0) return false;
+      plan_tile_unit(p, w, u);
+      u.kb_end = p.owner_kb;
+      if (p.total_iters > 0) u.kind = kUnitAddAfterZero;  // zeroes the tile, then adds
+      return true;
+    }
+    const int64_t L = (int64_t)p.kblocks - p.owner_kb;  // tail k-blocks of a tile
+    const int64_t Q = (int64_t)p.workers - p.num_tiles;
+    const int64_t q = (int64_t)w - p.num_tiles;
+    const int64_t T = p.total_iters;
+    if (L <= 0 || Q <= 0) return false;
+    const int64_t b = (T * q) / Q, e = (T * (q + 1)) / Q;
+    if (e <= b) return false;
+    const int64_t t = b / L + i;  // the i-th tile the range touches
+    if (t * L >= e) return false;
+    const int64_t s0 = t * L > b ? t * L : b;
+    const int64_t s1 = (t + 1) * L < e ? (t + 1) * L : e;
+    u.tile = (int32_t)t;
+    plan_tile_coords(p, u.tile, u.tm, u.tn);
+    u.kb_begin = p.owner_kb + (int32_t)(s0 - t * L);
+    u.kb_end = p.owner_kb + (int32_t)(s1 - t * L);
+    u.kind = kUnitAddAfterZeroed;
+    u.split = 0;
     return true;
   }
   const int64_t idx = (int64_t)w + (int64_t)i * p.workers;

@@ -7,21 +7,6 @@ per MMA shape, then one with the SM clock seen during the run.
 
     python -m dense_fp16_gemm_02_gb300.peak [iterations]
 
-With `--interference` it builds and runs `peak/mma_interference.cu`
-instead: the pair M256 N224 MMA loop while four more warps of every CTA
-make one kind of traffic (global stores, the register-store epilogue's
-pattern, shared-memory stores or loads, TMEM loads, bulk copies into shared
-memory), one JSON line per kind with the MMA rate and the traffic's rate.
-
-    python -m dense_fp16_gemm_02_gb300.peak --interference [iterations]
-
-With `--reduce` it builds and runs `peak/l2_reduce.cu`: bulk stores and
-bulk reduce-adds (.add.f32) of 4 KB fp32 blocks from shared memory, one
-issuing thread per SM, every CTA into its own region or nine CTAs into one
-region (a tile's split-K units), one JSON line per kind with GB/s.
-
-    python -m dense_fp16_gemm_02_gb300.peak --reduce [passes]
-
 With `--copies` it measures the host-device copy engines instead, the bound
 of the bench's end-to-end figure: pinned host memory to the device, back,
 and both directions at once on two streams, for 32, 128 and 256 MiB (CUDA
@@ -40,7 +25,7 @@ from . import build as _build
 from .clocks import ClockSampler
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-PROGRAMS = ("tensor_peak", "mma_interference", "l2_reduce")
+PROGRAMS = ("tensor_peak",)
 
 
 def build_peak(name: str = "tensor_peak") -> str:
@@ -115,12 +100,7 @@ def main(argv=None) -> int:
         for row in copy_rates():
             print(json.dumps(row))
         return 0
-    name = "tensor_peak"
-    if argv and argv[0] == "--interference":
-        name, argv = "mma_interference", argv[1:]
-    elif argv and argv[0] == "--reduce":
-        name, argv = "l2_reduce", argv[1:]
-    exe = build_peak(name)
+    exe = build_peak("tensor_peak")
     with ClockSampler(0) as clocks:
         clocks.mark_start()
         out = subprocess.run([exe, *argv], check=True, capture_output=True, text=True).stdout

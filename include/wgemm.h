@@ -31,9 +31,12 @@
  * occupancy it queried, and, per (device, stream), a small flag workspace for
  * the split-K and stream-K paths (allocated on first need with cudaMalloc,
  * grown when needed, freed by wgemm_release_workspace()). Calls on different
- * streams may run concurrently; the split-K and stream-K paths assume their
- * kernel's CTAs are all resident at once, which holds when no other kernel
- * shares the GPU.
+ * streams may run concurrently. The split-K and stream-K kernels (and their
+ * mixes) wait on flags that other CTAs of the same grid raise, so they are
+ * launched cooperatively: such a grid starts only once all of its CTAs fit on
+ * the GPU beside whatever else runs there, and then all are resident at once.
+ * A K-split call beside a long-running kernel from another stream therefore
+ * waits for room instead of running part of its grid.
  */
 #ifndef WGEMM_H
 #define WGEMM_H
@@ -94,8 +97,12 @@ int wgemm_f16f32(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
  * mode 0 = data parallel, 1 = split-K into `splits` ways (splits ≥ 1),
  * 2 = stream-K, 3 = whole waves of tiles data parallel and the rest (the
  * partial last wave and `splits` − 1 full waves before it, splits ≥ 1) by
- * stream-K, -1 = what the configuration table picks. Used by the tests and
- * the per-shape sweep. WGEMM_ERR_CONFIG if the combination cannot run.
+ * stream-K, 4 = owners and a tail split (fewer tiles than co-resident
+ * workers: each tile's owner runs its first k-blocks in step with the other
+ * owners, the idle workers share the tiles' remaining k-blocks, every part is
+ * added into C after the owner has zeroed the tile; `splits` is ignored),
+ * -1 = what the configuration table picks. Used by the tests and the
+ * per-shape sweep. WGEMM_ERR_CONFIG if the combination cannot run.
  */
 int wgemm_f16f32_config(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
                         int M, int N, int K, int lda, int ldb, int ldc,
@@ -292,6 +299,10 @@ int wgemm_release_workspace(void);
  * array's device address (cudaGetSymbolAddress) and the kernel's attributes
  * and occupancy; make that first call before any stream capture. The call
  * never calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * wgemm_set_pdl does not apply to this call: it is always launched without
+ * programmatic dependent launch, so it starts only after the previous kernel
+ * on the stream has finished.
  */
 int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
                                 int M, int N, int K, int lda, int ldb, int ldc,

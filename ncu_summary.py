@@ -2,10 +2,10 @@
 GEMM launches (with the traffic table bench.py reads) and the roofline table
 of the eleven shapes.
 
-    python -m dense_fp16_gemm_02_gb300.ncu_summary dram DRAM_CSV
-    python -m dense_fp16_gemm_02_gb300.ncu_summary roofline ROOFLINE_CSV BENCH_JSON
-    python -m dense_fp16_gemm_02_gb300.ncu_summary launches LAUNCHES_CSV
-    python -m dense_fp16_gemm_02_gb300.ncu_summary warm WARM_CSV COMPARE_JSONL
+    python ncu_summary.py dram DRAM_CSV
+    python ncu_summary.py roofline ROOFLINE_CSV BENCH_JSON
+    python ncu_summary.py launches LAUNCHES_CSV
+    python ncu_summary.py warm WARM_CSV COMPARE_JSONL
 
 DRAM_CSV is the `--csv --log-file` output of the dram command in
 profiles/dram_sweep.md; ROOFLINE_CSV and BENCH_JSON are those of
@@ -26,7 +26,7 @@ import statistics
 import sys
 from collections import OrderedDict
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 PROFILES = os.path.join(ROOT, "profiles")
 
 

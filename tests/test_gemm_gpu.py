@@ -9,9 +9,10 @@ Kernel Generation for Blackwell", section "The numbers"):
 * uniform[-1, 1] fp16 inputs: |C − C_ref| ≤ 2e-3·(|A|·|B|ᵀ)_ij + 1e-6 elementwise.
 
 Small cases run every configuration and every K-decomposition at sizes that
-span several tiles with ragged edges; the full-size cases of the workloads run
-the default per-shape choice (the launch the bench times) and are checked on
-sampled rows and columns the oracle computes one by one.
+span several tiles with ragged edges. The full-size cases of the workloads run
+the default per-shape choice (the launch the bench times) and are checked
+element by element over the whole of C, except 8192³ and 16384³, which are
+checked on 256 sampled rows and columns (the workload's own rule).
 """
 import re
 
@@ -25,7 +26,7 @@ from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
 pytestmark = pytest.mark.gpu
 
 RTOL, ATOL = 2e-3, 1e-6
-DP, SPLIT, STREAM, HYBRID = 0, 1, 2, 3
+DP, SPLIT, STREAM, HYBRID, TAIL = 0, 1, 2, 3, 4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -152,6 +153,17 @@ def test_stream_k_every_tma_config():
             check_full(A, B, K, kind, f"{name} stream-K {kind}", config=name, mode=STREAM)
 
 
+def test_tail_split_every_tma_config():
+    # Owners and a tail split (fewer tiles than workers): ragged edges, K not
+    # a multiple of 64; twice, to cross the flag epochs.
+    M, N, K = 520, 1100, 3000
+    for kind in ("int", "uniform"):
+        A, B = operands(M, N, K, 23, kind)
+        for name in k_split_configs():
+            for _ in range(2):
+                check_full(A, B, K, kind, f"{name} tail split {kind}", config=name, mode=TAIL)
+
+
 @pytest.mark.parametrize("held", [1, 2])
 def test_hybrid_every_tma_config(held):
     # Whole waves of tiles data parallel and the rest by stream-K: more tiles
@@ -174,7 +186,7 @@ def test_split_and_stream_equal_data_parallel_on_integers():
     A, B = inputs.gemm_operands(M, N, K, seed=5, kind="int")
     name = "g2_512x256_s4_a1_tma"
     base = run(A, B, K, config=name, mode=DP).cpu().numpy()
-    for mode, s in ((SPLIT, 2), (SPLIT, 9), (STREAM, 1), (HYBRID, 1)):
+    for mode, s in ((SPLIT, 2), (SPLIT, 9), (STREAM, 1), (HYBRID, 1), (TAIL, 1)):
         other = run(A, B, K, config=name, mode=mode, splits=s).cpu().numpy()
         assert np.array_equal(base, other), (mode, s)
 
@@ -183,13 +195,46 @@ def test_repeated_calls_share_flag_workspace():
     # Monotone epochs: flags are never reset between calls; alternate modes and
     # shapes on one stream and check every result.
     shapes = [(300, 700, 2000, SPLIT, 3), (520, 1100, 3000, STREAM, 1),
-              (256, 512, 4096, SPLIT, 9), (300, 700, 2000, STREAM, 1)]
+              (256, 512, 4096, SPLIT, 9), (300, 700, 2000, STREAM, 1),
+              (520, 1100, 3000, TAIL, 1)]
     for rep in range(3):
         for M, N, K, mode, s in shapes:
             A, B = inputs.gemm_operands(M, N, K, seed=rep, kind="int")
             C = run(A, B, K, config="g2_512x128_s4_a2_tma", mode=mode, splits=s)
             assert_exact(C.cpu().numpy().astype(np.float64), oracle.gemm_f64(A, B), "repeat")
     assert wgemm.wgemm_workspace_bytes() > 0
+
+
+def test_k_split_calls_on_several_streams_at_once():
+    """K-split grids wait on flags raised by other CTAs of the same grid, so
+    the library launches them cooperatively: a grid starts only once all its
+    CTAs fit. Here split-K, stream-K and tail-split calls, each filling most
+    of the GPU, are enqueued on three streams at once, with no ordering
+    between them, several rounds; every result is exact and no wait expires."""
+    M, N, K = 1024, 1024, 8192
+    A, B = inputs.gemm_operands(M, N, K, seed=17, kind="int")
+    ref = oracle.gemm_f64(A, B)
+    dA, dB = upload(A), upload(B)
+    cid = wgemm.config_id("g2_512x256_s4_a1_tma")
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    plans = [(SPLIT, 9), (STREAM, 1), (TAIL, 1)]
+    torch.cuda.synchronize()
+    outs = []
+    for rnd in range(4):
+        for s, (mode, sp) in zip(streams, plans):
+            C = torch.full((M, N), float("nan"), device="cuda")
+            C.record_stream(s)
+            outs.append((mode, C))
+        events = []
+        for (mode, C), s, (_, sp) in zip(outs[-3:], streams, plans):
+            s.wait_stream(torch.cuda.current_stream())
+            rc = wgemm.wgemm_f16f32_config(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K,
+                                           K, K, N, cid, mode, sp, s.cuda_stream)
+            assert rc == 0
+    for s in streams:
+        assert wgemm.wgemm_check(s.cuda_stream) == 0, wgemm.wgemm_last_device_error()
+    for mode, C in outs:
+        assert_exact(C.cpu().numpy().astype(np.float64), ref, f"mode {mode} on its own stream")
 
 
 def test_device_timeout_is_reported_and_context_survives():
@@ -333,16 +378,17 @@ def test_argument_errors_on_gpu():
 # ---------------------------------------------------------------- the workloads at full size
 
 WORKLOADS = [
-    # (M, N, K, kinds, sampled rows/cols or None for the full matrix)
-    (1024, 1024, 1024, ("int", "uniform"), None),
-    (1536, 1536, 1536, ("uniform",), 64),
-    (2048, 2048, 2048, ("uniform",), 64),
-    (3072, 1280, 2048, ("uniform",), 64),
-    (4096, 4096, 1024, ("uniform",), 64),
-    (4096, 4096, 4096, ("uniform",), 64),
-    (8192, 2048, 4096, ("uniform",), 64),
-    (1024, 1024, 65536, ("int", "uniform"), 32),
-    (2048, 2048, 16384, ("int", "uniform"), 32),
+    # (M, N, K, kinds): every element of C against the oracle. The integer
+    # copies (exact) are the pages' check; uniform inputs within the bound.
+    (1024, 1024, 1024, ("int", "uniform")),
+    (1536, 1536, 1536, ("uniform",)),
+    (2048, 2048, 2048, ("uniform",)),
+    (3072, 1280, 2048, ("uniform",)),
+    (4096, 4096, 1024, ("uniform",)),
+    (4096, 4096, 4096, ("uniform",)),
+    (8192, 2048, 4096, ("uniform",)),
+    (1024, 1024, 65536, ("int", "uniform")),
+    (2048, 2048, 16384, ("int", "uniform")),
 ]
 
 
@@ -360,22 +406,19 @@ def check_sampled(A, B, C: torch.Tensor, M, N, K, kind, n_sample, seed, what):
             assert_tol(got, ref, ref_abs, what)
 
 
-@pytest.mark.parametrize("M,N,K,kinds,sample", WORKLOADS)
-def test_workload_default_path(M, N, K, kinds, sample):
+@pytest.mark.parametrize("M,N,K,kinds", WORKLOADS)
+def test_workload_default_path(M, N, K, kinds):
     for kind in kinds:
         A, B = inputs.gemm_operands(M, N, K, seed=1000 + M + N + K, kind=kind)
         C = run(A, B, K)
-        if sample is None:
-            got = C.cpu().numpy().astype(np.float64)
-            if kind == "int":
-                assert_exact(got, oracle.gemm_f64(A, B), f"{M}x{N}x{K} int")
-            else:
-                ref, ref_abs = oracle.gemm_f64(A, B, with_abs=True)
-                assert_tol(got, ref, ref_abs, f"{M}x{N}x{K}")
-        else:
-            check_sampled(A, B, C, M, N, K, kind, sample, 77, f"{M}x{N}x{K} {kind}")
+        got = C.cpu().numpy().astype(np.float64)
         del C
         torch.cuda.empty_cache()
+        if kind == "int":
+            assert_exact(got, oracle.gemm_f64(A, B), f"{M}x{N}x{K} int")
+        else:
+            ref, ref_abs = oracle.gemm_f64(A, B, with_abs=True)
+            assert_tol(got, ref, ref_abs, f"{M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("n", [8192, 16384])

@@ -16,8 +16,8 @@ import pytest
 
 from dense_fp16_gemm_02_gb300 import build, wgemm
 
-KIND_STORE, KIND_RAISE, KIND_ADD_OWNER, KIND_ADD_ZERO = 0, 1, 2, 3
-DP, SPLIT, STREAM, HYBRID = 0, 1, 2, 3
+KIND_STORE, KIND_RAISE, KIND_ADD_OWNER, KIND_ADD_ZERO, KIND_ADD_ZEROED = 0, 1, 2, 3, 4
+DP, SPLIT, STREAM, HYBRID, TAIL = 0, 1, 2, 3, 4
 
 
 @pytest.fixture(scope="module")
@@ -126,6 +126,50 @@ def test_stream_k_covers_each_kblock_once(lib, M, N, K, workers):
         assert len(starts) == tm * tn and set(starts.values()) == {1}
 
 
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("workers", [2, 5, 76, 300])
+def test_tail_split_owners_and_tails(lib, M, N, K, workers):
+    """Owners and a tail split: worker t < tiles runs k-blocks [0, kh) of tile
+    t, kh = ceil(tiles·kb / workers); the other workers share the tails
+    [kh, kb) of all tiles, tile-major, in near-equal contiguous ranges. Every
+    (tile, k-block) once; each tile zeroed by its owner (the only zeroing
+    unit, the first and only unit of its worker, so every flag is raised at
+    the start and no unit waits on another's main loop); every worker's load
+    within one k-block of kh."""
+    for cfg in tma_configs(lib):
+        _, tr, tc = plan(lib, M, N, K, cfg, DP, 1, workers)
+        n = lib.wgemm_debug_plan(M, N, K, cfg, TAIL, 1, workers, None, 0, None, None)
+        tm, tn = tile_grid(M, N, tr, tc)
+        tiles, kb = tm * tn, -(-K // 64)
+        if tiles >= workers:
+            assert n == -6
+            continue
+        units, _, _ = plan(lib, M, N, K, cfg, TAIL, 1, workers)
+        hits = coverage(units, tm, tn, kb)
+        assert len(hits) == tiles * kb and set(hits.values()) == {1}
+        kh = min(kb, -(-(tiles * kb) // workers))
+        owners, tails = units[:tiles], units[tiles:]
+        assert [int(u[0]) for u in owners] == list(range(tiles))
+        assert np.all(owners[:, 3] == 0) and np.all(owners[:, 4] == kh)
+        assert np.all(owners[:, 5] == (KIND_STORE if kh == kb else KIND_ADD_ZERO))
+        assert np.all(owners[:, 6] == 0)
+        assert np.all(tails[:, 5] == KIND_ADD_ZEROED) and np.all(tails[:, 3] >= kh)
+        # Tail ranges per worker, from the definition; each worker's units are
+        # consecutive in the listing and in ascending tile order.
+        L, Q = kb - kh, workers - tiles
+        T = tiles * L
+        pos = 0
+        for q in range(Q):
+            b, e = T * q // Q, T * (q + 1) // Q
+            n_units = 0 if e <= b else (e - 1) // L - b // L + 1
+            mine = tails[pos:pos + n_units]
+            pos += n_units
+            load = int(sum(int(u[4]) - int(u[3]) for u in mine))
+            assert load == e - b and load <= kh + 1
+            assert list(mine[:, 0]) == sorted(mine[:, 0])
+        assert pos == len(tails)
 
 
 def simulate_stream_k(per_worker):

@@ -1,4 +1,4 @@
-"""The allocation-free split-K entry point against the existing one.
+"""The allocation-free split-K entry point against the existing one and the oracle.
 
 wgemm_f16f32_splitk_noalloc is for callers that may not allocate device
 memory while they run; its split-K flags sit in a fixed array inside the
@@ -57,15 +57,20 @@ def test_noalloc_matches_existing_entry_point(M, N, K, splits):
     for kind in ("int", "uniform"):
         A, B = inputs.gemm_operands(M, N, K, seed=M + splits, kind=kind)
         outs, ref = _both(A, B, M, N, K, splits)
+        exact, exact_abs = oracle.gemm_f64(A, B, with_abs=True)
         if kind == "int":
-            # Exact arithmetic: both entry points give the same values.
+            # Exact arithmetic: both entry points and the oracle agree exactly.
+            assert np.array_equal(ref, exact)
             for got in outs:
                 assert np.array_equal(got, ref)
+                assert np.array_equal(got, exact)
         else:
-            # Within the tolerance the other tests use, |A|·|B|ᵀ from the oracle.
-            _, ref_abs = oracle.gemm_f64(A, B, with_abs=True)
+            # Within the tolerance the other tests use: against the other
+            # entry point, and against the oracle's fp64 sum.
+            bound = RTOL * exact_abs + ATOL
             for got in outs:
-                assert np.all(np.abs(got - ref) <= RTOL * ref_abs + ATOL)
+                assert np.all(np.abs(got - ref) <= bound)
+                assert np.all(np.abs(got - exact) <= bound)
 
 
 def test_noalloc_rejects_problems_beyond_its_array():
@@ -79,4 +84,5 @@ def test_noalloc_rejects_problems_beyond_its_array():
     A, B = inputs.gemm_operands(256, 512, 640, seed=1, kind="int")
     outs, ref = _both(A, B, 256, 512, 640, 2)
     assert np.array_equal(outs[1], ref)
+    assert np.array_equal(outs[1], oracle.gemm_f64(A, B))
     assert wgemm.wgemm_workspace_bytes() == before  # the no-alloc calls took no workspace
