@@ -60,7 +60,7 @@ WORKLOADS = {
 WORKLOADS["all"] = (WORKLOADS["c1"] + WORKLOADS["sweep"] + WORKLOADS["large"]
                     + WORKLOADS["streamk"] + WORKLOADS["splitk"])
 MODE_NAMES = ["data-parallel", "split-K", "stream-K", "data-parallel + stream-K tail",
-              "owners + tail split"]
+              "stream-K, zeroing first"]
 
 
 def calls_per_step(M: int, N: int, K: int) -> int:

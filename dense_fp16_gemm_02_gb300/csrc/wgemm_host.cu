@@ -312,11 +312,13 @@ bool fuse_fits(const KernelEntry& e, int fuse) {
 }
 
 // Configurations that may run split-K or stream-K plans: TMA epilogue (the
-// reduce-adds), static schedule and no multicast (every worker resident and
-// owning its own tiles), fp32 C and no fused epilogue. The kernel compiles
-// its split-K and stream-K paths for exactly these (Cfg::kKSplit).
+// reduce-adds), static schedule (every worker resident and owning its own
+// units), no column multicast, fp32 C and no fused epilogue. Row-multicast
+// clusters qualify: the cluster is the worker and its groups share every
+// unit. The kernel compiles its split-K and stream-K paths for exactly these
+// (Cfg::kKSplit).
 bool can_split_k(const KernelEntry& e) {
-  return e.epi == kEpiTma && e.mc == 1 && e.mr == 1 && e.sched == 0 && e.out == 0 && !e.fuse;
+  return e.epi == kEpiTma && e.mc == 1 && e.sched == 0 && e.out == 0 && !e.fuse;
 }
 
 // Predicted microseconds of a configuration and K-decomposition from the
@@ -494,15 +496,12 @@ int make_plan(const KernelEntry& e, int M, int N, int K, int mode, int splits, i
       p->dp_tiles = dp_waves * max_w;
       p->total_iters = (int64_t)(p->num_tiles - p->dp_tiles) * p->kblocks;
     }
-  } else if (mode == kTailK) {
-    // Owners and a tail split: needs fewer tiles than workers. Owner and tail
-    // shares are balanced: the owners run ceil(tiles·kblocks / workers)
-    // k-blocks of their tile, the idle workers share the rest.
-    if (p->num_tiles >= max_w) return WGEMM_ERR_CONFIG;
-    p->workers = max_w;
-    const int64_t total = (int64_t)p->num_tiles * p->kblocks;
-    p->owner_kb = (int32_t)std::min<int64_t>(p->kblocks, (total + max_w - 1) / max_w);
-    p->total_iters = (int64_t)p->num_tiles * (p->kblocks - p->owner_kb);
+  } else if (mode == kStreamKZero) {
+    // Stream-K ranges with split-K's fix-up: owners zero their tile first.
+    p->mode = kStreamK;
+    p->zero_first = 1;
+    p->total_iters = (int64_t)p->num_tiles * p->kblocks;
+    p->workers = (int32_t)std::min<int64_t>(p->total_iters, max_w);
   } else {
     return WGEMM_ERR_CONFIG;
   }
@@ -687,7 +686,7 @@ int wgemm_gemm_config(const void* A, const void* B, void* C, int ab_type, int c_
                       int K, int lda, int ldb, int ldc, int config_id, int mode, int splits,
                       wgemm_stream_t stream) {
   if (config_id < 0 || config_id >= (int)registry().entries.size()) return WGEMM_ERR_CONFIG;
-  if (mode < -1 || mode > kTailK) return WGEMM_ERR_CONFIG;
+  if (mode < -1 || mode > kStreamKZero) return WGEMM_ERR_CONFIG;
   return run(A, B, C, ab_type, c_type, M, N, K, lda, ldb, ldc, config_id, mode, splits,
              reinterpret_cast<cudaStream_t>(stream));
 }

@@ -221,8 +221,10 @@ struct Cfg {
 
   // The configurations the host may give a split-K or stream-K plan; every
   // other one runs data-parallel plans only and compiles just that path.
+  // With row multicast (MR = 2) a worker is the cluster: both MMA groups walk
+  // the same units, so they always need the same k-blocks of B.
   static constexpr bool kKSplit =
-      EPI == kEpiTma && SCHED == kSchedStatic && MC == 1 && MR == 1 && OUT == kOut32 && FUSE == 0;
+      EPI == kEpiTma && SCHED == kSchedStatic && MC == 1 && OUT == kOut32 && FUSE == 0;
 
   static_assert(CG == 1 || CG == 2, "CG");
   static_assert(OUT == kOut32 || OUT == kOut16, "OUT");
@@ -990,7 +992,7 @@ struct Kernel {
     uint32_t sync_phase = 0;
 
     if constexpr (K::kKSplit) {
-      if (p.plan.mode == kSplitK || p.plan.mode == kTailK)
+      if (p.plan.mode == kSplitK || p.plan.zero_first)
         ok = zero_slices(p, base, rank, grp, worker, sync_phase, abort_flag);
     }
 
@@ -1022,24 +1024,34 @@ struct Kernel {
       const bool add = K::kKSplit && (u.kind == kUnitAddAfterOwner || u.kind == kUnitAddAfterZero ||
                                       u.kind == kUnitAddAfterZeroed);
       if constexpr (K::kKSplit) {
-        if (add && lane == 0) {
+        if (add) {
           if (u.kind == kUnitAddAfterOwner) {
-            ok = WG_CHECK(p.status, (int32_t)(u.tile * K::kClusterSize + crank) < p.flag_words, kCheckFlag,
-                          u.tile) &&
-                 wait_flag(p.flags + (u.tile * K::kClusterSize + crank), p.epoch + p.wait_skew, abort_flag, p.status,
-                           kSiteEpiFlagOwner);
-          } else {
-            for (int32_t s = 0; s < p.plan.splits && ok; ++s)
-              ok = WG_CHECK(p.status,
-                            (int32_t)((u.tile * K::kClusterSize + crank) * p.plan.splits + s) < p.flag_words,
+            if (lane == 0)
+              ok = WG_CHECK(p.status, (int32_t)(u.tile * K::kClusterSize + crank) < p.flag_words,
                             kCheckFlag, u.tile) &&
-                   wait_flag(p.flags + ((u.tile * K::kClusterSize + crank) * p.plan.splits + s),
-                             p.epoch + p.wait_skew,
-                             abort_flag, p.status, kSiteEpiFlagZero);
+                   wait_flag(p.flags + (u.tile * K::kClusterSize + crank), p.epoch + p.wait_skew,
+                             abort_flag, p.status, kSiteEpiFlagOwner);
+          } else {
+            // Every slice's zeroing flag of the tile, one lane per flag, so the
+            // acquire loads' round trips overlap instead of adding up.
+            const int32_t f0 = (u.tile * K::kClusterSize + crank) * p.plan.splits;
+            for (int32_t s0 = 0; s0 < p.plan.splits && ok; s0 += 32) {
+              const int32_t s = s0 + (int32_t)lane;
+              bool mine = true;
+              if (s < p.plan.splits)
+                mine = WG_CHECK(p.status, f0 + s < p.flag_words, kCheckFlag, u.tile) &&
+                       wait_flag(p.flags + (f0 + s), p.epoch + p.wait_skew, abort_flag, p.status,
+                                 kSiteEpiFlagZero);
+              ok = __all_sync(0xffffffffu, mine);
+            }
           }
-          // The flag's acquire covers generic writes; order them before the
-          // async-proxy reduce-add that follows.
-          fence_proxy_async_global();
+          // The lanes' acquires cover the generic zero stores (the warp
+          // barrier carries them to lane 0); order them before the
+          // async-proxy reduce-adds that lane 0 issues.
+          if (lane == 0) {
+            fence_acq_rel_gpu();
+            fence_proxy_async_global();
+          }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
@@ -1122,8 +1134,8 @@ struct Kernel {
   }
 
 
-  // Split-K and the tail split: before any unit of this worker runs, zero
-  // this CTA's share of every tile slice its zeroing units (kind
+  // Split-K and zero-first stream-K: before any unit of this worker runs,
+  // zero this CTA's share of every tile slice its zeroing units (kind
   // kUnitAddAfterZero) own and raise each slice's flag.
   __device__ static bool zero_slices(const KParams& p, uint32_t base, uint32_t rank, uint32_t grp,
                                      int32_t worker, uint32_t& sync_phase,

@@ -23,7 +23,12 @@
 //    tiles left over are shared out by stream-K over the same workers, after
 //    their data-parallel units. The page's stream-K spreads all tiles; this
 //    mix splits only the partial last wave (or the last few waves), so that
-//    the reduce-adds stay few when tiles outnumber workers.
+//    the reduce-adds stay few when tiles outnumber workers;
+//  * stream-K with zeroing first (`zero_first`): the same ranges as
+//    stream-K, with the fix-up of split-K. The unit holding a tile's first
+//    k-block zeroes the tile when its CTA starts and raises the tile's flag;
+//    every unit of the tile, that one included, adds its partial into C once
+//    the flag is up. No unit waits on another unit's main loop.
 #pragma once
 #include <stdint.h>
 
@@ -35,18 +40,19 @@
 
 namespace wg {
 
-// kHybridK is a host-side request: its plan runs as kStreamK with dp_tiles > 0.
+// kHybridK and kStreamKZero are host-side requests: their plans run as
+// kStreamK (with dp_tiles > 0, or with zero_first = 1).
 enum PlanMode : int32_t { kDataParallel = 0, kSplitK = 1, kStreamK = 2, kHybridK = 3,
-                          kTailK = 4 };
+                          kStreamKZero = 4 };
 
 // What the epilogue does with a unit's accumulator.
 enum UnitKind : int32_t {
   kUnitStore = 0,        // whole K of the tile: plain store
   kUnitStoreRaise = 1,   // stream-K: owns the tile's first k-block: store, then raise the flag
   kUnitAddAfterOwner = 2,// stream-K: add into C once the owner's flag is up
-  kUnitAddAfterZero = 3, // split-K, and a tail-split owner: zero this unit's slice of the
-                         // tile first; add into C once every slice of the tile is zeroed
-  kUnitAddAfterZeroed = 4,  // tail-split tail: add into C once the tile is zeroed
+  kUnitAddAfterZero = 3, // split-K, and a zero-first stream-K owner: zero this unit's slice
+                         // of the tile first; add into C once every slice of the tile is zeroed
+  kUnitAddAfterZeroed = 4,  // zero-first stream-K: add into C once the tile is zeroed
 };
 
 struct Plan {
@@ -61,8 +67,8 @@ struct Plan {
   int32_t workers;      // persistent workers in the grid (clusters launched, with CLC)
   int32_t sched;        // 0: static stride; 1: cluster launch control (tiles taken at run time)
   int32_t dp_tiles;     // stream-K: leading tiles run data parallel (a multiple of workers)
-  int64_t total_iters;  // stream-K: (num_tiles − dp_tiles) · kblocks; tail split: tail k-blocks
-  int32_t owner_kb;     // tail split: k-blocks [0, owner_kb) of a tile run on its owner
+  int64_t total_iters;  // stream-K: (num_tiles − dp_tiles) · kblocks
+  int32_t zero_first;   // stream-K: 1 = owners zero the tile first and every unit adds
   int32_t pad_;
 };
 
@@ -131,37 +137,9 @@ WG_PLAN_HD bool plan_unit(const Plan& p, int32_t w, int32_t i, Unit& u) {
     u.kb_end = (int32_t)(s1 - t * kb);
     u.split = 0;
     if (u.kb_begin == 0 && u.kb_end == p.kblocks) u.kind = kUnitStore;
+    else if (p.zero_first) u.kind = u.kb_begin == 0 ? kUnitAddAfterZero : kUnitAddAfterZeroed;
     else if (u.kb_begin == 0) u.kind = kUnitStoreRaise;
     else u.kind = kUnitAddAfterOwner;
-    return true;
-  }
-  if (p.mode == kTailK) {
-    // Worker w < num_tiles: its tile's first owner_kb k-blocks. Every other
-    // worker: its near-equal share of the tails, tile-major, in ascending order.
-    if (w < p.num_tiles) {
-      if (i > 0) return false;
-      plan_tile_unit(p, w, u);
-      u.kb_end = p.owner_kb;
-      if (p.total_iters > 0) u.kind = kUnitAddAfterZero;  // zeroes the tile, then adds
-      return true;
-    }
-    const int64_t L = (int64_t)p.kblocks - p.owner_kb;  // tail k-blocks of a tile
-    const int64_t Q = (int64_t)p.workers - p.num_tiles;
-    const int64_t q = (int64_t)w - p.num_tiles;
-    const int64_t T = p.total_iters;
-    if (L <= 0 || Q <= 0) return false;
-    const int64_t b = (T * q) / Q, e = (T * (q + 1)) / Q;
-    if (e <= b) return false;
-    const int64_t t = b / L + i;  // the i-th tile the range touches
-    if (t * L >= e) return false;
-    const int64_t s0 = t * L > b ? t * L : b;
-    const int64_t s1 = (t + 1) * L < e ? (t + 1) * L : e;
-    u.tile = (int32_t)t;
-    plan_tile_coords(p, u.tile, u.tm, u.tn);
-    u.kb_begin = p.owner_kb + (int32_t)(s0 - t * L);
-    u.kb_end = p.owner_kb + (int32_t)(s1 - t * L);
-    u.kind = kUnitAddAfterZeroed;
-    u.split = 0;
     return true;
   }
   const int64_t idx = (int64_t)w + (int64_t)i * p.workers;

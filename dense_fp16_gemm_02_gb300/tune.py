@@ -10,8 +10,8 @@ K-decomposition on this GPU and records the fastest for each shape.
 Each candidate call runs alone (L2 flushed with a 256 MiB write before it)
 and is timed with CUDA events on the launching stream; the median of the
 timed calls is kept. Split-K is tried only when the data-parallel tiles leave
-most workers idle, stream-K when they fill less than two waves, the owners +
-tail split when there are fewer tiles than workers. The emitted
+most workers idle, stream-K (with either fix-up) when they fill less than two
+waves. The emitted
 table is compiled into the library, which consults it before its shape rule.
 """
 from __future__ import annotations
@@ -52,13 +52,15 @@ def candidates(M, N, K, names, workers_pair, workers_single):
         cols, rows = (int(v) for v in name.split("_")[1].split("x"))
         tiles = -(-M // rows) * -(-N // cols)
         workers = workers_pair if cg == 2 else workers_single
+        if re.match(r"g\d[mr]2_", name):  # clusters of two MMA groups: half the workers
+            workers //= 2
         out.append((cid, 0, 1))
-        if not name.endswith("_tma") or kb < 8 or re.match(r"g\d[mr]2_", name):
+        if not name.endswith("_tma") or kb < 8 or re.match(r"g\dm2_", name):
             continue
         if tiles < 2 * workers:
             out.append((cid, 2, 1))
-        if tiles < workers:
-            out.append((cid, 4, 1))  # owners and a tail split (forced only; measured slower)
+        if tiles < 2 * workers:
+            out.append((cid, 4, 1))  # stream-K with zeroing first
         if tiles >= workers and tiles % workers:
             # whole waves data parallel, the partial wave (and one more) by stream-K
             out.append((cid, 3, 1))
@@ -233,7 +235,7 @@ def emit(json_paths, inc_path=TUNED_INC):
         "// Measured per-shape winners (generated by dense_fp16_gemm_02_gb300/tune.py from",
         f"// {boxes} on {d.get('gpu', 'a GB300')} with {d.get('sm_count')} SMs; do not edit by hand).",
         "// {M, N, K, configuration name, mode (0 data parallel, 1 split-K, 2 stream-K,",
-        "//  3 data-parallel waves + stream-K tail, 4 owners + tail split),",
+        "//  3 data-parallel waves + stream-K tail, 4 stream-K with zeroing first),",
         "//  splits, measured µs per call (mean over the sweeps)}",
     ]
     chosen = combine(sweeps)

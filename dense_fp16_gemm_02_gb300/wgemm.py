@@ -26,9 +26,9 @@ MODE_DATA_PARALLEL, MODE_SPLIT_K, MODE_STREAM_K = 0, 1, 2
 # Whole waves of tiles data parallel, the rest (partial last wave and `splits` − 1
 # full waves before it) by stream-K.
 MODE_HYBRID = 3
-# Fewer tiles than workers: each tile's owner runs its first k-blocks, the idle
-# workers share the tiles' remaining k-blocks; all add into the zeroed tile.
-MODE_TAIL = 4
+# Stream-K ranges with split-K's fix-up: each tile's owner zeroes it first and
+# every unit adds its partial into C.
+MODE_STREAM_K_ZERO = 4
 WGEMM_F32, WGEMM_F16, WGEMM_BF16 = 0, 1, 2
 
 

@@ -97,11 +97,10 @@ int wgemm_f16f32(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
  * mode 0 = data parallel, 1 = split-K into `splits` ways (splits ≥ 1),
  * 2 = stream-K, 3 = whole waves of tiles data parallel and the rest (the
  * partial last wave and `splits` − 1 full waves before it, splits ≥ 1) by
- * stream-K, 4 = owners and a tail split (fewer tiles than co-resident
- * workers: each tile's owner runs its first k-blocks in step with the other
- * owners, the idle workers share the tiles' remaining k-blocks, every part is
- * added into C after the owner has zeroed the tile; `splits` is ignored),
- * -1 = what the configuration table picks. Used by the tests and the
+ * stream-K, 4 = stream-K with zeroing first (the stream-K ranges; the unit
+ * holding a tile's first k-block zeroes the tile when its kernel starts,
+ * and every unit, that one included, adds its partial into C; `splits` is
+ * ignored), -1 = what the configuration table picks. Used by the tests and the
  * per-shape sweep. WGEMM_ERR_CONFIG if the combination cannot run.
  */
 int wgemm_f16f32_config(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,

@@ -6,6 +6,8 @@ of the eleven shapes.
     python ncu_summary.py roofline ROOFLINE_CSV BENCH_JSON
     python ncu_summary.py launches LAUNCHES_CSV
     python ncu_summary.py warm WARM_CSV COMPARE_JSONL
+    python ncu_summary.py shapes CSV_DIR BENCH_JSON
+    python ncu_summary.py launches-all LAUNCHES_CSV BENCH_JSON
 
 DRAM_CSV is the `--csv --log-file` output of the dram command in
 profiles/dram_sweep.md; ROOFLINE_CSV and BENCH_JSON are those of
@@ -90,6 +92,97 @@ def dram(csv_path: str) -> None:
     header = ("| shape | configuration | µs (ncu) | DRAM read MB | DRAM write MB | "
               "compulsory A+B MB | C MB |\n|---|---|---|---|---|---|---|\n")
     text = _set_digest(_replace_table(text, header, rows), digest)
+    open(p, "w").write(text)
+    print("\n".join(rows))
+
+
+def _bench_line(bench_json: str) -> dict:
+    with open(bench_json) as f:
+        return json.loads([l for l in f.read().splitlines() if l.startswith("{")][-1])
+
+
+SHAPE_HEADER = ("| M×N×K | configuration | mode | grid (CTAs) | waves | bench µs (events, median) | "
+                "kernel µs (CUPTI, flushed) | kernel µs (CUPTI, warm) | bench TFLOP/s | tensor frac "
+                "(bench) | ncu µs | tensor pipe active % (ncu) | SM active % (ncu) | DRAM read MB | "
+                "DRAM write MB | DRAM read ÷ compulsory A+B |\n"
+                "|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
+
+
+def shapes(csv_dir: str, bench_json: str) -> None:
+    """One ncu capture per shape (CSV_DIR/<M>x<N>x<K>.csv: one launch of the
+    shape's default configuration, one pass of seven counters) beside the
+    bench line: the table of profiles/roofline_all_shapes.md, and the DRAM
+    traffic per launch of every shape's kernel in profiles/traffic.json
+    (which the bench reads for its roofline line)."""
+    b = _bench()
+    d = _bench_line(bench_json)
+    digest = b.kernel_source_digest()
+    rows, traffic = [], []
+    for s in d["shapes"]:
+        M, N, K = (int(x) for x in s["shape"].split("x"))
+        by = read_ncu_csv(os.path.join(csv_dir, s["shape"] + ".csv"))
+        v = [x for x in by.values() if "wgemm_kernel" in x["kernel"]][-1]
+        cfg = _config_of_kernel(v["kernel"])
+        if cfg != s["config"]:
+            raise SystemExit(f"{s['shape']}: captured {cfg}, bench ran {s['config']}")
+        t = v["gpu__time_duration.sum"] / 1000.0
+        active = 100.0 * v["sm__cycles_active.avg"] / v["gpc__cycles_elapsed.max"]
+        grid = int(v.get("launch__grid_size", 0))
+        rd, wr = v["dram__bytes_read.sum"], v["dram__bytes_write.sum"]
+        ab = 2.0 * (M * K + N * K)
+        rows.append(
+            f"| {M}×{N}×{K} | {cfg} | {s['mode']} | {grid} | "
+            f"{_waves(cfg, M, N, grid, s['mode'], s.get('splits', 1))} | "
+            f"{s['us_median']:.3f} | {s.get('us_kernel_median', float('nan')):.3f} | "
+            f"{s.get('us_kernel_warm_median', float('nan')):.3f} | {s['tflops']} | "
+            f"{s['tensor_frac']} | {t:.1f} | "
+            f"{v['sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed']:.1f} | "
+            f"{active:.1f} | {rd / 1e6:.1f} | {wr / 1e6:.1f} | {rd / ab:.2f} |")
+        traffic.append({"kernel_src": digest, "config": cfg, "shape": s["shape"],
+                        "dram_bytes": int(rd + wr),
+                        "source": (f"profiles/roofline_all_shapes.md (dram__bytes_read.sum "
+                                   f"{int(rd):,} B + dram__bytes_write.sum {int(wr):,} B, "
+                                   "one launch)")})
+    with open(os.path.join(PROFILES, "traffic.json"), "w") as f:
+        json.dump(traffic, f, indent=1)
+    p = os.path.join(PROFILES, "roofline_all_shapes.md")
+    text = open(p).read()
+    text = _set_digest(_replace_table(text, SHAPE_HEADER, rows), digest)
+    open(p, "w").write(text)
+    print("\n".join(rows))
+
+
+def launches_all(csv_path: str, bench_json: str) -> None:
+    """The launch list of a bench run (every GEMM launch with
+    gpu__time_duration.sum; cold-cache and serialised under ncu) per
+    configuration: launches, total µs and share of the GEMM time, beside the
+    share of the bench line's own timed steps (CUDA events) for the same
+    configuration. Writes the table of profiles/launches_all_shapes.md."""
+    b = _bench()
+    d = _bench_line(bench_json)
+    by = read_ncu_csv(csv_path)
+    agg = OrderedDict()
+    for v in by.values():
+        if "wgemm_kernel" not in v["kernel"]:
+            continue
+        a = agg.setdefault(_config_of_kernel(v["kernel"]), [0, 0.0])
+        a[0] += 1
+        a[1] += v["gpu__time_duration.sum"] / 1000.0
+    total = sum(a[1] for a in agg.values())
+    bench_ms = OrderedDict()
+    for s in d["shapes"]:
+        bench_ms[s["config"]] = bench_ms.get(s["config"], 0.0) + s["us_median"] * s["calls"]
+    btotal = sum(bench_ms.values())
+    rows = []
+    for cfg, (n, us) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
+        shapes_of = ", ".join(s["shape"] for s in d["shapes"] if s["config"] == cfg)
+        rows.append(f"| {cfg} | {shapes_of} | {n} | {us:.1f} | {100.0 * us / total:.1f} % | "
+                    f"{100.0 * bench_ms.get(cfg, 0.0) / btotal:.1f} % |")
+    p = os.path.join(PROFILES, "launches_all_shapes.md")
+    text = open(p).read()
+    header = ("| configuration | shapes | launches (ncu) | total µs (ncu) | share of GEMM time "
+              "(ncu) | share of the bench's timed steps (events) |\n|---|---|---|---|---|---|\n")
+    text = _set_digest(_replace_table(text, header, rows), b.kernel_source_digest())
     open(p, "w").write(text)
     print("\n".join(rows))
 
@@ -215,7 +308,7 @@ def _waves(config: str, M: int, N: int, grid: int, mode: str, splits: int) -> st
         workers = min(workers, {1: 152, 2: 76, 4: 36}.get(cluster, workers))
     if mode == "split-K":
         tiles *= splits
-    elif mode == "stream-K":
+    elif mode.startswith("stream-K"):
         return "1 (stream)"
     elif mode == "data-parallel + stream-K tail":
         return f"{tiles / workers:.2f} (stream-K tail)"
@@ -267,6 +360,10 @@ def main(argv=None) -> int:
         launches(argv[1])
     elif len(argv) >= 3 and argv[0] == "warm":
         warm(argv[1], argv[2])
+    elif len(argv) >= 3 and argv[0] == "shapes":
+        shapes(argv[1], argv[2])
+    elif len(argv) >= 3 and argv[0] == "launches-all":
+        launches_all(argv[1], argv[2])
     else:
         print(__doc__)
         return 2

@@ -26,7 +26,7 @@ from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
 pytestmark = pytest.mark.gpu
 
 RTOL, ATOL = 2e-3, 1e-6
-DP, SPLIT, STREAM, HYBRID, TAIL = 0, 1, 2, 3, 4
+DP, SPLIT, STREAM, HYBRID, ZERO_FIRST = 0, 1, 2, 3, 4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -97,8 +97,9 @@ def is_multicast(name: str) -> bool:
 
 
 def k_split_configs():
-    """Configurations that run split-K and stream-K (TMA epilogue, no multicast)."""
-    return [n for n in configs("_tma") if not is_multicast(n)]
+    """Configurations that run split-K and stream-K: TMA epilogue, no column
+    multicast (row-multicast clusters run them as one worker)."""
+    return [n for n in configs("_tma") if not re.match(r"g\dm2_", n)]
 
 
 # ---------------------------------------------------------------- every configuration
@@ -153,15 +154,17 @@ def test_stream_k_every_tma_config():
             check_full(A, B, K, kind, f"{name} stream-K {kind}", config=name, mode=STREAM)
 
 
-def test_tail_split_every_tma_config():
-    # Owners and a tail split (fewer tiles than workers): ragged edges, K not
-    # a multiple of 64; twice, to cross the flag epochs.
-    M, N, K = 520, 1100, 3000
-    for kind in ("int", "uniform"):
-        A, B = operands(M, N, K, 23, kind)
-        for name in k_split_configs():
-            for _ in range(2):
-                check_full(A, B, K, kind, f"{name} tail split {kind}", config=name, mode=TAIL)
+def test_stream_k_zero_first_every_tma_config():
+    # Stream-K with zeroing first: ragged edges, K not a multiple of 64; more
+    # tiles than workers too (the 256-wide tiles at 2600 × 3000); twice, to
+    # cross the flag epochs.
+    for (M, N, K) in ((520, 1100, 3000), (2600, 3000, 700)):
+        for kind in ("int", "uniform"):
+            A, B = operands(M, N, K, 23, kind)
+            for name in k_split_configs():
+                for _ in range(2):
+                    check_full(A, B, K, kind, f"{name} stream-K zero first {M}x{N}x{K} {kind}",
+                               config=name, mode=ZERO_FIRST)
 
 
 @pytest.mark.parametrize("held", [1, 2])
@@ -186,7 +189,7 @@ def test_split_and_stream_equal_data_parallel_on_integers():
     A, B = inputs.gemm_operands(M, N, K, seed=5, kind="int")
     name = "g2_512x256_s4_a1_tma"
     base = run(A, B, K, config=name, mode=DP).cpu().numpy()
-    for mode, s in ((SPLIT, 2), (SPLIT, 9), (STREAM, 1), (HYBRID, 1), (TAIL, 1)):
+    for mode, s in ((SPLIT, 2), (SPLIT, 9), (STREAM, 1), (HYBRID, 1), (ZERO_FIRST, 1)):
         other = run(A, B, K, config=name, mode=mode, splits=s).cpu().numpy()
         assert np.array_equal(base, other), (mode, s)
 
@@ -196,7 +199,7 @@ def test_repeated_calls_share_flag_workspace():
     # shapes on one stream and check every result.
     shapes = [(300, 700, 2000, SPLIT, 3), (520, 1100, 3000, STREAM, 1),
               (256, 512, 4096, SPLIT, 9), (300, 700, 2000, STREAM, 1),
-              (520, 1100, 3000, TAIL, 1)]
+              (520, 1100, 3000, ZERO_FIRST, 1)]
     for rep in range(3):
         for M, N, K, mode, s in shapes:
             A, B = inputs.gemm_operands(M, N, K, seed=rep, kind="int")
@@ -208,16 +211,17 @@ def test_repeated_calls_share_flag_workspace():
 def test_k_split_calls_on_several_streams_at_once():
     """K-split grids wait on flags raised by other CTAs of the same grid, so
     the library launches them cooperatively: a grid starts only once all its
-    CTAs fit. Here split-K, stream-K and tail-split calls, each filling most
-    of the GPU, are enqueued on three streams at once, with no ordering
-    between them, several rounds; every result is exact and no wait expires."""
+    CTAs fit. Here split-K, stream-K and zero-first stream-K calls, each
+    filling most of the GPU, are enqueued on three streams at once, with no
+    ordering between them, several rounds; every result is exact and no wait
+    expires."""
     M, N, K = 1024, 1024, 8192
     A, B = inputs.gemm_operands(M, N, K, seed=17, kind="int")
     ref = oracle.gemm_f64(A, B)
     dA, dB = upload(A), upload(B)
     cid = wgemm.config_id("g2_512x256_s4_a1_tma")
     streams = [torch.cuda.Stream() for _ in range(3)]
-    plans = [(SPLIT, 9), (STREAM, 1), (TAIL, 1)]
+    plans = [(SPLIT, 9), (STREAM, 1), (ZERO_FIRST, 1)]
     torch.cuda.synchronize()
     outs = []
     for rnd in range(4):
@@ -225,7 +229,6 @@ def test_k_split_calls_on_several_streams_at_once():
             C = torch.full((M, N), float("nan"), device="cuda")
             C.record_stream(s)
             outs.append((mode, C))
-        events = []
         for (mode, C), s, (_, sp) in zip(outs[-3:], streams, plans):
             s.wait_stream(torch.cuda.current_stream())
             rc = wgemm.wgemm_f16f32_config(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K,

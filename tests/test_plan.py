@@ -17,7 +17,7 @@ import pytest
 from dense_fp16_gemm_02_gb300 import build, wgemm
 
 KIND_STORE, KIND_RAISE, KIND_ADD_OWNER, KIND_ADD_ZERO, KIND_ADD_ZEROED = 0, 1, 2, 3, 4
-DP, SPLIT, STREAM, HYBRID, TAIL = 0, 1, 2, 3, 4
+DP, SPLIT, STREAM, HYBRID, ZERO_FIRST = 0, 1, 2, 3, 4
 
 
 @pytest.fixture(scope="module")
@@ -63,9 +63,10 @@ def test_data_parallel_covers_each_tile_once(lib, M, N, K, workers):
 
 
 def tma_configs(lib):
-    """Configurations that run split-K and stream-K (TMA epilogue, no A multicast)."""
+    """Configurations that run split-K and stream-K (TMA epilogue, no column
+    multicast; a row-multicast cluster is one worker)."""
     return [i for i, n in enumerate(wgemm.config_names())
-            if n.endswith("_tma") and not re.match(r"g\d[mr]2_", n)]
+            if n.endswith("_tma") and not re.match(r"g\dm2_", n)]
 
 
 def direct_configs(lib):
@@ -73,7 +74,8 @@ def direct_configs(lib):
 
 
 def multicast_configs(lib):
-    return [i for i, n in enumerate(wgemm.config_names()) if re.match(r"g\d[mr]2_", n)]
+    """Column-multicast clusters (groups side by side sharing A): data parallel only."""
+    return [i for i, n in enumerate(wgemm.config_names()) if re.match(r"g\dm2_", n)]
 
 
 def coverage(units, tm, tn, kb):
@@ -129,47 +131,34 @@ def test_stream_k_covers_each_kblock_once(lib, M, N, K, workers):
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-@pytest.mark.parametrize("workers", [2, 5, 76, 300])
-def test_tail_split_owners_and_tails(lib, M, N, K, workers):
-    """Owners and a tail split: worker t < tiles runs k-blocks [0, kh) of tile
-    t, kh = ceil(tiles·kb / workers); the other workers share the tails
-    [kh, kb) of all tiles, tile-major, in near-equal contiguous ranges. Every
-    (tile, k-block) once; each tile zeroed by its owner (the only zeroing
-    unit, the first and only unit of its worker, so every flag is raised at
-    the start and no unit waits on another's main loop); every worker's load
-    within one k-block of kh."""
+@pytest.mark.parametrize("workers", [1, 5, 76, 300])
+def test_stream_k_zero_first(lib, M, N, K, workers):
+    """Stream-K with zeroing first: the same units as stream-K (each
+    (tile, k-block) once, the same ranges), but the unit holding a tile's
+    first k-block zeroes the tile (kind 3, split 0) and every other part of a
+    split tile adds after the zeroing (kind 4); a whole tile is stored. Every
+    zeroing unit's flag is raised at kernel start, so no unit waits on
+    another's main loop."""
     for cfg in tma_configs(lib):
-        _, tr, tc = plan(lib, M, N, K, cfg, DP, 1, workers)
-        n = lib.wgemm_debug_plan(M, N, K, cfg, TAIL, 1, workers, None, 0, None, None)
+        units, tr, tc = plan(lib, M, N, K, cfg, ZERO_FIRST, 1, workers)
+        plain, _, _ = plan(lib, M, N, K, cfg, STREAM, 1, workers)
+        assert np.array_equal(units[:, [0, 1, 2, 3, 4, 6]], plain[:, [0, 1, 2, 3, 4, 6]])
         tm, tn = tile_grid(M, N, tr, tc)
-        tiles, kb = tm * tn, -(-K // 64)
-        if tiles >= workers:
-            assert n == -6
-            continue
-        units, _, _ = plan(lib, M, N, K, cfg, TAIL, 1, workers)
+        kb = -(-K // 64)
         hits = coverage(units, tm, tn, kb)
-        assert len(hits) == tiles * kb and set(hits.values()) == {1}
-        kh = min(kb, -(-(tiles * kb) // workers))
-        owners, tails = units[:tiles], units[tiles:]
-        assert [int(u[0]) for u in owners] == list(range(tiles))
-        assert np.all(owners[:, 3] == 0) and np.all(owners[:, 4] == kh)
-        assert np.all(owners[:, 5] == (KIND_STORE if kh == kb else KIND_ADD_ZERO))
-        assert np.all(owners[:, 6] == 0)
-        assert np.all(tails[:, 5] == KIND_ADD_ZEROED) and np.all(tails[:, 3] >= kh)
-        # Tail ranges per worker, from the definition; each worker's units are
-        # consecutive in the listing and in ascending tile order.
-        L, Q = kb - kh, workers - tiles
-        T = tiles * L
-        pos = 0
-        for q in range(Q):
-            b, e = T * q // Q, T * (q + 1) // Q
-            n_units = 0 if e <= b else (e - 1) // L - b // L + 1
-            mine = tails[pos:pos + n_units]
-            pos += n_units
-            load = int(sum(int(u[4]) - int(u[3]) for u in mine))
-            assert load == e - b and load <= kh + 1
-            assert list(mine[:, 0]) == sorted(mine[:, 0])
-        assert pos == len(tails)
+        assert len(hits) == tm * tn * kb and set(hits.values()) == {1}
+        for u in units:
+            whole = u[3] == 0 and u[4] == kb
+            if whole:
+                assert u[5] == KIND_STORE
+            elif u[3] == 0:
+                assert u[5] == KIND_ADD_ZERO and u[6] == 0
+            else:
+                assert u[5] == KIND_ADD_ZEROED
+        # Every split tile has exactly one zeroing unit.
+        split_tiles = {int(u[0]) for u in units if u[5] in (KIND_ADD_ZERO, KIND_ADD_ZEROED)}
+        zeroers = [int(u[0]) for u in units if u[5] == KIND_ADD_ZERO]
+        assert sorted(zeroers) == sorted(split_tiles)
 
 
 def simulate_stream_k(per_worker):
