@@ -318,7 +318,9 @@ def run_ours(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda:0")
     build.build()
-    wgemm.load()
+    lib = wgemm.load()
+    if args.no_cooperative:  # for Nsight Compute, which cannot profile cooperative launches
+        lib.wgemm_debug_set_cooperative(0)
     shapes = WORKLOADS[args.workload]
     reps = [args.calls or calls_per_step(*s) for s in shapes]
     stream = torch.cuda.current_stream()
@@ -347,10 +349,16 @@ def run_ours(args):
     biases = [torch.from_numpy(inputs.matrix(1, N, 2000 + i, 6, "uniform").astype(np.float32)
                                .ravel()).to(dev) for i, (M, N, K) in enumerate(shapes)]
 
+    forced = wgemm.config_id(args.config) if args.config else None
+
     def call(i):
         (M, N, K) = shapes[i]
         _, _, dA, dB, C = data[i]
-        if fused:  # D = A·Bᵀ + D + bias: the previous result read back in place
+        if forced is not None:  # a forced configuration and K decomposition
+            rc = wgemm.wgemm_gemm_config(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), ab_type,
+                                         c_type, M, N, K, K, K, N, forced, args.mode,
+                                         args.splits, h)
+        elif fused:  # D = A·Bᵀ + D + bias: the previous result read back in place
             rc = wgemm.wgemm_gemm_ex(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), C.data_ptr(),
                                      biases[i].data_ptr(), 1.0, 1.0, ab_type, c_type, M, N, K,
                                      K, K, N, N, h)
@@ -462,6 +470,10 @@ def run_ours(args):
         # also take the reduce-add kernels (fused kind 2).
         fused_kind = 0 if args.epilogue != "fused" else (2 if c_type == wgemm.WGEMM_F32 else 1)
         cfg, mode, splits = wgemm.wgemm_select(M, N, K, c_type=c_type, fused=fused_kind)
+        if forced is not None:
+            cfg = forced
+            mode = args.mode if args.mode >= 0 else mode
+            splits = args.splits
         med = float(np.median(us))
         tf = flops[i] / (med * 1e-6) / 1e12
         c_rw = (2 if args.epilogue == "fused" else 1) * c_bytes * M * N  # C written (and read)
@@ -613,6 +625,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernel-time", action="store_true",
                     help="skip the CUPTI kernel-time pass")
+    ap.add_argument("--config", metavar="NAME",
+                    help="force this kernel configuration (profiling; default: the per-shape choice)")
+    ap.add_argument("--mode", type=int, default=-1,
+                    help="with --config: K decomposition (0 data parallel, 1 split-K, 2 stream-K, "
+                         "3 waves + stream-K tail, 4 stream-K with zeroing first)")
+    ap.add_argument("--splits", type=int, default=1, help="with --config: split-K ways")
+    ap.add_argument("--no-cooperative", action="store_true",
+                    help="launch K-split grids without the cooperative attribute (for ncu, which "
+                         "runs each kernel alone and cannot profile cooperative launches)")
     ap.add_argument("--types", choices=sorted(TYPES), default="f16f32",
                     help="operand and C types (the measured product is f16f32)")
     ap.add_argument("--values", choices=["uniform", "int"], default="uniform",
@@ -626,6 +647,8 @@ def main(argv=None):
         ap.error(why)
     if args.calls < 0:
         ap.error("--calls wants a count >= 0")
+    if args.config and args.epilogue == "fused":
+        ap.error("--config forces the plain product")
     if args.shape:
         dims = tuple(int(v) for v in args.shape.lower().split("x"))
         if len(dims) != 3 or min(dims) <= 0:

@@ -17,11 +17,13 @@ both arms' results on the shape are compared on a sample of rows.
 With `--warm` the calls run the way "SASS-Level Kernel Generation for
 Blackwell" (section "How we measured") timed its own: no L2 flush and no
 gate, each call followed by a device synchronisation, per shape first
-3 + `rounds` calls of the library and then 3 + `rounds` of cuBLAS, and no
-other kernel in between (the row check is skipped). Event times then
-include the launch; kernel-only times come from an ncu launch list of the
-same command taken with `--cache-control none`, which
-`ncu_summary warm <csv> <this output>` turns into a table.
+3 + `rounds` calls of the library and then 3 + `rounds` of cuBLAS (the row
+check is skipped). Event times then include the launch. With `--cupti` as
+well, each call's GPU kernel time comes from the CUPTI recorder (a cuBLAS
+call's kernels summed; a marker kernel separates the calls), median over the
+timed calls: the pages' own measure. Without it, kernel-only times come from
+an ncu launch list of the same command taken with `--cache-control none`,
+which `ncu_summary warm <csv> <this output>` turns into a table.
 """
 from __future__ import annotations
 
@@ -40,13 +42,19 @@ def main(argv=None) -> int:
     ap.add_argument("--rounds", type=int, default=20)
     ap.add_argument("--warm", action="store_true",
                     help="warm L2, synchronised calls, arms in blocks")
+    ap.add_argument("--cupti", action="store_true",
+                    help="with --warm: also each call's kernel time from CUPTI (a cuBLAS call's "
+                         "kernels summed), the median over the timed calls")
     args = ap.parse_args(argv)
 
     import torch
     sys.path.insert(0, ROOT)
     import bench
-    from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
+    from dense_fp16_gemm_02_gb300 import build, inputs, ktime, wgemm
     from dense_fp16_gemm_02_gb300.clocks import ClockSampler
+    if args.cupti and not args.warm:
+        ap.error("--cupti goes with --warm")
+    rec = ktime.KernelTimes() if args.cupti else None
 
     build.build()
     torch.cuda.set_device(0)
@@ -102,12 +110,30 @@ def main(argv=None) -> int:
                 return e0, e1
 
             ev = {"ours": [], "ref": []}
+            kt = {"ours": [], "ref": []}
             if args.warm:
                 for arm, fn in (("ours", ours), ("ref", ref)):
+                    if rec is not None:
+                        rec.start()
                     for r in range(3 + args.rounds):
                         e = timed_warm(fn)
                         if r >= 3:
                             ev[arm].append(e)
+                        if rec is not None:  # a marker kernel after every call
+                            torch.cuda._sleep(16)
+                            torch.cuda.synchronize()
+                    if rec is not None:
+                        rec.stop()
+                        # Each call's kernels lie between two markers (the
+                        # sleep kernel); a cuBLAS call may launch several.
+                        calls, cur = [], 0.0
+                        for name, t0, t1, _ in rec.records():
+                            if "sleep" in name or "spin" in name:
+                                calls.append(cur)
+                                cur = 0.0
+                            else:
+                                cur += (t1 - t0) * 1e-3
+                        kt[arm] = calls[3:]
             else:
                 for _ in range(3):  # warm-up, both arms
                     timed(ours)
@@ -136,13 +162,25 @@ def main(argv=None) -> int:
                    "cublas_tflops": round(fl / us["ref"] / 1e6, 1),
                    "speedup": round(us["ref"] / us["ours"], 3),
                    "max_rel_diff_vs_abs_product": err}
+            if rec is not None:
+                if len(kt["ours"]) != args.rounds or len(kt["ref"]) != args.rounds:
+                    raise RuntimeError(f"CUPTI: {len(kt['ours'])} and {len(kt['ref'])} calls "
+                                       f"for {args.rounds} rounds")
+                ko, kr = statistics.median(kt["ours"]), statistics.median(kt["ref"])
+                row.update({"ours_us_kernel": round(ko, 3), "cublas_us_kernel": round(kr, 3),
+                            "ours_tflops_kernel": round(fl / ko / 1e6, 1),
+                            "cublas_tflops_kernel": round(fl / kr / 1e6, 1),
+                            "speedup_kernel": round(kr / ko, 3)})
             rows.append(row)
             print(json.dumps(row), flush=True)
             del dA, dB, Bt, C
             torch.cuda.empty_cache()
         clocks.mark_stop()
     ratios = [r["speedup"] for r in rows]
+    kratios = [r["speedup_kernel"] for r in rows if "speedup_kernel" in r]
     print(json.dumps({"summary": {
+        "geomean_speedup_kernel": (round(statistics.geometric_mean(kratios), 3) if kratios
+                                   else None),
         "workload": args.workload, "rounds": args.rounds, "cublas_output": ref_out,
         "protocol": "warm L2, synchronised calls" if args.warm else "L2 flushed, gated calls",
         "geomean_speedup": round(statistics.geometric_mean(ratios), 3),

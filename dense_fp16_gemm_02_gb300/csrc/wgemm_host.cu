@@ -120,6 +120,7 @@ DeviceState g_dev[kMaxDevices];
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 uint32_t g_debug_wait_skew = 0;  // see wgemm_debug_set_flag_wait_skew
+bool g_cooperative = true;          // see wgemm_debug_set_cooperative
 uint64_t* g_debug_trace = nullptr;  // see wgemm_debug_set_trace
 bool g_pdl = false;                 // see wgemm_set_pdl
 int g_debug_trace_ctas = 0;
@@ -640,7 +641,7 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
   cudaLaunchAttribute attr[3];
   cudaLaunchConfig_t cfg = launch_config(e, params.plan.workers, stream, attr);
   if (e.cg * e.mc * e.mr == 1) cfg.numAttrs = 0;  // no cluster: a plain launch
-  if (params.plan.mode != kDataParallel) cooperative(cfg, attr);
+  if (params.plan.mode != kDataParallel && g_cooperative) cooperative(cfg, attr);
   if (g_pdl) {
     // May start (set-up only; loads wait) while the previous kernel on the
     // stream finishes, once that kernel allows its dependents to launch.
@@ -877,6 +878,14 @@ double wgemm_debug_predict_us(int M, int N, int K, int lda, int ldb, int config_
   return predict_us(*es[config_id], M, N, K, rows_on_sectors(lda, ldb), mode, splits, workers);
 }
 
+int wgemm_debug_set_cooperative(int enable) {
+  if (enable != 0 && enable != 1) return WGEMM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  const int prev = g_cooperative ? 1 : 0;
+  g_cooperative = enable == 1;
+  return prev;
+}
+
 int wgemm_debug_set_flag_wait_skew(int skew) {
   if (skew < 0) return WGEMM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -1016,7 +1025,7 @@ int run_noalloc(const uint16_t* A, const uint16_t* B, float* C, int M, int N, in
   params.epoch = ++na->epoch;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_config(e, params.plan.workers, stream, attr);
-  cooperative(cfg, attr);
+  if (g_cooperative) cooperative(cfg, attr);
   void* args[] = {&params};
   if (cudaLaunchKernelExC(&cfg, e.func, args) != cudaSuccess) {
     cudaGetLastError();

@@ -104,6 +104,8 @@ def load():
         lib.wgemm_debug_predict_us.restype = ctypes.c_double
         lib.wgemm_debug_set_flag_wait_skew.argtypes = [i]
         lib.wgemm_debug_set_flag_wait_skew.restype = i
+        lib.wgemm_debug_set_cooperative.argtypes = [i]
+        lib.wgemm_debug_set_cooperative.restype = i
         lib.wgemm_debug_smem_desc.argtypes = [u32]
         lib.wgemm_debug_smem_desc.restype = u64
         lib.wgemm_debug_idesc.argtypes = [i, i, i]

@@ -338,6 +338,19 @@ int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16_t* B, floa
 int wgemm_debug_set_flag_wait_skew(int skew);
 
 /*
+ * Profiling hook: enable = 0 launches the split-K and stream-K grids from
+ * the next call on without the cooperative attribute, 1 (the default)
+ * restores it. Nsight Compute cannot profile a cooperative cluster launch
+ * (the launch fails with an error), but it runs every profiled kernel alone
+ * on the GPU, so all of a grid's CTAs are resident there anyway. Outside a
+ * profiler keep the default: a plain K-split launch beside another
+ * long-running kernel may start only part of its grid, whose flag waits then
+ * expire (WGEMM_ERR_DEVICE_TIMEOUT). Returns the previous setting, or
+ * WGEMM_ERR_INVALID_ARG.
+ */
+int wgemm_debug_set_cooperative(int enable);
+
+/*
  * Timeline tracing (a library built with WGEMM_TRACE=1 only; other builds
  * ignore the buffer). wgemm_debug_set_trace: from the next call on, CTA b of
  * each GEMM kernel writes %globaltimer values (ns) into

@@ -169,19 +169,29 @@ def launches_all(csv_path: str, bench_json: str) -> None:
         a[0] += 1
         a[1] += v["gpu__time_duration.sum"] / 1000.0
     total = sum(a[1] for a in agg.values())
-    bench_ms = OrderedDict()
+    # The list also holds the warm-up steps and the end-to-end passes (one
+    # call per shape each), which weigh the large shapes more than a timed
+    # step does; the weighted share puts each configuration's mean launch
+    # time on the bench's calls per step.
+    bench_ms, calls = OrderedDict(), OrderedDict()
     for s in d["shapes"]:
         bench_ms[s["config"]] = bench_ms.get(s["config"], 0.0) + s["us_median"] * s["calls"]
+        calls[s["config"]] = calls.get(s["config"], 0) + s["calls"]
     btotal = sum(bench_ms.values())
+    weighted = {cfg: us / n * calls.get(cfg, 0) for cfg, (n, us) in agg.items()}
+    wtotal = sum(weighted.values())
     rows = []
     for cfg, (n, us) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
         shapes_of = ", ".join(s["shape"] for s in d["shapes"] if s["config"] == cfg)
-        rows.append(f"| {cfg} | {shapes_of} | {n} | {us:.1f} | {100.0 * us / total:.1f} % | "
+        rows.append(f"| {cfg} | {shapes_of} | {n} | {us:.1f} | {us / n:.1f} | "
+                    f"{100.0 * us / total:.1f} % | {100.0 * weighted[cfg] / wtotal:.1f} % | "
                     f"{100.0 * bench_ms.get(cfg, 0.0) / btotal:.1f} % |")
     p = os.path.join(PROFILES, "launches_all_shapes.md")
     text = open(p).read()
-    header = ("| configuration | shapes | launches (ncu) | total µs (ncu) | share of GEMM time "
-              "(ncu) | share of the bench's timed steps (events) |\n|---|---|---|---|---|---|\n")
+    header = ("| configuration | shapes | launches (ncu) | total µs (ncu) | mean µs per launch (ncu) "
+              "| share of GEMM time (ncu) | share, weighted by the bench's calls per step (ncu) "
+              "| share of the bench's timed steps (events) |\n"
+              "|---|---|---|---|---|---|---|---|\n")
     text = _set_digest(_replace_table(text, header, rows), b.kernel_source_digest())
     open(p, "w").write(text)
     print("\n".join(rows))

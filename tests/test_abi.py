@@ -175,6 +175,15 @@ def test_configurations_name_their_c_width(lib):
             assert n[:-2] in names
 
 
+def test_cooperative_switch(lib):
+    # Host-only: the profiling hook toggles the cooperative attribute of
+    # K-split launches; the default is on.
+    assert lib.wgemm_debug_set_cooperative(2) == -1 and lib.wgemm_debug_set_cooperative(-1) == -1
+    assert lib.wgemm_debug_set_cooperative(0) == 1
+    assert lib.wgemm_debug_set_cooperative(1) == 0
+    assert lib.wgemm_debug_set_cooperative(1) == 1
+
+
 def test_pdl_switch(lib):
     assert lib.wgemm_set_pdl(2) == -1 and lib.wgemm_set_pdl(-1) == -1
     prev = lib.wgemm_set_pdl(1)

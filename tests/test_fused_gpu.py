@@ -21,6 +21,7 @@ import pytest
 import torch
 
 import oracle
+from config_names import compiled_config_names
 from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
 
 pytestmark = pytest.mark.gpu
@@ -45,13 +46,18 @@ def ceil8(k):
 
 def fused_names(width):
     """The Cin-ring fused configurations of one D width."""
-    names = [n for n in wgemm.config_names() if "_direct_ab" in n]
+    names = [n for n in compiled_config_names() if "_direct_ab" in n]
     return [n for n in names if n.endswith("_h") == (width == 16)]
 
 
 def reduce_names():
     """The reduce-add fused configurations (in place, beta = 1, fp32 D)."""
-    return [n for n in wgemm.config_names() if "_tma_ab" in n]
+    return [n for n in compiled_config_names() if "_tma_ab" in n]
+
+
+def by_width(cs):
+    """(D type, configuration) pairs: every fused configuration of each D type's width."""
+    return [(c, n) for c in cs for n in fused_names(32 if c == "f32" else 16)]
 
 
 def upload(x: np.ndarray, ab: str) -> torch.Tensor:
@@ -134,34 +140,28 @@ def epilogue_operands(M, N, kind, seed, c):
     return cin, bias, 0.75, -0.5
 
 
-@pytest.mark.parametrize("c", ["f32", "f16", "bf16"])
-@pytest.mark.parametrize("idx", range(6))
-def test_every_fused_config(idx, c):
-    names = fused_names(32 if c == "f32" else 16)
-    if idx >= len(names):
-        pytest.skip("fewer fused configurations compiled")
+@pytest.mark.parametrize("c,name", by_width(["f32", "f16", "bf16"]))
+def test_every_fused_config(c, name):
+    idx = fused_names(32 if c == "f32" else 16).index(name)
     M, N, K = 600, 1100, 300
     for ab in ("f16", "bf16"):
         for kind in ("int", "uniform"):
             A, B = inputs.gemm_operands(M, N, K, seed=40 + idx, kind=kind, lda=ceil8(K),
                                         ldb=ceil8(K), pad="nan", dtype=ab)
             cin, bias, alpha, beta = epilogue_operands(M, N, kind, 41 + idx, c)
-            D = run_fused(A, B, K, ab, c, alpha, beta, cin, bias, config=names[idx])
-            check(D, A, B, K, kind, c, alpha, beta, cin, bias, f"{names[idx]} {ab}->{c} {kind}")
+            D = run_fused(A, B, K, ab, c, alpha, beta, cin, bias, config=name)
+            check(D, A, B, K, kind, c, alpha, beta, cin, bias, f"{name} {ab}->{c} {kind}")
 
 
-@pytest.mark.parametrize("c", ["f32", "bf16"])
-@pytest.mark.parametrize("idx", range(6))
-def test_fused_multi_round_in_place(idx, c):
+@pytest.mark.parametrize("c,name", by_width(["f32", "bf16"]))
+def test_fused_multi_round_in_place(c, name):
     # More tiles than workers, ragged edges, D written over Cin.
-    names = fused_names(32 if c == "f32" else 16)
-    if idx >= len(names):
-        pytest.skip("fewer fused configurations compiled")
+    idx = fused_names(32 if c == "f32" else 16).index(name)
     M, N, K = 2600, 7000, 136
     A, B = inputs.gemm_operands(M, N, K, seed=50 + idx, kind="int", lda=ceil8(K), ldb=ceil8(K))
     cin, bias, alpha, beta = epilogue_operands(M, N, "int", 51 + idx, c)
-    D = run_fused(A, B, K, "f16", c, alpha, beta, cin, bias, config=names[idx], in_place=True)
-    check(D, A, B, K, "int", c, alpha, beta, cin, bias, f"{names[idx]} in place")
+    D = run_fused(A, B, K, "f16", c, alpha, beta, cin, bias, config=name, in_place=True)
+    check(D, A, B, K, "int", c, alpha, beta, cin, bias, f"{name} in place")
 
 
 @pytest.mark.parametrize("c", ["f32", "f16", "bf16"])
@@ -223,11 +223,9 @@ def test_fused_argument_checks():
     assert wgemm.wgemm_check(None) == 0
 
 
-@pytest.mark.parametrize("idx", range(6))
-def test_every_reduce_config_in_place(idx):
-    names = reduce_names()
-    if idx >= len(names):
-        pytest.skip("fewer reduce-add configurations compiled")
+@pytest.mark.parametrize("name", reduce_names())
+def test_every_reduce_config_in_place(name):
+    idx = reduce_names().index(name)
     M, N, K = 600, 1100, 300
     for ab in ("f16", "bf16"):
         for kind in ("int", "uniform"):
@@ -235,23 +233,21 @@ def test_every_reduce_config_in_place(idx):
                                         ldb=ceil8(K), pad="nan", dtype=ab)
             cin, bias, alpha, _ = epilogue_operands(M, N, kind, 81 + idx, "f32")
             for b in (bias, None):
-                D = run_fused(A, B, K, ab, "f32", alpha, 1.0, cin, b, config=names[idx],
+                D = run_fused(A, B, K, ab, "f32", alpha, 1.0, cin, b, config=name,
                               in_place=True)
                 check(D, A, B, K, kind, "f32", alpha, 1.0, cin, b,
-                      f"{names[idx]} {ab} {kind} bias={b is not None}")
+                      f"{name} {ab} {kind} bias={b is not None}")
 
 
-@pytest.mark.parametrize("idx", range(6))
-def test_reduce_multi_round(idx):
+@pytest.mark.parametrize("name", reduce_names())
+def test_reduce_multi_round(name):
     # More tiles than workers, ragged edges: every tile is added exactly once.
-    names = reduce_names()
-    if idx >= len(names):
-        pytest.skip("fewer reduce-add configurations compiled")
+    idx = reduce_names().index(name)
     M, N, K = 2600, 7000, 136
     A, B = inputs.gemm_operands(M, N, K, seed=90 + idx, kind="int", lda=ceil8(K), ldb=ceil8(K))
     cin, bias, alpha, _ = epilogue_operands(M, N, "int", 91 + idx, "f32")
-    D = run_fused(A, B, K, "f16", "f32", alpha, 1.0, cin, bias, config=names[idx], in_place=True)
-    check(D, A, B, K, "int", "f32", alpha, 1.0, cin, bias, f"{names[idx]} multi-round")
+    D = run_fused(A, B, K, "f16", "f32", alpha, 1.0, cin, bias, config=name, in_place=True)
+    check(D, A, B, K, "int", "f32", alpha, 1.0, cin, bias, f"{name} multi-round")
 
 
 def test_reduce_configs_only_in_place_with_unit_beta():

@@ -21,6 +21,7 @@ import pytest
 import torch
 
 import oracle
+from config_names import plain_fp32
 from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
 
 pytestmark = pytest.mark.gpu
@@ -106,34 +107,28 @@ def k_split_configs():
 
 
 @pytest.mark.parametrize("kind", ["int", "uniform"])
-@pytest.mark.parametrize("cfg", range(48))
-def test_every_config_ragged(cfg, kind):
-    names = configs()
-    if cfg >= len(names):
-        pytest.skip("fewer configurations compiled")
+@pytest.mark.parametrize("name", plain_fp32())
+def test_every_config_ragged(name, kind):
     # 3 tile rows and 3 tile columns for the largest tiles, all edges ragged,
     # K a non-multiple of the 64-wide k-block.
     M, N, K = 600, 1100, 300
-    A, B = operands(M, N, K, 100 + cfg, kind)
-    check_full(A, B, K, kind, f"{names[cfg]} {kind}", config=names[cfg], mode=DP)
+    A, B = operands(M, N, K, 100 + plain_fp32().index(name), kind)
+    check_full(A, B, K, kind, f"{name} {kind}", config=name, mode=DP)
 
 
-@pytest.mark.parametrize("cfg", range(48))
-def test_every_config_multi_round(cfg):
+@pytest.mark.parametrize("name", plain_fp32())
+def test_every_config_multi_round(name):
     # More tiles than co-resident workers for every configuration (≥ 2 tiles
     # per worker even for the 512×256 pair tile: 11 × 14 = 154 tiles over at
     # most 76 pairs), so each CTA alternates accumulators and crosses tiles;
     # ragged last tile row and column, K not a multiple of 64. Exact on
     # integer inputs; run twice to catch state left over between launches.
-    names = configs()
-    if cfg >= len(names):
-        pytest.skip("fewer configurations compiled")
     M, N, K = 2600, 7000, 136
-    A, B = operands(M, N, K, 300 + cfg, "int")
+    A, B = operands(M, N, K, 300 + plain_fp32().index(name), "int")
     ref = oracle.gemm_f64(A, B, K=K)
     for _ in range(2):
-        C = run(A, B, K, config=names[cfg], mode=DP).cpu().numpy().astype(np.float64)
-        assert_exact(C, ref, f"{names[cfg]} multi-round")
+        C = run(A, B, K, config=name, mode=DP).cpu().numpy().astype(np.float64)
+        assert_exact(C, ref, f"{name} multi-round")
 
 
 @pytest.mark.parametrize("splits", [2, 3, 7])

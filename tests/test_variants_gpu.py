@@ -17,6 +17,7 @@ import pytest
 import torch
 
 import oracle
+from config_names import plain_16bit, plain_fp32
 from dense_fp16_gemm_02_gb300 import build, inputs, wgemm
 
 pytestmark = pytest.mark.gpu
@@ -115,23 +116,20 @@ def names_by_width():
 
 # ------------------------------------------------------------------ bf16 operands, fp32 C
 
-@pytest.mark.parametrize("cfg", range(32))
-def test_bf16_inputs_every_fp32_config(cfg):
-    fp32, _ = names_by_width()
-    if cfg >= len(fp32):
-        pytest.skip("fewer configurations compiled")
+@pytest.mark.parametrize("name", plain_fp32())
+def test_bf16_inputs_every_fp32_config(name):
     M, N, K = 600, 1100, 300
     for kind in ("int", "uniform"):
-        A, B = operands(M, N, K, 500 + cfg, kind, "bf16")
-        C = run(A, B, K, "bf16", "f32", config=fp32[cfg], mode=DP)
-        check(C, A, B, K, kind, "f32", f"{fp32[cfg]} bf16 {kind}")
+        A, B = operands(M, N, K, 500 + plain_fp32().index(name), kind, "bf16")
+        C = run(A, B, K, "bf16", "f32", config=name, mode=DP)
+        check(C, A, B, K, kind, "f32", f"{name} bf16 {kind}")
 
 
 def test_bf16_inputs_split_and_stream_k():
     fp32, _ = names_by_width()
     M, N, K = 300, 520, 1000
     A, B = operands(M, N, K, 77, "int", "bf16")
-    for name in [n for n in fp32 if n.endswith("_tma") and not re.match(r"g\d[mr]2_", n)]:
+    for name in [n for n in fp32 if n.endswith("_tma") and not re.match(r"g\dm2_", n)]:
         cid = wgemm.config_id(name)
         for mode, splits in ((wgemm.MODE_SPLIT_K, 3), (wgemm.MODE_STREAM_K, 1)):
             dA, dB = upload(A, "bf16"), upload(B, "bf16")
@@ -147,34 +145,28 @@ def test_bf16_inputs_split_and_stream_k():
 # ------------------------------------------------------------------ 16-bit C
 
 @pytest.mark.parametrize("c", ["f16", "bf16"])
-@pytest.mark.parametrize("cfg", range(20))
-def test_16bit_output_every_config(cfg, c):
-    _, h = names_by_width()
-    if cfg >= len(h):
-        pytest.skip("fewer configurations compiled")
+@pytest.mark.parametrize("name", plain_16bit())
+def test_16bit_output_every_config(name, c):
     M, N, K = 600, 1100, 300
     for ab in ("f16", "bf16"):
         for kind in ("int", "uniform"):
-            A, B = operands(M, N, K, 700 + cfg, kind, ab)
-            C = run(A, B, K, ab, c, config=h[cfg], mode=DP)
-            check(C, A, B, K, kind, c, f"{h[cfg]} {ab}->{c} {kind}")
+            A, B = operands(M, N, K, 700 + plain_16bit().index(name), kind, ab)
+            C = run(A, B, K, ab, c, config=name, mode=DP)
+            check(C, A, B, K, kind, c, f"{name} {ab}->{c} {kind}")
 
 
-@pytest.mark.parametrize("cfg", range(20))
-def test_16bit_output_multi_round(cfg):
+@pytest.mark.parametrize("name", plain_16bit())
+def test_16bit_output_multi_round(name):
     # More tiles than workers, ragged edges; integer sums up to ±544 so bf16 C
     # rounds (8 significant bits): both sides round the same exact sum.
-    _, h = names_by_width()
-    if cfg >= len(h):
-        pytest.skip("fewer configurations compiled")
     M, N, K = 2600, 7000, 136
-    A, B = operands(M, N, K, 900 + cfg, "int", "bf16")
+    A, B = operands(M, N, K, 900 + plain_16bit().index(name), "int", "bf16")
     ref = oracle.round_f64(oracle.gemm_f64(A, B, K=K), "bf16")
     for _ in range(2):
-        C = run(A, B, K, "bf16", "bf16", config=h[cfg], mode=DP)
+        C = run(A, B, K, "bf16", "bf16", config=name, mode=DP)
         _, bits = host_values(C, "bf16")
         bad = np.argwhere(bits != ref)
-        assert bad.size == 0, f"{h[cfg]}: {len(bad)} mismatches, first {bad[:5].tolist()}"
+        assert bad.size == 0, f"{name}: {len(bad)} mismatches, first {bad[:5].tolist()}"
 
 
 @pytest.mark.parametrize("ab,c", [("bf16", "f32"), ("f16", "f16"), ("bf16", "bf16"),
