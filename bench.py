@@ -275,8 +275,9 @@ def single_gpu_only(args) -> str | None:
 
 def run_reference(args):
     shapes = WORKLOADS[args.workload]
-    # About 150 s of oracle work over the whole run, however many steps.
-    budget = max(0.02 * len(shapes), min(60.0, 150.0 / max(1, args.steps + args.warmup)))
+    # About 100 s of sampled oracle work over the whole run, however many
+    # steps (each call also decodes all of B, which 16384³ makes 2 GB of fp64).
+    budget = max(0.02 * len(shapes), min(60.0, 100.0 / max(1, args.steps + args.warmup)))
     ab = TYPES[args.types][0]
     for _ in range(args.warmup):
         oracle_sample_rate(shapes, budget / 4, ab=ab)
