@@ -83,9 +83,10 @@ typedef uint16_t wgemm_bf16_t;
  *      configuration that stores from registers is chosen.
  * M == 0 or N == 0: nothing to do, returns WGEMM_OK. K == 0: C := 0 (the empty
  * sum). C must not overlap A or B. The kernel configuration (tile shape, pair
- * MMA, depth, scheduler, split-K or stream-K) is chosen per shape from a
- * measured table, else by a rule. Returns WGEMM_OK once the work is enqueued,
- * else a negative WGEMM_ERR_* code (nothing enqueued).
+ * MMA, depth, scheduler, split-K) is chosen per shape from a measured table,
+ * else by a rule; stream-K runs when forced (wgemm_f16f32_config). Returns
+ * WGEMM_OK once the work is enqueued, else a negative WGEMM_ERR_* code
+ * (nothing enqueued).
  */
 int wgemm_f16f32(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C,
                  int M, int N, int K, int lda, int ldb, int ldc,
@@ -218,7 +219,7 @@ int wgemm_set_pdl(int enable);
  * fused alpha/beta/bias epilogue (direct: with an F-block Cin ring; tma_ab1:
  * the in-place reduce-add form); _h a 16-bit C.
  * Split-K and stream-K run on the static, fp32, unfused "tma" configurations
- * without m2 or r2.
+ * without m2 (an r2 cluster runs them as one worker).
  */
 int wgemm_num_configs(void);
 const char* wgemm_config_name(int config_id);
