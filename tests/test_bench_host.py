@@ -89,3 +89,18 @@ def test_peaks_and_pipe_ceiling():
         assert "burst" in src
     ceiling, what = bench.pipe_ceiling()
     assert ceiling == pytest.approx(2333.6) and "N224" in what
+
+
+def test_traffic_table_matches_the_kernel_sources():
+    """The bench reports the dominant kernel's DRAM bytes per launch from the
+    committed one-launch captures only when they were taken on the current
+    kernel sources. The table holds a row for every one of the eleven shapes
+    with the default configuration, on these sources."""
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rows = json.load(f)
+    digest = bench.kernel_source_digest()
+    shapes = {bench.shape_name(s) for s in bench.WORKLOADS["all"]}
+    assert {r["shape"] for r in rows if r["kernel_src"] == digest} == shapes
+    dominant = [r for r in rows if r["shape"] == "16384x16384x16384"][0]
+    assert bench.committed_traffic(dominant["config"], (16384, 16384, 16384)) == \
+        dominant["dram_bytes"] > 0
