@@ -235,6 +235,23 @@ def test_k_split_calls_on_several_streams_at_once():
         assert_exact(C.cpu().numpy().astype(np.float64), ref, f"mode {mode} on its own stream")
 
 
+def test_k_split_without_cooperative_launch():
+    """The profiling hook launches K-split grids plainly (for Nsight Compute,
+    which runs kernels alone); on an otherwise idle GPU the results stay
+    exact, and the default is restored."""
+    lib = wgemm.load()
+    M, N, K = 1024, 1024, 8192
+    A, B = inputs.gemm_operands(M, N, K, seed=19, kind="int")
+    ref = oracle.gemm_f64(A, B)
+    assert lib.wgemm_debug_set_cooperative(0) == 1
+    try:
+        for mode, sp in ((SPLIT, 9), (STREAM, 1), (ZERO_FIRST, 1)):
+            C = run(A, B, K, config="g2_512x256_s4_a1_tma", mode=mode, splits=sp)
+            assert_exact(C.cpu().numpy().astype(np.float64), ref, f"plain launch, mode {mode}")
+    finally:
+        assert lib.wgemm_debug_set_cooperative(1) == 0
+
+
 def test_device_timeout_is_reported_and_context_survives():
     # Failure detection without a GPU fault: the split-K waiters are told to
     # wait for a flag value that nothing writes. Their bounded waits run out

@@ -1,6 +1,6 @@
 """The measurement tools beside the bench run on the GPU and report sane
-figures: the cuBLAS comparison (the two arms agree on the contraction) and
-the copy-engine measurement."""
+figures: the bench line itself, the cuBLAS comparison (the two arms agree on
+the contraction) and the copy-engine measurement."""
 import json
 import os
 import subprocess
@@ -33,3 +33,26 @@ def test_copy_engine_rates():
     assert len(rows) == 1
     assert rows[0]["h2d_gbs"] > 1.0 and rows[0]["d2h_gbs"] > 1.0
     assert rows[0]["both_directions_gbs"] > 1.0
+
+
+def test_bench_line_has_every_key():
+    """A short bench run prints one JSON line with the keys the driver reads:
+    throughput, CUDA-event and CUPTI times per shape, the roofline, the
+    clocks, the end-to-end figure and the launch count."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "c1",
+                        "--steps", "3", "--warmup", "3", "--calls", "2", "--no-cpu-baseline"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "gpu_launches", "clocks", "shapes"):
+        assert key in line, key
+    assert line["n_gpus"] == 1 and line["value"] > 0 and line["gpu_launches"] == 3 * 2
+    s = line["shapes"][0]
+    assert s["shape"] == "1024x1024x1024" and s["calls"] == 6 and s["us_median"] > 0
+    kt = s.get("us_kernel_median")  # absent only when CUPTI is unavailable
+    assert kt is None or 0 < kt <= s["us_median"] * 2
+    assert line["roofline"]["bound"] == "tensor" and 0 < line["roofline"]["frac"] < 1.5
+    assert line["e2e"]["h2d_bytes_per_step"] == 2 * (2 * 1024 * 1024)
+
