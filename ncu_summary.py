@@ -1,6 +1,6 @@
-"""Summaries of ncu captures for profiles/: the DRAM traffic of the sweep's
-GEMM launches (with the traffic table bench.py reads) and the roofline table
-of the eleven shapes.
+"""Summaries of ncu captures for profiles/: the roofline table of the eleven
+shapes from one capture per shape (with the DRAM traffic table bench.py
+reads), the bench's launch list, and older tables of the sweep shapes.
 
     python ncu_summary.py dram DRAM_CSV
     python ncu_summary.py roofline ROOFLINE_CSV BENCH_JSON
@@ -68,25 +68,22 @@ def _set_digest(text: str, digest: str) -> str:
 
 
 def dram(csv_path: str) -> None:
+    """The DRAM table of profiles/dram_sweep.md (the six sweep shapes, one
+    launch each). profiles/traffic.json comes from `shapes`, which covers all
+    eleven shapes."""
     b = _bench()
     shapes = b.WORKLOADS["sweep"]
     by = read_ncu_csv(csv_path)
     if len(by) != len(shapes):
         raise SystemExit(f"{len(by)} launches in {csv_path}, expected {len(shapes)}")
     digest = b.kernel_source_digest()
-    rows, traffic = [], []
+    rows = []
     for (M, N, K), v in zip(shapes, by.values()):
         cfg = _config_of_kernel(v["kernel"])
         rd, wr = v["dram__bytes_read.sum"], v["dram__bytes_write.sum"]
         t = v["gpu__time_duration.sum"] / 1000.0
         rows.append(f"| {M}x{N}x{K} | {cfg} | {t:.1f} | {rd / 1e6:.1f} | {wr / 1e6:.1f} | "
                     f"{2 * (M * K + N * K) / 1e6:.1f} | {4 * M * N / 1e6:.1f} |")
-        traffic.append({"kernel_src": digest, "config": cfg, "shape": f"{M}x{N}x{K}",
-                        "dram_bytes": int(rd + wr),
-                        "source": (f"profiles/dram_sweep.md (dram__bytes_read.sum {int(rd):,} B + "
-                                   f"dram__bytes_write.sum {int(wr):,} B, one launch)")})
-    with open(os.path.join(PROFILES, "traffic.json"), "w") as f:
-        json.dump(traffic, f, indent=1)
     p = os.path.join(PROFILES, "dram_sweep.md")
     text = open(p).read()
     header = ("| shape | configuration | µs (ncu) | DRAM read MB | DRAM write MB | "
