@@ -105,3 +105,51 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm),
                 "samples_outside_region": outside}
+
+
+class EnergyCounterUnavailable(RuntimeError):
+    pass
+
+
+class EnergyCounter:
+    """The GPU's total-energy counter (NVML, millijoules since the driver
+    loaded), read only. The device is the one torch calls cuda:0, found by
+    its PCI address; where torch does not give that address, NVML must see
+    exactly one GPU."""
+
+    def __init__(self):
+        import ctypes
+
+        import torch
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError as e:
+            raise EnergyCounterUnavailable(f"NVML not found: {e}") from e
+        if nv.nvmlInit_v2() != 0:
+            raise EnergyCounterUnavailable("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(0)
+        bus = getattr(props, "pci_bus_id", None)
+        if bus is not None:
+            pci = (f"{getattr(props, 'pci_domain_id', 0):08x}:{bus:02x}:"
+                   f"{getattr(props, 'pci_device_id', 0):02x}.0")
+            rc = nv.nvmlDeviceGetHandleByPciBusId_v2(pci.encode(), ctypes.byref(handle))
+            self.device = f"PCI {pci}"
+        else:
+            count = ctypes.c_uint()
+            nv.nvmlDeviceGetCount_v2(ctypes.byref(count))
+            if count.value != 1:
+                raise EnergyCounterUnavailable(f"NVML sees {count.value} GPUs and torch gives "
+                                               "no PCI address")
+            rc = nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(handle))
+            self.device = "NVML index 0 (the only GPU)"
+        if rc != 0:
+            raise EnergyCounterUnavailable(f"no NVML handle for {self.device} (error {rc})")
+        self._nv, self._handle, self._ct = nv, handle, ctypes
+
+    def joules(self) -> float:
+        mj = self._ct.c_ulonglong()
+        rc = self._nv.nvmlDeviceGetTotalEnergyConsumption(self._handle, self._ct.byref(mj))
+        if rc != 0:
+            raise EnergyCounterUnavailable(f"nvmlDeviceGetTotalEnergyConsumption: error {rc}")
+        return mj.value / 1000.0

@@ -13,6 +13,13 @@ timed calls is kept. Split-K is tried only when the data-parallel tiles leave
 most workers idle, stream-K (with either fix-up) when they fill less than two
 waves. The emitted
 table is compiled into the library, which consults it before its shape rule.
+
+Calls of half a millisecond or more, back to back, run the GB300 into its power
+cap, and then the energy a call takes, not its time alone, sets the clock:
+a configuration that reads more from DRAM runs slower once the cap holds,
+though it ties in a lone call. For such shapes the finalists are also timed
+in blocks of consecutive flushed calls (`--sustained`, on by default), and
+that time decides.
 """
 from __future__ import annotations
 
@@ -39,6 +46,7 @@ SHAPES = {
             (4096, 4096, 1024), (4096, 4096, 4096), (8192, 2048, 4096), (8192, 8192, 8192),
             (16384, 16384, 16384), (2048, 2048, 16384), (1024, 1024, 65536)],
     "ksplit": [(2048, 2048, 16384), (1024, 1024, 65536)],
+    "large": [(8192, 8192, 8192), (16384, 16384, 16384)],
 }
 
 
@@ -115,6 +123,43 @@ def final_rounds(us):
     return max(20, min(200, int(20000.0 / max(us, 1.0))))
 
 
+# Calls at least this long run under the power cap when issued back to back
+# (8192³ and up: about 0.6 ms and more at full rate).
+SUSTAINED_US = 500.0
+SUSTAINED_BLOCK_US = 500_000.0  # GEMM time per block of consecutive calls
+SUSTAINED_ROUNDS = 3
+
+
+def time_block(wgemm, torch, bufs, M, N, K, cid, mode, splits, flush, calls):
+    """Median per-call time of `calls` consecutive flushed calls, no gate
+    between them (the GPU stays busy, as in a long run of large GEMMs); the
+    first third are left out while the clock settles."""
+    dA, dB, C = bufs
+    stream = torch.cuda.current_stream()
+    h = stream.cuda_stream
+    evs = []
+    for r in range(calls):
+        flush.fill_(float(r))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        rc = wgemm.wgemm_f16f32_config(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, K, K,
+                                       N, cid, mode, splits, h)
+        e1.record(stream)
+        if rc != 0:
+            return None
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    if wgemm.wgemm_check(h) != 0:
+        raise RuntimeError(f"device error in config {cid} mode {mode}: "
+                           f"{wgemm.wgemm_last_device_error()}")
+    return statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs[calls // 3:])
+
+
+def block_calls(us):
+    """Calls per sustained block: about SUSTAINED_BLOCK_US of GEMM time."""
+    return max(30, int(SUSTAINED_BLOCK_US / max(us, 1.0)))
+
+
 def _mid_mean(xs):
     """Mean of the middle half of xs (a quarter trimmed from each end)."""
     xs = sorted(xs)
@@ -123,7 +168,7 @@ def _mid_mean(xs):
     return sum(mid) / len(mid)
 
 
-def sweep(shapes, out_path):
+def sweep(shapes, out_path, sustained=True):
     import torch
 
     sys.path.insert(0, ROOT)
@@ -156,7 +201,10 @@ def sweep(shapes, out_path):
         # and the mean of the middle half of the rounds decides (the event
         # timer ticks near 1 µs, so a median ties at small sizes; the launch
         # phase against the tick varies, so an average resolves below it).
-        nf = finalists(rows)
+        long_calls = sustained and rows[0]["us"] >= SUSTAINED_US
+        # Under the power cap the lone-call screen orders the candidates
+        # loosely, so long calls keep more finalists.
+        nf = finalists(rows, hi=16 if long_calls else 8)
         finals = rows[:nf]
         ids = {n: i for i, n in enumerate(names)}
         per = {i: [] for i in range(len(finals))}
@@ -173,6 +221,27 @@ def sweep(shapes, out_path):
         for j, f in enumerate(finals):
             f["us_interleaved"] = round(_mid_mean(per[j]), 3)
         finals.sort(key=lambda r: r["us_interleaved"])
+        if long_calls:
+            # Blocks of consecutive calls, the finalists' blocks alternating
+            # (order reversed every round); the mean of a finalist's block
+            # medians decides.
+            calls = block_calls(rows[0]["us"])
+            blk = {j: [] for j in range(len(finals))}
+            for rnd in range(SUSTAINED_ROUNDS):
+                order = list(range(len(finals)))
+                if rnd % 2:
+                    order.reverse()
+                for j in order:
+                    f = finals[j]
+                    us = time_block(wgemm, torch, bufs, M, N, K, ids[f["config"]], f["mode"],
+                                    f["splits"], flush, calls)
+                    if us is not None:
+                        blk[j].append(us)
+            for j, f in enumerate(finals):
+                if len(blk[j]) == SUSTAINED_ROUNDS:
+                    f["us_sustained"] = round(sum(blk[j]) / len(blk[j]), 3)
+                    f["sustained_blocks_us"] = [round(v, 1) for v in blk[j]]
+            finals.sort(key=lambda r: r.get("us_sustained", float("inf")))
         rows = finals + rows[nf:]
         results.append({"shape": [M, N, K], "best": rows[0], "candidates": rows})
         print(json.dumps({"shape": [M, N, K], "best": rows[0], "next": rows[1:4]}), flush=True)
@@ -184,9 +253,14 @@ def sweep(shapes, out_path):
 
 
 def _score(c):
-    """A candidate's time in one sweep: its interleaved time if it was a
-    finalist, else its screen median."""
-    return c.get("us_interleaved", c["us"])
+    """A candidate's time in one sweep: its sustained time where the sweep
+    took one, else its interleaved time if it was a finalist, else its
+    screen median."""
+    return c.get("us_sustained", c.get("us_interleaved", c["us"]))
+
+
+def _sustained(result):
+    return any("us_sustained" in c for c in result["candidates"])
 
 
 def combine(sweeps):
@@ -195,14 +269,26 @@ def combine(sweeps):
     Sweeps on different boxes rank near-equal cluster configurations
     differently (each chip groups its SMs differently), so one box's winner
     is not taken on its own; relative times remove the boxes' overall speed.
+    Where some sweeps timed a shape's finalists sustained (back to back,
+    under the power cap) and others did not, only the sustained ones count
+    for that shape: the two regimes rank configurations differently, and
+    the sustained one is how long runs of such calls behave. Candidates
+    without a sustained time in such a sweep are left out too.
     Returns {shape: (candidate dict with "us" = mean time, relative score)}."""
+    sustained_shapes = {tuple(r["shape"]) for d in sweeps for r in d["results"]
+                        if _sustained(r)}
     per_shape = {}
     for d in sweeps:
         for r in d["results"]:
             shape = tuple(r["shape"])
-            best = min(_score(c) for c in r["candidates"])
+            cands = r["candidates"]
+            if shape in sustained_shapes:
+                cands = [c for c in cands if "us_sustained" in c]
+                if not cands:
+                    continue
+            best = min(_score(c) for c in cands)
             acc = per_shape.setdefault(shape, {})
-            for c in r["candidates"]:
+            for c in cands:
                 key = (c["config"], c["mode"], c["splits"])
                 rel, us = acc.get(key, ([], []))
                 rel.append(_score(c) / best)
@@ -236,11 +322,17 @@ def emit(json_paths, inc_path=TUNED_INC):
         f"// {boxes} on {d.get('gpu', 'a GB300')} with {d.get('sm_count')} SMs; do not edit by hand).",
         "// {M, N, K, configuration name, mode (0 data parallel, 1 split-K, 2 stream-K,",
         "//  3 data-parallel waves + stream-K tail, 4 stream-K with zeroing first),",
-        "//  splits, measured µs per call (mean over the sweeps)}",
+        "//  splits, measured µs per call (mean over the sweeps; back to back where the",
+        "//  sweeps timed the shape so)}",
     ]
     chosen = combine(sweeps)
-    for r in d["results"]:
-        M, N, K = r["shape"]
+    # Every shape any sweep timed, in the order the sweeps list them.
+    shapes = []
+    for sw in sweeps:
+        for r in sw["results"]:
+            if tuple(r["shape"]) not in shapes:
+                shapes.append(tuple(r["shape"]))
+    for (M, N, K) in shapes:
         b, _ = chosen[(M, N, K)]
         lines.append(f'{{{M}, {N}, {K}, "{b["config"]}", {b["mode"]}, {b["splits"]}, '
                      f'{b["us"]:.3f}}},')
@@ -342,12 +434,29 @@ def rates(out_path, points=RATE_POINTS, only=None):
                   indent=1)
 
 
-def emit_rates(json_paths, inc_path=RATES_INC):
+_RATE_KEYS = ("t0_us", "a_us", "b_us", "t0u_us", "au_us", "bu_us")
+
+
+def read_rates_inc(inc_path=RATES_INC):
+    """The rows of a written rates table, as `--rates` rows (by name)."""
+    rows = {}
+    with open(inc_path) as f:
+        for line in f:
+            m = re.match(r'\{"([^"]+)",((?:\s*-?[\d.]+,?){6})\},?\s*$', line.strip())
+            if m:
+                vals = [float(v) for v in m.group(2).split(",") if v.strip()]
+                rows[m.group(1)] = {"config": m.group(1), **dict(zip(_RATE_KEYS, vals))}
+    return rows
+
+
+def emit_rates(json_paths, inc_path=RATES_INC, keep=False):
     """Writes the rates table from one or more `--rates` outputs; a
-    configuration measured in a later file replaces its earlier row."""
+    configuration measured in a later file replaces its earlier row. With
+    `keep`, the table's current rows come first (a new measurement of a
+    configuration replaces its row, other rows stay)."""
     if isinstance(json_paths, str):
         json_paths = [json_paths]
-    merged, d = {}, {}
+    merged, d = (read_rates_inc(inc_path) if keep else {}), {}
     for path in json_paths:
         with open(path) as f:
             d = json.load(f)
@@ -481,13 +590,17 @@ def pdl_report(out_path, shapes=PDL_SHAPES, calls=40, rounds=8):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--out", default="tune.json")
-    ap.add_argument("--shapes", default="all")
+    ap.add_argument("--shapes", default="all", choices=sorted(SHAPES))
+    ap.add_argument("--no-sustained", action="store_true",
+                    help="skip the back-to-back timing of long calls' finalists")
     ap.add_argument("--emit", metavar="JSON", nargs="+",
                     help="write csrc/wgemm_tuned.inc from one or more sweeps (several boxes)")
     ap.add_argument("--rates", metavar="JSON", help="measure per-configuration rates")
     ap.add_argument("--emit-rates", metavar="JSON", nargs="+",
                     help="write csrc/wgemm_rates.inc (later files override earlier rows)")
     ap.add_argument("--only", metavar="REGEX", help="--rates: configurations matching REGEX")
+    ap.add_argument("--keep", action="store_true",
+                    help="--emit-rates: keep the table's rows not measured in the given files")
     ap.add_argument("--validate", metavar="JSON", help="check the rule on off-table shapes")
     ap.add_argument("--pdl-report", metavar="JSON",
                     help="back-to-back calls with programmatic dependent launch off and on")
@@ -496,7 +609,7 @@ def main(argv=None):
         print(emit(args.emit))
         return 0
     if args.emit_rates:
-        print(emit_rates(args.emit_rates))
+        print(emit_rates(args.emit_rates, keep=args.keep))
         return 0
     if args.rates:
         rates(args.rates, only=args.only)
@@ -507,7 +620,7 @@ def main(argv=None):
     if args.pdl_report:
         pdl_report(args.pdl_report)
         return 0
-    sweep(SHAPES[args.shapes], args.out)
+    sweep(SHAPES[args.shapes], args.out, sustained=not args.no_sustained)
     return 0
 
 

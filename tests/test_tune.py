@@ -76,3 +76,65 @@ def test_final_rounds_scale_with_call_time():
     assert tune.final_rounds(20.0) == 200
     assert tune.final_rounds(600.0) == 33
     assert tune.final_rounds(5000.0) == 20
+
+
+def _sus(c, sustained):
+    c = dict(c)
+    c["us_sustained"] = sustained
+    return c
+
+
+def test_sustained_time_decides_where_a_sweep_took_it(tmp_path):
+    shape = (16384, 16384, 16384)
+    # A lone-call sweep prefers X; the sustained sweep prefers Y, and X is
+    # 4 % slower back to back.
+    lone = _sweep(shape, [_c("X", 5100.0, 5100.0), _c("Y", 5200.0, 5200.0)])
+    held = _sweep(shape, [_sus(_c("Y", 5300.0, 5300.0), 5160.0),
+                          _sus(_c("X", 5150.0, 5150.0), 5370.0),
+                          _c("Z", 5000.0)])  # screened only: no sustained time, left out
+    got, score = tune.combine([lone, held])[shape]
+    assert got["config"] == "Y" and got["us"] == 5160.0 and score == 1.0
+    # Without the sustained sweep the lone-call winner stands.
+    assert tune.combine([lone])[shape][0]["config"] == "X"
+    # A shape no sweep timed back to back is combined as before.
+    other = (1024, 1024, 1024)
+    a = _sweep(other, [_c("P", 10.0, 10.0), _c("Q", 10.5, 10.5)])
+    assert tune.combine([a, held])[other][0]["config"] == "P"
+    # The table lists every shape of every sweep, in the sweeps' order.
+    paths = []
+    for i, d in enumerate((a, held)):
+        js = tmp_path / f"s{i}.json"
+        js.write_text(json.dumps(d))
+        paths.append(str(js))
+    inc = tmp_path / "t.inc"
+    tune.emit(paths, str(inc))
+    rows = [l for l in inc.read_text().splitlines() if l.startswith("{")]
+    assert rows == ['{1024, 1024, 1024, "P", 0, 1, 10.000},',
+                    '{16384, 16384, 16384, "Y", 0, 1, 5160.000},']
+
+
+def test_block_calls_cover_half_a_second():
+    assert tune.block_calls(5000.0) == 100
+    assert tune.block_calls(600.0) == 833
+    assert tune.block_calls(100000.0) == 30
+
+
+def test_rates_table_keeps_rows_not_measured_again(tmp_path):
+    inc = tmp_path / "r.inc"
+    inc.write_text('// header\n{"A", 1.000, 2.000, 0.10000, 1.500, 2.500, 0.20000},\n'
+                   '{"B", 3.000, -0.500, 0.30000, 3.500, 4.000, 0.40000},\n')
+    assert tune.read_rates_inc(str(inc))["B"]["a_us"] == -0.5
+    js = tmp_path / "new.json"
+    js.write_text(json.dumps({"gpu": "test GPU", "rates": [
+        {"config": "B", "t0_us": 5.0, "a_us": 6.0, "b_us": 0.7, "t0u_us": 5.5, "au_us": 6.5,
+         "bu_us": 0.8},
+        {"config": "C", "t0_us": 9.0, "a_us": 1.0, "b_us": 0.9, "t0u_us": 9.5, "au_us": 1.5,
+         "bu_us": 0.95}]}))
+    tune.emit_rates([str(js)], str(inc), keep=True)
+    rows = [l for l in inc.read_text().splitlines() if l.startswith("{")]
+    assert rows == ['{"A", 1.000, 2.000, 0.10000, 1.500, 2.500, 0.20000},',
+                    '{"B", 5.000, 6.000, 0.70000, 5.500, 6.500, 0.80000},',
+                    '{"C", 9.000, 1.000, 0.90000, 9.500, 1.500, 0.95000},']
+    # Without keep, only the measured rows are written.
+    tune.emit_rates([str(js)], str(inc))
+    assert len([l for l in inc.read_text().splitlines() if l.startswith("{")]) == 2
