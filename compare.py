@@ -138,6 +138,7 @@ def main(argv=None) -> int:
 
             ev = {"ours": [], "ref": []}
             kt = {"ours": [], "ref": []}
+            knames = {"ours": set(), "ref": set()}
             if args.warm:
                 for arm, fn in (("ours", ours), ("ref", ref)):
                     if rec is not None:
@@ -160,6 +161,7 @@ def main(argv=None) -> int:
                                 cur = 0.0
                             else:
                                 cur += (t1 - t0) * 1e-3
+                                knames[arm].add(name[:120])
                         kt[arm] = calls[3:]
             else:
                 for _ in range(3):  # warm-up, both arms
@@ -194,7 +196,8 @@ def main(argv=None) -> int:
                     raise RuntimeError(f"CUPTI: {len(kt['ours'])} and {len(kt['ref'])} calls "
                                        f"for {args.rounds} rounds")
                 ko, kr = statistics.median(kt["ours"]), statistics.median(kt["ref"])
-                row.update({"ours_us_kernel": round(ko, 3), "cublas_us_kernel": round(kr, 3),
+                row.update({"cublas_kernels": sorted(knames["ref"]),
+                            "ours_us_kernel": round(ko, 3), "cublas_us_kernel": round(kr, 3),
                             "ours_tflops_kernel": round(fl / ko / 1e6, 1),
                             "cublas_tflops_kernel": round(fl / kr / 1e6, 1),
                             "speedup_kernel": round(kr / ko, 3)})

@@ -8,6 +8,7 @@ reads), the bench's launch list, and older tables of the sweep shapes.
     python ncu_summary.py warm WARM_CSV COMPARE_JSONL
     python ncu_summary.py shapes CSV_DIR BENCH_JSON
     python ncu_summary.py launches-all LAUNCHES_CSV BENCH_JSON
+    python ncu_summary.py bench BENCH_JSON
 
 DRAM_CSV is the `--csv --log-file` output of the dram command in
 profiles/dram_sweep.md; ROOFLINE_CSV and BENCH_JSON are those of
@@ -15,7 +16,9 @@ profiles/roofline_all_shapes.md; LAUNCHES_CSV that of
 profiles/launches_sweep.md (every launch with gpu__time_duration.sum). The files under profiles/ are rewritten
 (their prose is kept; the tables and the kernel-source digest are replaced).
 `warm` prints the table of profiles/warm_l2_kernel_times.md from the launch
-list of `compare --warm` and that command's output.
+list of `compare --warm` and that command's output. `bench` rewrites the
+head of profiles/bench_default_all_shapes.md (result, roofline line and
+per-shape table) from the default bench line; its "Reading." stays.
 """
 from __future__ import annotations
 
@@ -357,6 +360,81 @@ def _entry_args(name: str):
             1 if m.group(11) else 0, int(m.group(10) or 0), mr)
 
 
+# The pages' B200 kernel times per call (µs; "SASS-Level Kernel Generation for
+# Blackwell", section "The numbers", the shape table): context, another chip.
+PAGES_B200_US = {
+    "1024x1024x1024": "4.64–4.67", "1536x1536x1536": "7.87", "2048x2048x2048": "14.46",
+    "3072x1280x2048": "14.08", "4096x4096x1024": "26.11", "4096x4096x4096": "75.78–75.97",
+    "8192x2048x4096": "75.84–75.97", "8192x8192x8192": "553.1–554.3",
+    "16384x16384x16384": "4132.8–4239.4", "2048x2048x16384": "73.92–74.11",
+    "1024x1024x65536": "76.93–77.22",
+}
+
+BENCH_HEADER = ("| M×N×K | configuration | mode | calls | event µs median (min–max) | "
+                "kernel µs, flushed (CUPTI) | kernel µs, warm (CUPTI) | TFLOP/s (events) | "
+                "of measured peak | of pipe ceiling | TFLOP/s (warm kernel) | "
+                "pages' B200 kernel µs (context) |\n|---|---|---|---|---|---|---|---|---|---|---|---|\n")
+
+
+def bench_profile(bench_json: str) -> None:
+    """The head of profiles/bench_default_all_shapes.md from a default bench
+    line: the command, the result, the roofline line and the per-shape table.
+    Everything from the line "Reading." on is kept."""
+    b = _bench()
+    d = _bench_line(bench_json)
+    path = os.path.join(PROFILES, "bench_default_all_shapes.md")
+    with open(path) as f:
+        old = f.read()
+    reading = old[old.index("\nReading.") + 1:] if "\nReading." in old else "Reading.\n"
+    ro, ck, e2e, cpu = d["roofline"], d["clocks"], d["e2e"], d["cpu_baseline"]
+    launches = d["gpu_launches"]
+    reasons = ck.get("reasons") or []
+    noted = (" (kept and noted: the power cap during the large shapes)"
+             if "sw_power_cap" in reasons else "")
+    rows = []
+    for r in d["shapes"]:
+        M, N, K = (int(x) for x in r["shape"].split("x"))
+        mode = r["mode"] + (f" {r['splits']}" if r["mode"] == "split-K" else "")
+        rows.append(
+            f"| {M}×{N}×{K} | {r['config']} | {mode} | {r['calls']} | "
+            f"{r['us_median']:.2f} ({r['us_min']:.2f}–{r['us_max']:.2f}) | "
+            f"{r.get('us_kernel_median', float('nan')):.2f} | "
+            f"{r.get('us_kernel_warm_median', float('nan')):.2f} | {r['tflops']} | "
+            f"{r['tensor_frac']:.3f} | {r['pipe_frac']:.3f} | "
+            f"{r.get('tflops_kernel_warm', float('nan'))} | {PAGES_B200_US.get(r['shape'], '')} |")
+    head = f"""# The default bench line: all eleven shapes, one GB300
+
+The driver's own command, on the kernel sources of digest `{b.kernel_source_digest()}` (bench.py
+`kernel_source_digest`). One step calls every shape several times, each call
+alone: an L2 flush (a 256 MiB write), a GPU-side gate, then CUDA events
+around the call. After the timed steps, CUPTI records the kernel time of 20
+flushed calls per shape and of 20 calls with a warm L2 and a device
+synchronisation after each call (the pages' protocol, "How we measured").
+
+    python bench.py                 # --steps 20 --warmup 5 by default; prints one JSON line
+    python ncu_summary.py bench bench.json   # writes this head; the reading below is prose
+
+Result: `value` {d['value']} TFLOP/s (Σ flops of a step ÷ its summed event time;
+the step is dominated by 16384³), {launches} timed launches, {d['wall_s_timed']} s timed. Clocks in
+the timed region: SM {ck['sm_mhz']} MHz median of {ck['sm_max_mhz']} ({ck['samples']} samples), reasons {reasons}{noted}. End to end (uploads of A and B,
+the calls, downloads of C, pipelined on two copy streams): {e2e['value']} TFLOP/s,
+{e2e['h2d_bytes_per_step']} B up and {e2e['d2h_bytes_per_step']} B down per step. CPU oracle: {cpu['value']:.4f} TFLOP/s on {cpu['cores']} cores
+(row-sampled).
+
+Roofline line: the dominant kernel is `{ro['kernel']}` ({ro['launches']} launches in the timed steps; its
+`traffic` is taken at {ro['traffic_shape']}),
+{ro['achieved']} TFLOP/s over its event times, {ro['frac']:.3f} of the measured cuBLAS bf16 burst rate
+({ro['peak']}), {ro['frac_vs_sustained']:.3f} of the sustained rate ({ro['peak_sustained']}), {ro['frac_vs_pipe_ceiling']:.3f} of the tcgen05 pipe ceiling
+({ro['pipe_ceiling']}, `profiles/tensor_pipe_ceiling.md`); {ro['achieved_kernel_time']} TFLOP/s from its CUPTI
+kernel times. DRAM bytes per launch (`traffic`): {ro['traffic'] if ro['traffic'] is not None else "none in this line (no capture of this kernel at that shape on these sources when it ran)"}.
+
+"""
+    text = head + BENCH_HEADER + "\n".join(rows) + "\n\n" + reading
+    with open(path, "w") as f:
+        f.write(text)
+    print(text[:len(head) + len(BENCH_HEADER)] + "\n".join(rows))
+
+
 def main(argv=None) -> int:
     argv = sys.argv[1:] if argv is None else argv
     if len(argv) >= 2 and argv[0] == "dram":
@@ -371,6 +449,8 @@ def main(argv=None) -> int:
         shapes(argv[1], argv[2])
     elif len(argv) >= 3 and argv[0] == "launches-all":
         launches_all(argv[1], argv[2])
+    elif len(argv) >= 2 and argv[0] == "bench":
+        bench_profile(argv[1])
     else:
         print(__doc__)
         return 2
