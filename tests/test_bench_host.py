@@ -104,3 +104,12 @@ def test_traffic_table_matches_the_kernel_sources():
     dominant = [r for r in rows if r["shape"] == "16384x16384x16384"][0]
     assert bench.committed_traffic(dominant["config"], (16384, 16384, 16384)) == \
         dominant["dram_bytes"] > 0
+
+
+@pytest.mark.parametrize("argv", [["--energy", "--warm"], ["--configs", "x"],
+                                  ["--cupti"]])
+def test_compare_argument_errors(argv):
+    """compare.py refuses inconsistent options before it touches a GPU."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "compare.py"), *argv],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 2 and "error" in r.stderr

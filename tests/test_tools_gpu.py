@@ -27,6 +27,23 @@ def test_compare_with_cublas_on_1024():
     assert summary["shapes"] == 1 and summary["geomean_speedup"] > 0
 
 
+def test_compare_energy_per_call():
+    """Back-to-back blocks with the NVML energy counter: the library, cuBLAS
+    and one forced configuration each report positive joules and time per
+    call at 2048³."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "compare.py"), "--shape",
+                        "2048x2048x2048", "--energy", "--rounds", "1",
+                        "--configs", "g1_128x256_s4_a2_direct"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    rows, summary = lines[:-1], lines[-1]["summary"]
+    assert [x["arm"] for x in rows] == ["library", "cublas", "g1_128x256_s4_a2_direct"]
+    for x in rows:
+        assert x["us_per_call"] > 0 and x["joules_per_call"] > 0 and x["watts"] > 0, x
+    assert summary["idle_watts"] > 0
+
+
 def test_copy_engine_rates():
     from dense_fp16_gemm_02_gb300 import peak
     rows = peak.copy_rates(sizes_mib=(8,), reps=2)
