@@ -1045,3 +1045,169 @@ extern "C" int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16
   return wg::run_noalloc(A, B, C, M, N, K, lda, ldb, ldc, splits,
                          reinterpret_cast<cudaStream_t>(stream));
 }
+
+// ---------------------------------------------------------------- host buffers
+// wgemm_f16f32_host: A and B in host memory, C returned to host memory, through
+// the caller's device buffers. B goes up whole; A goes up in row panels, each
+// panel's GEMM starts as soon as its rows have landed, and each panel of C goes
+// down as soon as it is computed, so the copies in both directions overlap the
+// GEMMs of the other panels. Uploads and downloads run on two streams of the
+// library's own (one per direction and device: the two copy directions use
+// separate copy engines); the GEMMs run on the caller's stream, which waits
+// for the last download before the call's end.
+namespace wg {
+namespace {
+
+constexpr int kMaxHostPanels = 8;
+constexpr int64_t kHostPanelBytes = 8ll << 20;  // A and C bytes per panel, at least
+int g_debug_host_panels = 0;                     // see wgemm_debug_set_host_panels
+
+struct HostCopyStreams {
+  bool init = false;
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t landed[kMaxHostPanels] = {}, computed[kMaxHostPanels] = {};
+};
+std::mutex g_host_mu;  // one host-buffer call issues at a time
+HostCopyStreams g_host[kMaxDevices];
+
+int host_streams(int dev, HostCopyStreams** out) {
+  HostCopyStreams& h = g_host[dev];
+  if (!h.init) {
+    bool ok = cudaStreamCreateWithFlags(&h.up, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&h.down, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming) == cudaSuccess;
+    for (int p = 0; ok && p < kMaxHostPanels; ++p)
+      ok = cudaEventCreateWithFlags(&h.landed[p], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&h.computed[p], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      return WGEMM_ERR_LAUNCH;
+    }
+    h.init = true;
+  }
+  *out = &h;
+  return WGEMM_OK;
+}
+
+// Panels of A's rows: as many as min(A bytes, C bytes) holds 8 MiB, 1 to 8,
+// each a multiple of 256 rows (every configuration's tile height divides it).
+// More panels overlap more of the copies with the GEMMs; the partly idle last
+// wave of each panel's tiles costs less than that gains (one call at 16384³
+// took 15.3, 11.7, 10.0 and 9.4 ms with 1, 2, 4 and 8 panels; 4096³ 0.77
+// and 0.63 ms with 1 and 8). Returns the rows per panel.
+int host_panel_rows(int M, int N, int K, int mode) {
+  int64_t p = std::min<int64_t>(2ll * M * K, 4ll * M * N) / kHostPanelBytes;
+  if (g_debug_host_panels > 0) p = g_debug_host_panels;
+  if (mode != kDataParallel) p = 1;  // a K split keeps one launch
+  p = std::max<int64_t>(1, std::min<int64_t>(p, kMaxHostPanels));
+  int rows = (int)((M + p - 1) / p);
+  rows = (rows + 255) / 256 * 256;
+  return std::min(std::max(rows, 1), M);
+}
+
+int run_host(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C, int M, int N, int K, int lda,
+             int ldb, int ldc, wgemm_f16_t* dA, wgemm_f16_t* dB, float* dC, cudaStream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return WGEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return WGEMM_OK;
+  if (!C || !dC || ldc < N) return WGEMM_ERR_INVALID_ARG;
+  if (K > 0 && (!A || !B || !dA || !dB || lda < K || ldb < K)) return WGEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dA) & 15) || (reinterpret_cast<uintptr_t>(dB) & 15) ||
+      (reinterpret_cast<uintptr_t>(dC) & 15))
+    return WGEMM_ERR_ALIGNMENT;
+  const int64_t kd = ((int64_t)K + 7) / 8 * 8, nd = ((int64_t)N + 3) / 4 * 4;
+  int config = -1, mode = -1, splits = 1;  // K == 0: the zero kernel, no configuration
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    DeviceState* st;
+    const int rc = device_state(&dev, &st);
+    if (rc != WGEMM_OK) return rc;
+    if (K > 0) {
+      const Choice c = choose(*st, M, N, K, (int)kd, (int)kd, true, 0, 0);
+      config = c.config;
+      mode = c.mode;
+      splits = c.splits;
+    }
+  }
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return WGEMM_ERR_NO_DEVICE;
+  }
+  HostCopyStreams* h;
+  int rc = host_streams(dev, &h);
+  if (rc != WGEMM_OK) return rc;
+  const int rows = K > 0 ? host_panel_rows(M, N, K, mode) : M;
+  const int panels = (M + rows - 1) / rows;
+  auto fail = [] {
+    cudaGetLastError();
+    return WGEMM_ERR_LAUNCH;
+  };
+  // Everything before the call on the caller's stream comes first (the
+  // caller's earlier use of dA, dB and dC included).
+  if (cudaEventRecord(h->start, stream) != cudaSuccess ||
+      cudaStreamWaitEvent(h->up, h->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(h->down, h->start, 0) != cudaSuccess)
+    return fail();
+  if (K > 0 && cudaMemcpy2DAsync(dB, kd * 2, B, (size_t)ldb * 2, (size_t)K * 2, N,
+                                 cudaMemcpyHostToDevice, h->up) != cudaSuccess)
+    return fail();
+  for (int p = 0; p < panels; ++p) {
+    const int r0 = p * rows, mp = std::min(rows, M - r0);
+    if (K > 0 && cudaMemcpy2DAsync(dA + r0 * kd, kd * 2, A + (int64_t)r0 * lda, (size_t)lda * 2,
+                                   (size_t)K * 2, mp, cudaMemcpyHostToDevice, h->up) != cudaSuccess)
+      return fail();
+    if (cudaEventRecord(h->landed[p], h->up) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, h->landed[p], 0) != cudaSuccess)
+      return fail();
+    // The panel is rows [r0, r0 + mp) of the same product, so the
+    // configuration chosen for the whole shape serves it.
+    rc = run(dA + r0 * kd, dB, dC + r0 * nd, WGEMM_F16, WGEMM_F32, mp, N, K, (int)kd, (int)kd,
+             (int)nd, config, mode, splits, stream);
+    if (rc != WGEMM_OK) return rc;
+    if (cudaEventRecord(h->computed[p], stream) != cudaSuccess ||
+        cudaStreamWaitEvent(h->down, h->computed[p], 0) != cudaSuccess ||
+        cudaMemcpy2DAsync(C + (int64_t)r0 * ldc, (size_t)ldc * 4, dC + r0 * nd, nd * 4,
+                          (size_t)N * 4, mp, cudaMemcpyDeviceToHost, h->down) != cudaSuccess)
+      return fail();
+  }
+  if (cudaEventRecord(h->done, h->down) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, h->done, 0) != cudaSuccess)
+    return fail();
+  return WGEMM_OK;
+}
+
+}  // namespace
+}  // namespace wg
+
+extern "C" int wgemm_f16f32_host(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C, int M,
+                                 int N, int K, int lda, int ldb, int ldc, wgemm_f16_t* dA,
+                                 wgemm_f16_t* dB, float* dC, wgemm_stream_t stream) {
+  return wg::run_host(A, B, C, M, N, K, lda, ldb, ldc, dA, dB, dC,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int wgemm_host_device_elems(int M, int N, int K, size_t* a_elems, size_t* b_elems,
+                                       size_t* c_elems) {
+  if (M < 0 || N < 0 || K < 0) return WGEMM_ERR_INVALID_ARG;
+  const size_t kd = ((size_t)K + 7) / 8 * 8, nd = ((size_t)N + 3) / 4 * 4;
+  if (a_elems) *a_elems = (size_t)M * kd;
+  if (b_elems) *b_elems = (size_t)N * kd;
+  if (c_elems) *c_elems = (size_t)M * nd;
+  return WGEMM_OK;
+}
+
+extern "C" int wgemm_debug_set_host_panels(int panels) {
+  if (panels < 0 || panels > wg::kMaxHostPanels) return WGEMM_ERR_INVALID_ARG;
+  const int prev = wg::g_debug_host_panels;
+  wg::g_debug_host_panels = panels;
+  return prev;
+}
+
+extern "C" int wgemm_debug_host_panel_rows(int M, int N, int K) {
+  if (M <= 0 || N < 0 || K <= 0) return WGEMM_ERR_INVALID_ARG;
+  return wg::host_panel_rows(M, N, K, wg::kDataParallel);
+}

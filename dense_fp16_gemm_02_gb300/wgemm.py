@@ -60,6 +60,15 @@ def load():
         lib.wgemm_f16f32_config.restype = i
         lib.wgemm_f16f32_splitk_noalloc.argtypes = [p, p, p, i, i, i, i, i, i, i, p]
         lib.wgemm_f16f32_splitk_noalloc.restype = i
+        lib.wgemm_f16f32_host.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, p]
+        lib.wgemm_f16f32_host.restype = i
+        sz = ctypes.POINTER(ctypes.c_size_t)
+        lib.wgemm_host_device_elems.argtypes = [i, i, i, sz, sz, sz]
+        lib.wgemm_host_device_elems.restype = i
+        lib.wgemm_debug_set_host_panels.argtypes = [i]
+        lib.wgemm_debug_set_host_panels.restype = i
+        lib.wgemm_debug_host_panel_rows.argtypes = [i, i, i]
+        lib.wgemm_debug_host_panel_rows.restype = i
         lib.wgemm_gemm.argtypes = [p, p, p, i, i, i, i, i, i, i, i, p]
         lib.wgemm_gemm.restype = i
         lib.wgemm_gemm_config.argtypes = [p, p, p, i, i, i, i, i, i, i, i, i, i, i, p]
@@ -229,6 +238,59 @@ def wgemm_f16f32_splitk_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, 
     """Split-K on device pointers with the library's fixed scratch array (no
     allocation); returns the status code."""
     return load().wgemm_f16f32_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, splits, stream)
+
+
+def wgemm_f16f32_host(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                      ldc: int, dA: int, dB: int, dC: int, stream: int | None) -> int:
+    """A, B and C in host memory (pinned for overlap), through the caller's
+    device buffers dA, dB, dC (sizes from host_device_elems); returns the
+    status code."""
+    return load().wgemm_f16f32_host(A, B, C, M, N, K, lda, ldb, ldc, dA, dB, dC, stream)
+
+
+def host_device_elems(M: int, N: int, K: int) -> tuple[int, int, int]:
+    """Element counts of the device buffers wgemm_f16f32_host needs:
+    (A: M·kd fp16, B: N·kd fp16, C: M·nd fp32)."""
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    rc = load().wgemm_host_device_elems(M, N, K, ctypes.byref(a), ctypes.byref(b),
+                                        ctypes.byref(c))
+    if rc != 0:
+        raise ValueError(status_string(rc))
+    return a.value, b.value, c.value
+
+
+def gemm_from_host(A, B, stream=None):
+    """C = A·Bᵀ for fp16 torch tensors in (pinned) host memory: C comes back
+    as a new pinned fp32 host tensor; the device buffers are allocated here
+    (torch) for this call. Asynchronous on `stream` (default: the current
+    one): synchronise before reading C."""
+    import torch
+
+    if A.is_cuda or B.is_cuda or A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("gemm_from_host takes fp16 host tensors")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError("A is M×K and B is N×K")
+    if A.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("rows must be contiguous")
+    M, K = A.shape
+    N = B.shape[0]
+    na, nb, nc = host_device_elems(M, N, K)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    dA = torch.empty(max(na, 1), dtype=torch.float16, device=dev)
+    dB = torch.empty(max(nb, 1), dtype=torch.float16, device=dev)
+    dC = torch.empty(max(nc, 1), dtype=torch.float32, device=dev)
+    C = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = wgemm_f16f32_host(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, A.stride(0),
+                           B.stride(0), N, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(),
+                           s.cuda_stream)
+    if rc != 0:
+        raise RuntimeError(status_string(rc))
+    # The device buffers must outlive the enqueued work.
+    dA.record_stream(s)
+    dB.record_stream(s)
+    dC.record_stream(s)
+    return C
 
 
 def wgemm_select(M: int, N: int, K: int, lda: int | None = None, ldb: int | None = None,

@@ -309,6 +309,56 @@ int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16_t* B, floa
                                 int splits, wgemm_stream_t stream);
 
 /*
+ * wgemm_f16f32_host: the same product, C = A·Bᵀ with fp16 A and B and fp32
+ * accumulation and C ("SASS-Level Kernel Generation for Blackwell", section
+ * "The numbers", the setup paragraph), with A, B and C in HOST memory: the
+ * call uploads A and B, computes, and downloads C, all asynchronously on
+ * `stream`.
+ *
+ * A (M×K, row pitch lda >= K), B (N×K, pitch ldb >= K) and C (M×N, pitch
+ * ldc >= N) are host pointers, any alignment; they should be page-locked
+ * (cudaHostAlloc or cudaHostRegister) for the copies to overlap anything,
+ * and must stay valid and untouched until `stream` reaches the call's end.
+ * dA, dB and dC are device buffers the caller owns, 16-byte aligned, of at
+ * least the element counts wgemm_host_device_elems gives: M·kd, N·kd and
+ * M·nd with kd = K rounded up to a multiple of 8 and nd = N rounded up to a
+ * multiple of 4 (the pitches the call uses on the device). Their contents
+ * on return are the device copies of A, B and C.
+ *
+ * How it runs: B goes up whole; A goes up in row panels (a multiple of 256
+ * rows each; as many as min(A bytes, C bytes) holds 8 MiB, 1 to 8, and one
+ * when the product splits K); each panel's GEMM runs on `stream` as soon as
+ * its rows have landed, with the configuration chosen for the whole shape,
+ * and each panel of C goes down as soon as it is computed. So the uploads and
+ * downloads overlap the other panels' GEMMs. The copies run on two streams
+ * the library creates per device (one per direction); they wait for
+ * everything enqueued on `stream` before the call, and `stream` waits for
+ * the last download, so work enqueued on `stream` after the call sees C in
+ * host memory. Consecutive calls on one stream therefore do not overlap;
+ * calls on different streams overlap their copies with each other's GEMMs.
+ * Calls from several host threads are serialised inside the library.
+ *
+ * Returns WGEMM_OK (also for M == 0 or N == 0, which enqueue nothing; K == 0
+ * downloads zeros), WGEMM_ERR_INVALID_ARG (negative sizes, a NULL pointer
+ * with a non-empty operand, a pitch below its row length),
+ * WGEMM_ERR_ALIGNMENT (a device buffer not 16-byte aligned), or an error of
+ * the GEMM call or WGEMM_ERR_LAUNCH from a failed copy or event; after an
+ * error, part of the work may be enqueued and C is undefined.
+ */
+int wgemm_f16f32_host(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C, int M, int N,
+                      int K, int lda, int ldb, int ldc, wgemm_f16_t* dA, wgemm_f16_t* dB,
+                      float* dC, wgemm_stream_t stream);
+
+/*
+ * Device buffer sizes for wgemm_f16f32_host, in elements: a_elems = M·kd
+ * (fp16), b_elems = N·kd (fp16), c_elems = M·nd (fp32), kd and nd as above.
+ * Any output pointer may be NULL. Host only. Returns WGEMM_OK or
+ * WGEMM_ERR_INVALID_ARG (a negative size).
+ */
+int wgemm_host_device_elems(int M, int N, int K, size_t* a_elems, size_t* b_elems,
+                            size_t* c_elems);
+
+/*
  * Host-side introspection, no GPU needed (used by the host tests).
  *
  * wgemm_debug_smem_desc: the 64-bit tcgen05 shared-memory descriptor the
@@ -350,6 +400,18 @@ int wgemm_debug_set_flag_wait_skew(int skew);
  * WGEMM_ERR_INVALID_ARG.
  */
 int wgemm_debug_set_cooperative(int enable);
+
+/*
+ * Test hook: panels > 0 makes wgemm_f16f32_host split A into that many row
+ * panels (before the rounding to 256 rows), whatever the shape's bytes; 0
+ * (the default) restores the rule. Returns the previous setting, or
+ * WGEMM_ERR_INVALID_ARG for panels outside 0..8.
+ * wgemm_debug_host_panel_rows: the rows per panel wgemm_f16f32_host uses for
+ * a data-parallel product of this shape (host only), or
+ * WGEMM_ERR_INVALID_ARG.
+ */
+int wgemm_debug_set_host_panels(int panels);
+int wgemm_debug_host_panel_rows(int M, int N, int K);
 
 /*
  * Timeline tracing (a library built with WGEMM_TRACE=1 only; other builds

@@ -259,3 +259,37 @@ def test_ncu_summary_warm_groups_launches_by_arm_and_call(tmp_path, capsys):
     assert out[0].startswith("| 64×64×64 | 10.00 | 6.00 | 0.600 |")
     assert out[1].startswith("| 128×64×64 | 11.00 | 7.00 | 0.636 |")
     assert "| 2 |" in out[0]
+
+
+def test_host_buffer_entry_without_launch(lib):
+    """wgemm_f16f32_host checks its arguments before it touches a device, and
+    the device buffer sizes and the panel rule are host arithmetic."""
+    call = wgemm.wgemm_f16f32_host
+    h, d = 4096, 4096  # stand-in addresses, never dereferenced here
+    assert call(h, h, h, -1, 4, 8, 8, 8, 4, d, d, d, None) == -1
+    assert call(h, h, h, 0, 4, 8, 8, 8, 4, d, d, d, None) == 0  # nothing to do
+    assert call(h, h, None, 4, 4, 8, 8, 8, 4, d, d, d, None) == -1  # no host C
+    assert call(h, h, h, 4, 4, 8, 8, 8, 3, d, d, d, None) == -1  # ldc < N
+    assert call(None, h, h, 4, 4, 8, 8, 8, 4, d, d, d, None) == -1  # no host A
+    assert call(h, h, h, 4, 4, 8, 8, 8, 4, d + 8, d, d, None) == -2  # device A off 16 B
+    assert call(h, h, h, 4, 4, 8, 8, 8, 4, d, d, d + 4, None) == -2  # device C off 16 B
+    # Device pitches: K up to a multiple of 8, N up to a multiple of 4.
+    assert wgemm.host_device_elems(600, 1101, 300) == (600 * 304, 1101 * 304, 600 * 1104)
+    assert wgemm.host_device_elems(0, 0, 0) == (0, 0, 0)
+    with pytest.raises(ValueError):
+        wgemm.host_device_elems(-1, 4, 4)
+    # Panels: min(A bytes, C bytes) / 8 MiB, 1 to 8, rows a multiple of 256.
+    rows = lib.wgemm_debug_host_panel_rows
+    assert rows(16384, 16384, 16384) == 2048
+    assert rows(8192, 8192, 8192) == 1024
+    assert rows(4096, 4096, 4096) == 1024  # A is 32 MiB: four panels
+    assert rows(2048, 2048, 2048) == 2048  # A is 8 MiB: one panel
+    assert rows(1024, 1024, 65536) == 1024  # C is 4 MiB: one panel
+    assert rows(600, 1100, 300) == 600
+    assert rows(0, 4, 4) == -1
+    prev = lib.wgemm_debug_set_host_panels(3)
+    try:
+        assert rows(1000, 777, 520) == 512  # ceil(1000 / 3) rounded up to 256
+    finally:
+        lib.wgemm_debug_set_host_panels(prev)
+    assert lib.wgemm_debug_set_host_panels(9) == -1
