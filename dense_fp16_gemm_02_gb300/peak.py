@@ -49,12 +49,31 @@ def copy_rates(sizes_mib=(32, 128, 256), reps=10):
     dev = torch.device("cuda")
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     out = []
+
+    def on_two(first, second):
+        """Run two copies at once, one per stream, after the current stream's work."""
+        cur = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(cur)
+        s1.wait_event(start)
+        s2.wait_event(start)
+        with torch.cuda.stream(s1):
+            first()
+        with torch.cuda.stream(s2):
+            second()
+        for s in (s1, s2):
+            e = torch.cuda.Event()
+            e.record(s)
+            cur.wait_event(e)
+
     for mib in sizes_mib:
         n = mib << 20
         h_in = torch.empty(n, dtype=torch.uint8).pin_memory()
         h_out = torch.empty(n, dtype=torch.uint8).pin_memory()
         d_in = torch.empty(n, dtype=torch.uint8, device=dev)
         d_out = torch.empty(n, dtype=torch.uint8, device=dev)
+        d_in2 = torch.empty(n, dtype=torch.uint8, device=dev)
+        h_out2 = torch.empty(n, dtype=torch.uint8).pin_memory()
 
         def timed(fn):
             ts = []
@@ -71,25 +90,24 @@ def copy_rates(sizes_mib=(32, 128, 256), reps=10):
             return ts[len(ts) // 2] * 1e-3  # s
 
         def both():
-            cur = torch.cuda.current_stream()
-            start = torch.cuda.Event()
-            start.record(cur)
-            s1.wait_event(start)
-            s2.wait_event(start)
-            with torch.cuda.stream(s1):
-                d_in.copy_(h_in, non_blocking=True)
-            with torch.cuda.stream(s2):
-                h_out.copy_(d_out, non_blocking=True)
-            for s in (s1, s2):
-                e = torch.cuda.Event()
-                e.record(s)
-                cur.wait_event(e)
+            on_two(lambda: d_in.copy_(h_in, non_blocking=True),
+                   lambda: h_out.copy_(d_out, non_blocking=True))
+
+        def two_up():  # two uploads at once: more copy engines, the same link
+            on_two(lambda: d_in.copy_(h_in, non_blocking=True),
+                   lambda: d_in2.copy_(h_out, non_blocking=True))
+
+        def two_down():
+            on_two(lambda: h_out.copy_(d_out, non_blocking=True),
+                   lambda: h_out2.copy_(d_in, non_blocking=True))
 
         out.append({
             "mib": mib,
             "h2d_gbs": round(n / timed(lambda: d_in.copy_(h_in, non_blocking=True)) / 1e9, 1),
             "d2h_gbs": round(n / timed(lambda: h_out.copy_(d_out, non_blocking=True)) / 1e9, 1),
             "both_directions_gbs": round(2 * n / timed(both) / 1e9, 1),
+            "h2d_two_streams_gbs": round(2 * n / timed(two_up) / 1e9, 1),
+            "d2h_two_streams_gbs": round(2 * n / timed(two_down) / 1e9, 1),
         })
     return out
 

@@ -50,6 +50,7 @@ def test_copy_engine_rates():
     assert len(rows) == 1
     assert rows[0]["h2d_gbs"] > 1.0 and rows[0]["d2h_gbs"] > 1.0
     assert rows[0]["both_directions_gbs"] > 1.0
+    assert rows[0]["h2d_two_streams_gbs"] > 1.0 and rows[0]["d2h_two_streams_gbs"] > 1.0
 
 
 def test_bench_line_has_every_key():
