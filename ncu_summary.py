@@ -416,8 +416,8 @@ synchronisation after each call (the pages' protocol, "How we measured").
 
 Result: `value` {d['value']} TFLOP/s (Σ flops of a step ÷ its summed event time;
 the step is dominated by 16384³), {launches} timed launches, {d['wall_s_timed']} s timed. Clocks in
-the timed region: SM {ck['sm_mhz']} MHz median of {ck['sm_max_mhz']} ({ck['samples']} samples), reasons {reasons}{noted}. End to end (uploads of A and B,
-the calls, downloads of C, pipelined on two copy streams): {e2e['value']} TFLOP/s,
+the timed region: SM {ck['sm_mhz']} MHz median of {ck['sm_max_mhz']} ({ck['samples']} samples), reasons {reasons}{noted}. End to end
+({d['timing']['e2e']}): {e2e['value']} TFLOP/s,
 {e2e['h2d_bytes_per_step']} B up and {e2e['d2h_bytes_per_step']} B down per step. CPU oracle: {cpu['value']:.4f} TFLOP/s on {cpu['cores']} cores
 (row-sampled).
 
