@@ -1142,42 +1142,50 @@ int run_host(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C, int M, int N,
   if (rc != WGEMM_OK) return rc;
   const int rows = K > 0 ? host_panel_rows(M, N, K, mode) : M;
   const int panels = (M + rows - 1) / rows;
-  auto fail = [] {
-    cudaGetLastError();
-    return WGEMM_ERR_LAUNCH;
-  };
   // Everything before the call on the caller's stream comes first (the
   // caller's earlier use of dA, dB and dC included).
   if (cudaEventRecord(h->start, stream) != cudaSuccess ||
       cudaStreamWaitEvent(h->up, h->start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(h->down, h->start, 0) != cudaSuccess)
-    return fail();
+      cudaStreamWaitEvent(h->down, h->start, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return WGEMM_ERR_LAUNCH;
+  }
+  rc = WGEMM_OK;
   if (K > 0 && cudaMemcpy2DAsync(dB, kd * 2, B, (size_t)ldb * 2, (size_t)K * 2, N,
                                  cudaMemcpyHostToDevice, h->up) != cudaSuccess)
-    return fail();
-  for (int p = 0; p < panels; ++p) {
+    rc = WGEMM_ERR_LAUNCH;
+  for (int p = 0; p < panels && rc == WGEMM_OK; ++p) {
     const int r0 = p * rows, mp = std::min(rows, M - r0);
-    if (K > 0 && cudaMemcpy2DAsync(dA + r0 * kd, kd * 2, A + (int64_t)r0 * lda, (size_t)lda * 2,
-                                   (size_t)K * 2, mp, cudaMemcpyHostToDevice, h->up) != cudaSuccess)
-      return fail();
-    if (cudaEventRecord(h->landed[p], h->up) != cudaSuccess ||
-        cudaStreamWaitEvent(stream, h->landed[p], 0) != cudaSuccess)
-      return fail();
+    if ((K > 0 && cudaMemcpy2DAsync(dA + r0 * kd, kd * 2, A + (int64_t)r0 * lda,
+                                    (size_t)lda * 2, (size_t)K * 2, mp, cudaMemcpyHostToDevice,
+                                    h->up) != cudaSuccess) ||
+        cudaEventRecord(h->landed[p], h->up) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, h->landed[p], 0) != cudaSuccess) {
+      rc = WGEMM_ERR_LAUNCH;
+      break;
+    }
     // The panel is rows [r0, r0 + mp) of the same product, so the
     // configuration chosen for the whole shape serves it.
     rc = run(dA + r0 * kd, dB, dC + r0 * nd, WGEMM_F16, WGEMM_F32, mp, N, K, (int)kd, (int)kd,
              (int)nd, config, mode, splits, stream);
-    if (rc != WGEMM_OK) return rc;
+    if (rc != WGEMM_OK) break;
     if (cudaEventRecord(h->computed[p], stream) != cudaSuccess ||
         cudaStreamWaitEvent(h->down, h->computed[p], 0) != cudaSuccess ||
         cudaMemcpy2DAsync(C + (int64_t)r0 * ldc, (size_t)ldc * 4, dC + r0 * nd, nd * 4,
                           (size_t)N * 4, mp, cudaMemcpyDeviceToHost, h->down) != cudaSuccess)
-      return fail();
+      rc = WGEMM_ERR_LAUNCH;
   }
+  if (rc != WGEMM_OK) cudaGetLastError();
+  // The caller's stream waits for both copy streams, also after an error,
+  // so that synchronising it covers every copy this call enqueued.
   if (cudaEventRecord(h->done, h->down) != cudaSuccess ||
-      cudaStreamWaitEvent(stream, h->done, 0) != cudaSuccess)
-    return fail();
-  return WGEMM_OK;
+      cudaStreamWaitEvent(stream, h->done, 0) != cudaSuccess ||
+      cudaEventRecord(h->done, h->up) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, h->done, 0) != cudaSuccess) {
+    cudaGetLastError();
+    if (rc == WGEMM_OK) rc = WGEMM_ERR_LAUNCH;
+  }
+  return rc;
 }
 
 }  // namespace

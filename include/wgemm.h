@@ -342,8 +342,10 @@ int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16_t* B, floa
  * downloads zeros), WGEMM_ERR_INVALID_ARG (negative sizes, a NULL pointer
  * with a non-empty operand, a pitch below its row length),
  * WGEMM_ERR_ALIGNMENT (a device buffer not 16-byte aligned), or an error of
- * the GEMM call or WGEMM_ERR_LAUNCH from a failed copy or event; after an
- * error, part of the work may be enqueued and C is undefined.
+ * the GEMM call or WGEMM_ERR_LAUNCH from a failed copy or event. After an
+ * error part of the work may be enqueued and C is undefined, but `stream`
+ * still waits for every copy the call enqueued, so synchronising it is
+ * enough before the buffers are freed.
  */
 int wgemm_f16f32_host(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C, int M, int N,
                       int K, int lda, int ldb, int ldc, wgemm_f16_t* dA, wgemm_f16_t* dB,

@@ -135,3 +135,14 @@ def test_host_buffer_argument_errors(lib):
                 z.data_ptr(), z.data_ptr(), s) == -1  # lda < K
     assert call(h.data_ptr(), h.data_ptr(), c.data_ptr(), 4, 4, 8, 8, 8, 4, z.data_ptr() + 2,
                 z.data_ptr(), z.data_ptr(), s) == -2  # device A off 16 bytes
+
+
+def test_host_buffers_split_k_shape(lib):
+    # The table runs 1024×1024×65536 as split-K 9: through the host call it
+    # stays one launch (one panel), with the K split, exact on integers.
+    M, N, K = 1024, 1024, 65536
+    assert wgemm.wgemm_select(M, N, K)[1] == 1  # split-K
+    A, B = inputs.gemm_operands(M, N, K, seed=44, kind="int")
+    rc, hC, keep, s = host_call(A, B, M, N, K, K, K, N)
+    finish(rc, s)
+    check(hC, A, B, M, N, K, "int", "split-K shape through the host call")
