@@ -373,9 +373,26 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
   // Stream-K is not chosen here. Its model assumes the data-parallel k-loop
   // rate, but stream-K's ranges start at scattered k offsets, and measured
   // k-loops run 12-35% slower than that; split-K's units stay in step.
+  // Calls predicted at kLongCallUs or more run under the power cap when they
+  // come back to back, and there the lone-call rates mislead. The 512-column
+  // tiles with cluster launch control read the fewest operand bytes per flop
+  // and hand out tiles in serpentine order, which keeps the tiles in flight
+  // adjacent and cuts DRAM reads (16384³: 7.9 against 17.9 GB per call for
+  // the 256×256 static tile), so they spend less energy per call and run at
+  // a higher clock. Back to back (blocks of consecutive calls) the 512×256
+  // CLC tile beat the rule's lone-call choice by 2–5 % at 12288³ and
+  // 8192×8192×16384, and the 256×256 static tile by 9 % at 16384³; the
+  // 256-column CLC tiles did not (12288³: 2299 against 2260 µs). The rates,
+  // fitted on calls of up to 4 waves and K = 4096, put the 512×256 CLC tile
+  // 14–22 % behind there; at 12288³ they predict 1750 µs for the static
+  // choice, which took 2260–2323 µs back to back. So for such calls the best
+  // 512-column CLC configuration is taken when its prediction is within 30 %
+  // of the best and the shape gives it at least two waves of tiles.
+  constexpr double kLongCallUs = 500.0, kClcMargin = 1.30;
   const auto& es = registry().entries;
-  Choice best{-1, kDataParallel, 1}, best_split{-1, kDataParallel, 1};
-  double best_us = 0.0, best_split_us = 0.0;
+  Choice best{-1, kDataParallel, 1}, best_split{-1, kDataParallel, 1},
+      best_clc{-1, kDataParallel, 1};
+  double best_us = 0.0, best_split_us = 0.0, best_clc_us = 0.0;
   for (int id = 0; id < (int)es.size(); ++id) {
     const KernelEntry& e = *es[id];
     if (e.out != out || !fuse_fits(e, fuse) || (e.epi == kEpiTma && !c_tma_ok)) continue;
@@ -388,6 +405,13 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
       if (us >= 0.0 && (c.config < 0 || us < c_us)) {
         c = {id, mode, splits};
         c_us = us;
+      }
+      const int64_t clc_tiles = (int64_t)((M + e.tile_rows - 1) / e.tile_rows) *
+                                ((N + e.tile_cols - 1) / e.tile_cols);
+      if (mode == kDataParallel && e.sched == 1 && e.tile_cols >= 512 && us >= 0.0 &&
+          clc_tiles >= 2 * (int64_t)w && (best_clc.config < 0 || us < best_clc_us)) {
+        best_clc = {id, mode, splits};
+        best_clc_us = us;
       }
     };
     consider(kDataParallel, 1);
@@ -402,6 +426,9 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
   }
   if (best_split.config >= 0 && (best.config < 0 || best_split_us < 0.9 * best_us))
     return best_split;
+  if (best.config >= 0 && best_us >= kLongCallUs && best_clc.config >= 0 &&
+      best_clc_us <= kClcMargin * best_us)
+    return best_clc;
   if (best.config >= 0) return best;
   // No rates compiled in: a plain fallback.
   if (fuse) {

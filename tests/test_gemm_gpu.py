@@ -478,6 +478,23 @@ def test_rule_k_split_choices():
         assert wgemm.wgemm_select(M, N, K, pitch, pitch)[1] in (DP, SPLIT)
 
 
+def test_rule_long_calls_take_cluster_launch_control():
+    """Off-table calls predicted at 0.5 ms or more take the 512-column
+    cluster-launch-control tile (back to back, under the power cap, it ran
+    2-5 % faster than the rule's lone-call choice at 12288³ and
+    8192×8192×16384); shorter ones keep the lone-call rule."""
+    names = wgemm.config_names()
+    for M, N, K in ((12288, 12288, 12288), (8192, 8192, 16384), (16384, 16384, 8192)):
+        cid, mode, splits = wgemm.wgemm_select(M, N, K)
+        assert mode == DP and names[cid] == "g2_512x256_s4_a1_tma_clc", (M, N, K, names[cid])
+    cid, mode, _ = wgemm.wgemm_select(12288, 12288, 12288)
+    A, B = inputs.gemm_operands(12288, 12288, 12288, seed=3100, kind="int")
+    C = run(A, B, 12288)
+    check_sampled(A, B, C, 12288, 12288, 12288, "int", 32, 93, f"12288³ via {names[cid]}")
+    del C
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("M,N,K,pitch", OFF_TABLE)
 def test_off_table_rule_sampled(M, N, K, pitch):
     cid, mode, splits = wgemm.wgemm_select(M, N, K, pitch, pitch)
