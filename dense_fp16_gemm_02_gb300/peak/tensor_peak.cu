@@ -184,6 +184,9 @@ int main(int argc, char** argv) {
   measure<2, 256, 2>("pair M256 N256, 2 atoms", src, sms, iters / 2, 4);
   measure<1, 256, 1>("single M128 N256", src, sms, iters, 4);
   measure<1, 128, 1>("single M128 N128", src, sms, iters, 4);
+  // The small shapes' tiles: N = 64 per MMA.
+  measure<1, 64, 1>("single M128 N64", src, sms, iters, 4);
+  measure<2, 64, 1>("pair M256 N64", src, sms, iters, 4);
   CHECK(cudaFree(src));
   return 0;
 }
