@@ -15,6 +15,7 @@ const KernelEntry kEntriesPair[] = {
     WG_ENTRY("g2_256x160_s8_a2_direct", 2, 1, 160, 8, 2, kEpiDirect),
     WG_ENTRY("g2_256x128_s8_a2_tma", 2, 1, 128, 8, 2, kEpiTma),
     WG_ENTRY("g2_256x64_s10_a2_direct", 2, 1, 64, 10, 2, kEpiDirect),
+    WG_ENTRY_X2("g2_256x64_s5x2_a2_direct", 2, 1, 64, 5, 2, kEpiDirect, 1),
 };
 const int kNumEntriesPair = sizeof(kEntriesPair) / sizeof(kEntriesPair[0]);
 

@@ -12,6 +12,8 @@ namespace wg {
 const KernelEntry kEntriesRowMc[] = {
     WG_ENTRY_MR("g1r2_128x128_s8_a2_direct", 1, 1, 64, 8, 2, kEpiDirect, 2, kSchedStatic),
     WG_ENTRY_MR("g1r2_128x256_s6_a2_direct", 1, 1, 128, 6, 2, kEpiDirect, 2, kSchedStatic),
+    WG_ENTRY_X2("g1r2_128x256_s3x2_a2_direct", 1, 1, 128, 3, 2, kEpiDirect, 2),
+    WG_ENTRY_X2("g1r2_128x128_s4x2_a2_direct", 1, 1, 64, 4, 2, kEpiDirect, 2),
     WG_ENTRY_MR("g2r2_256x128_s10_a2_direct", 2, 1, 64, 10, 2, kEpiDirect, 2, kSchedStatic),
     WG_ENTRY_MR("g2r2_256x256_s8_a2_direct", 2, 1, 128, 8, 2, kEpiDirect, 2, kSchedStatic),
     WG_ENTRY_MR("g2r2_256x384_s7_a2_direct", 2, 1, 192, 7, 2, kEpiDirect, 2, kSchedStatic),

@@ -45,21 +45,25 @@ extern const int kNumEntriesRowMc;
 // kernel template). MC = MMA groups per cluster side by side along C's
 // columns (sharing the A tile), MR = groups stacked along C's rows (sharing
 // the B tile); SCHED = kSchedStatic or kSchedClc; OUT = kOut32 or kOut16;
-// FUSE = 0 or the Cin ring depth.
-#define WG_ENTRY_GEN(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR)                \
+// FUSE = 0 or the Cin ring depth; KPS = k-blocks per stage (1 or 2).
+#define WG_ENTRY_GEN(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR, KPS)           \
   wg::KernelEntry {                                                                                 \
     NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, MR, SCHED,                                            \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR>::kTileRows,               \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR>::kTileCols, OUT, FUSE,    \
-        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR>::kSmemBytes,              \
-        reinterpret_cast<const void*>(                                                              \
-            &wg::wgemm_kernel<wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR>>)   \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR, KPS>::kTileRows,          \
+        wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR, KPS>::kTileCols, OUT,     \
+        FUSE, wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR, KPS>::kSmemBytes,   \
+        reinterpret_cast<const void*>(&wg::wgemm_kernel<                                            \
+                                      wg::Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, \
+                                              MR, KPS>>)                                            \
   }
 #define WG_ENTRY_ANY(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE) \
-  WG_ENTRY_GEN(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, 1)
+  WG_ENTRY_GEN(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, 1, 1)
 // MR groups stacked along C's rows sharing the B tile (fp32 C).
 #define WG_ENTRY_MR(NAME, CG, REPS, BN, STAGES, ACC, EPI, MR, SCHED) \
-  WG_ENTRY_GEN(NAME, CG, REPS, BN, STAGES, ACC, EPI, 1, SCHED, wg::kOut32, 0, MR)
+  WG_ENTRY_GEN(NAME, CG, REPS, BN, STAGES, ACC, EPI, 1, SCHED, wg::kOut32, 0, MR, 1)
+// Stages of two k-blocks ("_s<STAGES>x2_"), fp32 C, static schedule.
+#define WG_ENTRY_X2(NAME, CG, REPS, BN, STAGES, ACC, EPI, MR) \
+  WG_ENTRY_GEN(NAME, CG, REPS, BN, STAGES, ACC, EPI, 1, wg::kSchedStatic, wg::kOut32, 0, MR, 2)
 #define WG_ENTRY_OUT(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT) \
   WG_ENTRY_ANY(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, 0)
 #define WG_ENTRY_FULL(NAME, CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED) \

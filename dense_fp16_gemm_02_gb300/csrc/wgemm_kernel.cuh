@@ -143,7 +143,7 @@ enum SchedMode : int { kSchedStatic = 0, kSchedClc = 1 };
 enum OutWidth : int { kOut32 = 0, kOut16 = 1 };
 
 template <int CG_, int REPS_, int BN_, int STAGES_, int ACC_, int EPI_, int MC_ = 1,
-          int SCHED_ = kSchedStatic, int OUT_ = kOut32, int FUSE_ = 0, int MR_ = 1>
+          int SCHED_ = kSchedStatic, int OUT_ = kOut32, int FUSE_ = 0, int MR_ = 1, int KPS_ = 1>
 struct Cfg {
   static constexpr int OUT = OUT_;        // OutWidth: fp32 C, or 16-bit C (data parallel only)
   // FUSE > 0: alpha/beta/bias epilogue (data parallel only). With register
@@ -158,6 +158,10 @@ struct Cfg {
   static constexpr int REPS = REPS_;      // stacked MMA atoms per CTA (C columns 128·REPS)
   static constexpr int BN = BN_;          // MMA N = C rows of a tile
   static constexpr int STAGES = STAGES_;  // ring depth
+  // k-blocks per stage (1 or 2). With two, a stage's barrier hand-off and
+  // MMA commit serve eight MMAs instead of four: where the MMA thread, not
+  // the tensor pipe, sets the k-loop's pace (small N), that pace rises.
+  static constexpr int KPS = KPS_;
   static constexpr int ACC = ACC_;        // TMEM accumulators
   static constexpr int EPI = EPI_;        // EpilogueMode
 
@@ -178,7 +182,8 @@ struct Cfg {
   static constexpr int kArowsPart = kArows / MR;
   static constexpr uint32_t kAbytes = kArows * 128;
   static constexpr uint32_t kBbytes = kBrows * 128;
-  static constexpr uint32_t kStageBytes = kAbytes + kBbytes;
+  static constexpr uint32_t kKbBytes = kAbytes + kBbytes;  // one k-block of both operands
+  static constexpr uint32_t kStageBytes = KPS * kKbBytes;   // k-block q at q · kKbBytes
   static constexpr uint32_t kAccCols = REPS * BN;   // TMEM columns per accumulator
   static constexpr uint32_t kTmemCols = pow2_at_least_32(kAccCols * ACC);
   static constexpr uint32_t kCBytes = OUT == kOut16 ? 2 : 4;  // bytes per C element
@@ -243,7 +248,8 @@ struct Cfg {
   static_assert(kBrows % 8 == 0, "operand rows in 8-row groups");
   static_assert(kAccCols * ACC <= 512, "TMEM capacity");
   static_assert(kSmemBytes <= 232448, "shared memory");
-  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static_assert(kKbBytes % 1024 == 0, "stage and k-block alignment");
+  static_assert(KPS == 1 || KPS == 2, "KPS");
 };
 
 // An fp32 accumulator value (its bits) rounded to the 16-bit C type, to
@@ -496,26 +502,27 @@ struct Kernel {
     return (uint16_t)(((1u << K::CG) - 1u) << (grp * K::CG));
   }
 
-  // Loads k-block `kb` of a unit into stage s and accounts its bytes.
-  __device__ static void load_stage(const KParams& p, uint32_t base, uint32_t s, int32_t kb,
-                                    int32_t b_row0, int32_t a_row0, uint32_t rank, uint32_t grp) {
+  // Loads k-block `kb` of a unit into k-block slot q of stage s (the stage's
+  // bytes are accounted once, by load_stage).
+  __device__ static void load_kb(const KParams& p, uint32_t base, uint32_t s, uint32_t q,
+                                 int32_t kb, int32_t b_row0, int32_t a_row0, uint32_t rank,
+                                 uint32_t grp) {
     const uint32_t full = bar_full(base, s);
-    const uint32_t a_dst = stage_b(base, s) + grp * K::kBrowsPart * 128;
+    const uint32_t sa = stage_a(base, s) + q * K::kKbBytes, sb = sa + K::kAbytes;
+    const uint32_t a_dst = sb + grp * K::kBrowsPart * 128;
     if constexpr (K::MR > 1) {
       // Part grp of the B slice goes to this rank of every group; the A rows
       // are this CTA's own. b_row0 is the slice's first row.
-      const uint32_t b_dst = stage_a(base, s) + grp * K::kArowsPart * 128;
+      const uint32_t b_dst = sa + grp * K::kArowsPart * 128;
       const int32_t b_part = b_row0 + (int32_t)grp * K::kArowsPart;
       if constexpr (K::CG == 1) {
-        mbar_arrive_expect_tx(full, K::kStageBytes);
         tma_load_2d_multicast(b_dst, &p.tmB, full, kb * kBK, b_part, same_rank_mask(rank));
-        tma_load_2d(stage_b(base, s), &p.tmA, full, kb * kBK, a_row0);
+        tma_load_2d(sb, &p.tmA, full, kb * kBK, a_row0);
       } else {
-        if (rank == 0) mbar_arrive_expect_tx(full, 2 * K::kStageBytes);
         const uint32_t full_leader = mapa_shared(full, group_leader(grp));
         tma_load_2d_pair_multicast(b_dst, &p.tmB, full_leader, kb * kBK, b_part,
                                    same_rank_mask(rank));
-        tma_load_2d_pair(stage_b(base, s), &p.tmA, full_leader, kb * kBK, a_row0);
+        tma_load_2d_pair(sb, &p.tmA, full_leader, kb * kBK, a_row0);
       }
       return;
     }
@@ -526,21 +533,18 @@ struct Kernel {
       if (p.plan.mode != kDataParallel) {
         const uint64_t pol = l2_policy_evict_first();
         if constexpr (K::CG == 1) {
-          mbar_arrive_expect_tx(full, K::kStageBytes);
-          tma_load_2d_hint(stage_a(base, s), &p.tmB, full, kb * kBK, b_row0, pol);
+          tma_load_2d_hint(sa, &p.tmB, full, kb * kBK, b_row0, pol);
           tma_load_2d_hint(a_dst, &p.tmA, full, kb * kBK, a_row0, pol);
         } else {
-          if (rank == 0) mbar_arrive_expect_tx(full, 2 * K::kStageBytes);
           const uint32_t full_leader = mapa_shared(full, group_leader(grp));
-          tma_load_2d_pair_hint(stage_a(base, s), &p.tmB, full_leader, kb * kBK, b_row0, pol);
+          tma_load_2d_pair_hint(sa, &p.tmB, full_leader, kb * kBK, b_row0, pol);
           tma_load_2d_pair_hint(a_dst, &p.tmA, full_leader, kb * kBK, a_row0, pol);
         }
         return;
       }
     }
     if constexpr (K::CG == 1) {
-      mbar_arrive_expect_tx(full, K::kStageBytes);
-      tma_load_2d(stage_a(base, s), &p.tmB, full, kb * kBK, b_row0);
+      tma_load_2d(sa, &p.tmB, full, kb * kBK, b_row0);
       if constexpr (K::MC == 1)
         tma_load_2d(a_dst, &p.tmA, full, kb * kBK, a_row0);
       else
@@ -548,15 +552,27 @@ struct Kernel {
     } else {
       // Every byte that lands in either CTA of a pair is counted on the
       // pair leader's full barrier.
-      if (rank == 0) mbar_arrive_expect_tx(full, 2 * K::kStageBytes);
       const uint32_t full_leader = mapa_shared(full, group_leader(grp));
-      tma_load_2d_pair(stage_a(base, s), &p.tmB, full_leader, kb * kBK, b_row0);
+      tma_load_2d_pair(sa, &p.tmB, full_leader, kb * kBK, b_row0);
       if constexpr (K::MC == 1)
         tma_load_2d_pair(a_dst, &p.tmA, full_leader, kb * kBK, a_row0);
       else
         tma_load_2d_pair_multicast(a_dst, &p.tmA, full_leader, kb * kBK, a_row0,
                                    same_rank_mask(rank));
     }
+  }
+
+  // Loads k-blocks kb0 .. kb0 + nk − 1 (nk <= KPS) of a unit into stage s: one
+  // arrival on the stage's full barrier counts the bytes of all of them (in
+  // a pair, both CTAs' bytes, on the leader's barrier), then each k-block's
+  // loads.
+  __device__ static void load_stage(const KParams& p, uint32_t base, uint32_t s, int32_t kb0,
+                                    int32_t nk, int32_t b_row0, int32_t a_row0, uint32_t rank,
+                                    uint32_t grp) {
+    if (K::CG == 1 || rank == 0)
+      mbar_arrive_expect_tx(bar_full(base, s), (uint32_t)nk * K::kKbBytes * (uint32_t)K::CG);
+    for (int32_t q = 0; q < nk; ++q)
+      load_kb(p, base, s, (uint32_t)q, kb0 + q, b_row0, a_row0, rank, grp);
   }
 
   // Kernels without a cluster start filling the ring as soon as the barriers
@@ -581,8 +597,8 @@ struct Kernel {
       const int32_t b_row0 = u.tn * K::kTileCols + (int32_t)rank * K::kCtaCols;
       const int32_t a_row0 = u.tm * K::kTileRows + (int32_t)rank * K::kBrows;
       uint32_t n = 0;
-      for (int32_t kb = u.kb_begin; kb < u.kb_end && n < (uint32_t)K::STAGES; ++kb, ++n)
-        load_stage(p, base, n, kb, b_row0, a_row0, rank, grp);
+      for (int32_t kb = u.kb_begin; kb < u.kb_end && n < (uint32_t)K::STAGES; kb += K::KPS, ++n)
+        load_stage(p, base, n, kb, min(K::KPS, u.kb_end - kb), b_row0, a_row0, rank, grp);
       return n;
     }
   }
@@ -603,12 +619,16 @@ struct Kernel {
       const int32_t a_row0 = u.tm * K::kTileRows + row_group(grp) * K::BN +
                              (int32_t)rank * K::kBrows +
                              (K::MC > 1 ? (int32_t)grp * K::kBrowsPart : 0);  // rows of A
-      for (int32_t kb = u.kb_begin + (i == 0 ? (int32_t)prefilled : 0); kb < u.kb_end; ++kb) {
+      // Stages of KPS k-blocks from the unit's start (the last one may be
+      // short); unit 0's first `prefilled` stages are already loaded.
+      const int32_t kb_first =
+          i == 0 ? min(u.kb_end, u.kb_begin + (int32_t)prefilled * K::KPS) : u.kb_begin;
+      for (int32_t kb = kb_first; kb < u.kb_end; kb += K::KPS) {
         if (!wait_bar(bar_empty(base, s), ph ^ 1, abort_flag, p.status, kSiteProducerEmpty)) {
           ok = false;
           break;
         }
-        load_stage(p, base, s, kb, b_row0, a_row0, rank, grp);
+        load_stage(p, base, s, kb, min(K::KPS, u.kb_end - kb), b_row0, a_row0, rank, grp);
         ++fills;
         if (++s == (uint32_t)K::STAGES) { s = 0; ph ^= 1; }
       }
@@ -656,22 +676,28 @@ struct Kernel {
         ok = false;
         break;
       }
-      for (int32_t kb = u.kb_begin; kb < u.kb_end; ++kb) {
+      for (int32_t kb = u.kb_begin; kb < u.kb_end; kb += K::KPS) {
         if (!wait_bar(bar_full(base, s), ph, abort_flag, p.status, kSiteMmaFull)) {
           ok = false;
           break;
         }
         if (WGEMM_TRACE && i == 0 && kb == u.kb_begin) trace_event(p, kTrFirstData);
         tcgen05_fence_after();
-        const uint32_t sa = stage_a(base, s), sb = stage_b(base, s);
+        // The stage's k-blocks (the same split as the producer's).
+        const int32_t nk = min(K::KPS, u.kb_end - kb);
 #pragma unroll
-        for (int r = 0; r < K::REPS; ++r) {
+        for (int32_t q = 0; q < K::KPS; ++q) {
+          if (q >= nk) break;
+          const uint32_t sa = stage_a(base, s) + (uint32_t)q * K::kKbBytes, sb = sa + K::kAbytes;
 #pragma unroll
-          for (int j = 0; j < kBK / 16; ++j) {
-            const uint64_t adesc = umma_smem_desc_sw128(sa + r * 128 * 128 + j * 32);
-            const uint64_t bdesc = umma_smem_desc_sw128(sb + j * 32);
-            umma_f16<K::CG>(d + r * K::BN, adesc, bdesc, idesc,
-                            (kb > u.kb_begin || j > 0) ? 1u : 0u);
+          for (int r = 0; r < K::REPS; ++r) {
+#pragma unroll
+            for (int j = 0; j < kBK / 16; ++j) {
+              const uint64_t adesc = umma_smem_desc_sw128(sa + r * 128 * 128 + j * 32);
+              const uint64_t bdesc = umma_smem_desc_sw128(sb + j * 32);
+              umma_f16<K::CG>(d + r * K::BN, adesc, bdesc, idesc,
+                              (kb + q > u.kb_begin || j > 0) ? 1u : 0u);
+            }
           }
         }
         if constexpr (K::kClusterSize == 1) umma_commit(bar_empty(base, s));

@@ -19,7 +19,8 @@ cap, and then the energy a call takes, not its time alone, sets the clock:
 a configuration that reads more from DRAM runs slower once the cap holds,
 though it ties in a lone call. For such shapes the finalists are also timed
 in blocks of consecutive flushed calls (`--sustained`, on by default), and
-that time decides.
+that time decides. At the other end, calls under 40 µs whose finalists tie
+within a timer tick are ranked by their warm-L2 kernel time from CUPTI.
 """
 from __future__ import annotations
 
@@ -47,6 +48,7 @@ SHAPES = {
             (16384, 16384, 16384), (2048, 2048, 16384), (1024, 1024, 65536)],
     "ksplit": [(2048, 2048, 16384), (1024, 1024, 65536)],
     "large": [(8192, 8192, 8192), (16384, 16384, 16384)],
+    "small": [(1024, 1024, 1024), (1536, 1536, 1536), (2048, 2048, 2048), (3072, 1280, 2048)],
 }
 
 
@@ -155,6 +157,43 @@ def time_block(wgemm, torch, bufs, M, N, K, cid, mode, splits, flush, calls):
     return statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs[calls // 3:])
 
 
+# Calls shorter than this whose finalists tie within a timer tick (flushed
+# L2, CUDA events) are told apart by their warm-L2 kernel time from CUPTI,
+# the measure of "SASS-Level Kernel Generation for Blackwell" ("How we
+# measured"): the event time then carries launch costs the kernels share.
+WARM_TIEBREAK_US = 40.0
+
+
+def time_warm_kernels(wgemm, torch, rec, bufs, M, N, K, finals, ids, rounds=4, calls=20):
+    """Median CUPTI kernel time (µs) of each finalist with a warm L2: blocks
+    of synchronised calls, the finalists' blocks alternating."""
+    dA, dB, C = bufs
+    h = torch.cuda.current_stream().cuda_stream
+    per = {j: [] for j in range(len(finals))}
+    for rnd in range(rounds):
+        order = list(range(len(finals)))
+        if rnd % 2:
+            order.reverse()
+        for j in order:
+            f = finals[j]
+            call = lambda: wgemm.wgemm_f16f32_config(dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
+                                                     M, N, K, K, K, N, ids[f["config"]],
+                                                     f["mode"], f["splits"], h)
+            for _ in range(3):
+                if call() != 0:
+                    return None
+            torch.cuda.synchronize()
+            rec.start()
+            for _ in range(calls):
+                call()
+                torch.cuda.synchronize()
+            rec.stop()
+            per[j] += [(e - s0) / 1e3 for n, s0, e, _ in rec.records() if "wgemm_kernel" in n]
+    if wgemm.wgemm_check(h) != 0:
+        raise RuntimeError(f"device error: {wgemm.wgemm_last_device_error()}")
+    return [statistics.median(per[j]) if per[j] else None for j in range(len(finals))]
+
+
 def block_calls(us):
     """Calls per sustained block: about SUSTAINED_BLOCK_US of GEMM time."""
     return max(30, int(SUSTAINED_BLOCK_US / max(us, 1.0)))
@@ -178,13 +217,19 @@ def sweep(shapes, out_path, sustained=True):
     torch.cuda.set_device(0)
     sm = torch.cuda.get_device_properties(0).multi_processor_count
     flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device="cuda")
+    from dense_fp16_gemm_02_gb300 import ktime
+    try:
+        rec = ktime.KernelTimes()
+    except ktime.KernelTimesUnavailable as e:  # no tie-break by kernel time
+        print(f"# CUPTI unavailable: {e}", file=sys.stderr, flush=True)
+        rec = None
     results = []
     for (M, N, K) in shapes:
         A, B = inputs.gemm_operands(M, N, K, seed=1000, kind="uniform")
         bufs = (torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(),
                 torch.empty((M, N), dtype=torch.float32, device="cuda"))
         del A, B
-        rows = []
+        rows, failed = [], []
         for cid, mode, s in candidates(M, N, K, names, sm // 2, sm):
             # Progress on stderr first, so a failing candidate is always named.
             print(f"# {M}x{N}x{K} {names[cid]} mode {mode} splits {s}", file=sys.stderr,
@@ -193,6 +238,8 @@ def sweep(shapes, out_path, sustained=True):
             if us is not None:
                 rows.append({"config": names[cid], "mode": mode, "splits": s, "us": round(us, 3),
                              "tflops": round(2.0 * M * N * K / us / 1e6, 1)})
+            else:  # refused by the library for this shape: recorded, never a winner
+                failed.append({"config": names[cid], "mode": mode, "splits": s})
         rows.sort(key=lambda r: r["us"])
         # Finalists: the screen times each candidate's calls back to back, so
         # clock and temperature drift over a long sweep can order near-equal
@@ -242,8 +289,19 @@ def sweep(shapes, out_path, sustained=True):
                     f["us_sustained"] = round(sum(blk[j]) / len(blk[j]), 3)
                     f["sustained_blocks_us"] = [round(v, 1) for v in blk[j]]
             finals.sort(key=lambda r: r.get("us_sustained", float("inf")))
+        elif finals[0]["us_interleaved"] < WARM_TIEBREAK_US:
+            tied = [f for f in finals
+                    if f["us_interleaved"] <= finals[0]["us_interleaved"] + TICK_US]
+            if len(tied) > 1 and rec is not None:
+                warm = time_warm_kernels(wgemm, torch, rec, bufs, M, N, K, tied, ids)
+                for f, w in zip(tied, warm or []):
+                    if w is not None:
+                        f["us_warm_kernel"] = round(w, 3)
+                finals.sort(key=lambda r: (0, r["us_warm_kernel"]) if "us_warm_kernel" in r
+                            else (1, r["us_interleaved"]))
         rows = finals + rows[nf:]
-        results.append({"shape": [M, N, K], "best": rows[0], "candidates": rows})
+        results.append({"shape": [M, N, K], "best": rows[0], "candidates": rows,
+                        "failed": failed})
         print(json.dumps({"shape": [M, N, K], "best": rows[0], "next": rows[1:4]}), flush=True)
         del bufs
         torch.cuda.empty_cache()
@@ -254,16 +312,16 @@ def sweep(shapes, out_path, sustained=True):
 
 def _score(c):
     """A candidate's time in one sweep: its sustained time where the sweep
-    took one, else its interleaved time if it was a finalist, else its
-    screen median."""
-    return c.get("us_sustained", c.get("us_interleaved", c["us"]))
+    took one, else its warm-L2 kernel time where ties were broken by it,
+    else its interleaved time if it was a finalist, else its screen median."""
+    return c.get("us_sustained", c.get("us_warm_kernel", c.get("us_interleaved", c["us"])))
 
 
 def _sustained(result):
     return any("us_sustained" in c for c in result["candidates"])
 
 
-def combine(sweeps):
+def combine(sweeps, known=None):
     """Per shape, the candidate (configuration, mode, splits) with the lowest
     mean time relative to each sweep's best, over the sweeps that timed it.
     Sweeps on different boxes rank near-equal cluster configurations
@@ -273,19 +331,47 @@ def combine(sweeps):
     under the power cap) and others did not, only the sustained ones count
     for that shape: the two regimes rank configurations differently, and
     the sustained one is how long runs of such calls behave. Candidates
-    without a sustained time in such a sweep are left out too.
+    without a sustained time in such a sweep are left out too. Likewise,
+    where sweeps broke a short shape's tie by warm-L2 kernel time, only the
+    tied finalists count, by that time.
+    `known`: the configurations compiled now; candidates of others (removed
+    since a sweep) are dropped. Sweeps that tried fewer candidates of a
+    shape than the widest sweep of it (made before configurations were
+    added) do not count for that shape, so new configurations can win; a
+    candidate a sweep tried and the library refused is listed under
+    "failed" and still counts as tried.
     Returns {shape: (candidate dict with "us" = mean time, relative score)}."""
     sustained_shapes = {tuple(r["shape"]) for d in sweeps for r in d["results"]
                         if _sustained(r)}
+    warm_shapes = {tuple(r["shape"]) for d in sweeps for r in d["results"]
+                   if any("us_warm_kernel" in c for c in r["candidates"])}
+
+    def usable(r):
+        cands = r["candidates"]
+        if known is not None:
+            cands = [c for c in cands if c["config"] in known]
+        if tuple(r["shape"]) in sustained_shapes:
+            cands = [c for c in cands if "us_sustained" in c]
+        elif tuple(r["shape"]) in warm_shapes:  # the tied finalists, by kernel time
+            cands = [c for c in cands if "us_warm_kernel" in c]
+        return cands
+
+    def tried(r):
+        keys = {(c["config"], c["mode"], c["splits"]) for c in r["candidates"] + r.get("failed", [])}
+        return {k for k in keys if known is None or k[0] in known}
+
+    widest = {}
+    for d in sweeps:
+        for r in d["results"]:
+            shape = tuple(r["shape"])
+            widest[shape] = max(widest.get(shape, 0), len(tried(r)))
     per_shape = {}
     for d in sweeps:
         for r in d["results"]:
             shape = tuple(r["shape"])
-            cands = r["candidates"]
-            if shape in sustained_shapes:
-                cands = [c for c in cands if "us_sustained" in c]
-                if not cands:
-                    continue
+            cands = usable(r)
+            if not cands or len(tried(r)) < widest[shape]:
+                continue
             best = min(_score(c) for c in cands)
             acc = per_shape.setdefault(shape, {})
             for c in cands:
@@ -306,7 +392,7 @@ def combine(sweeps):
     return out
 
 
-def emit(json_paths, inc_path=TUNED_INC):
+def emit(json_paths, inc_path=TUNED_INC, known=None):
     """Writes the measured winners as a C table the library compiles in, from
     one sweep or several (see combine)."""
     if isinstance(json_paths, str):
@@ -323,9 +409,9 @@ def emit(json_paths, inc_path=TUNED_INC):
         "// {M, N, K, configuration name, mode (0 data parallel, 1 split-K, 2 stream-K,",
         "//  3 data-parallel waves + stream-K tail, 4 stream-K with zeroing first),",
         "//  splits, measured µs per call (mean over the sweeps; back to back where the",
-        "//  sweeps timed the shape so)}",
+        "//  sweeps timed the shape so; warm-L2 kernel time where it broke a tie)}",
     ]
-    chosen = combine(sweeps)
+    chosen = combine(sweeps, known)
     # Every shape any sweep timed, in the order the sweeps list them.
     shapes = []
     for sw in sweeps:
@@ -606,7 +692,9 @@ def main(argv=None):
                     help="back-to-back calls with programmatic dependent launch off and on")
     args = ap.parse_args(argv)
     if args.emit:
-        print(emit(args.emit))
+        sys.path.insert(0, ROOT)
+        from dense_fp16_gemm_02_gb300 import wgemm
+        print(emit(args.emit, known=set(wgemm.config_names())))
         return 0
     if args.emit_rates:
         print(emit_rates(args.emit_rates, keep=args.keep))

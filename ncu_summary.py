@@ -333,6 +333,8 @@ def _config_of_kernel(kernel: str) -> str:
     args = tuple(int(x) for x in m.group(1).split(","))
     if len(args) == 10:  # captures from before the MR argument existed
         args += (1,)
+    if len(args) == 11:  # captures from before the KPS argument existed
+        args += (1,)
     sys.path.insert(0, ROOT)
     from dense_fp16_gemm_02_gb300 import build, wgemm
     build.build()
@@ -343,11 +345,11 @@ def _config_of_kernel(kernel: str) -> str:
 
 
 def _entry_args(name: str):
-    """The Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR>
+    """The Cfg<CG, REPS, BN, STAGES, ACC, EPI, MC, SCHED, OUT, FUSE, MR, KPS>
     arguments of a configuration, rebuilt from its name (g<CG>[m<MC>|r<MR>]_
-    <tile columns>x<tile rows>_s<STAGES>_a<ACC>_<epilogue>[_clc][_ab<FUSE>][_h])."""
-    m = re.match(r"g(\d)(?:m(\d))?(?:r(\d))?_(\d+)x(\d+)_s(\d+)_a(\d)_(tma|direct)(_clc)?"
-                 r"(?:_ab(\d))?(_h)?$", name)
+    <tile columns>x<tile rows>_s<STAGES>[x<KPS>]_a<ACC>_<epilogue>[_clc][_ab<FUSE>][_h])."""
+    m = re.match(r"g(\d)(?:m(\d))?(?:r(\d))?_(\d+)x(\d+)_s(\d+)(?:x(\d))?_a(\d)_(tma|direct)"
+                 r"(_clc)?(?:_ab(\d))?(_h)?$", name)
     if not m:
         return None
     cg = int(m.group(1))
@@ -355,9 +357,9 @@ def _entry_args(name: str):
     mr = int(m.group(3) or 1)
     cols, rows = int(m.group(4)), int(m.group(5))
     reps = cols // (128 * cg * mc)
-    return (cg, reps, rows // mr, int(m.group(6)), int(m.group(7)),
-            1 if m.group(8) == "tma" else 0, mc, 1 if m.group(9) else 0,
-            1 if m.group(11) else 0, int(m.group(10) or 0), mr)
+    return (cg, reps, rows // mr, int(m.group(6)), int(m.group(8)),
+            1 if m.group(9) == "tma" else 0, mc, 1 if m.group(10) else 0,
+            1 if m.group(12) else 0, int(m.group(11) or 0), mr, int(m.group(7) or 1))
 
 
 # The pages' B200 kernel times per call (µs; "SASS-Level Kernel Generation for

@@ -203,17 +203,19 @@ def test_ncu_summary_maps_every_configuration_to_its_template_arguments(tmp_path
     import ncu_summary
     names = wgemm.config_names()
     args = [ncu_summary._entry_args(n) for n in names]
-    assert all(a is not None and len(a) == 11 for a in args)
+    assert all(a is not None and len(a) == 12 for a in args)
     assert len(set(args)) == len(names)  # one configuration per template instantiation
     kernel = "void wgemm_kernel<Cfg<%s>>(KParams)" % ", ".join(str(x) for x in args[0])
     assert ncu_summary._config_of_kernel(kernel) == names[0]
-    # A row-multicast configuration, and a name captured before the eleventh
-    # template argument existed.
-    rm = [n for n in names if "r2_" in n][0]
-    k_rm = "void wgemm_kernel<Cfg<%s>>(KParams)" % ", ".join(str(x) for x in args[names.index(rm)])
-    assert ncu_summary._config_of_kernel(k_rm) == rm
-    old = "void wgemm_kernel<Cfg<%s>>(KParams)" % ", ".join(str(x) for x in args[0][:10])
-    assert ncu_summary._config_of_kernel(old) == names[0]
+    # A row-multicast configuration, one with two k-blocks per stage, and
+    # names captured before the eleventh and twelfth template arguments existed.
+    for pick in ([n for n in names if "r2_" in n][0], [n for n in names if "x2_a" in n][0]):
+        k = "void wgemm_kernel<Cfg<%s>>(KParams)" % ", ".join(str(x) for x in args[names.index(pick)])
+        assert ncu_summary._config_of_kernel(k) == pick
+    assert ncu_summary._entry_args("g1_128x64_s4x2_a2_direct")[-1] == 2
+    for n_args in (10, 11):
+        old = "void wgemm_kernel<Cfg<%s>>(KParams)" % ", ".join(str(x) for x in args[0][:n_args])
+        assert ncu_summary._config_of_kernel(old) == names[0]
     csv_text = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
                 '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
                 '"Metric Value"\n'

@@ -51,10 +51,17 @@ def test_combine_takes_the_best_mean_over_boxes():
     assert abs(score - (15.3 / 15.0 + 1.0) / 2) < 1e-12
     # One sweep alone keeps its own winner.
     assert tune.combine([box1])[shape][0]["config"] == "X"
-    # A candidate missing from a sweep cannot win by absence.
+    # A candidate the library refused on one box cannot win by absence.
     box3 = _sweep(shape, [_c("Z", 10.0, 10.0), _c("Y", 15.0, 15.0)])
     box4 = _sweep(shape, [_c("Y", 15.0, 15.0)])
+    box4["results"][0]["failed"] = [{"config": "Z", "mode": 0, "splits": 1}]
     assert tune.combine([box3, box4])[shape][0]["config"] == "Y"
+    # A sweep made before Z existed tried fewer candidates: it no longer
+    # counts for the shape, and Z, timed by every wider sweep, can win.
+    old = _sweep(shape, [_c("Y", 14.0, 14.0)])
+    assert tune.combine([box3, old])[shape][0]["config"] == "Z"
+    # Configurations no longer compiled are dropped before that comparison.
+    assert tune.combine([box3, old], known={"Y"})[shape][0]["config"] == "Y"
 
 
 def _rows(*us):
@@ -138,3 +145,21 @@ def test_rates_table_keeps_rows_not_measured_again(tmp_path):
     # Without keep, only the measured rows are written.
     tune.emit_rates([str(js)], str(inc))
     assert len([l for l in inc.read_text().splitlines() if l.startswith("{")]) == 2
+
+
+def _warm(c, us):
+    c = dict(c)
+    c["us_warm_kernel"] = us
+    return c
+
+
+def test_warm_kernel_time_breaks_short_ties():
+    shape = (1024, 1024, 1024)
+    # Two finalists tie on flushed events; the warm-L2 kernel time decides.
+    tied = _sweep(shape, [_warm(_c("P", 10.2, 10.22), 6.9), _warm(_c("Q", 10.2, 10.221), 6.4),
+                          _c("R", 12.3, 12.3)])
+    got, _ = tune.combine([tied])[shape]
+    assert got["config"] == "Q" and got["us"] == 6.4
+    # A sweep without the tie-break does not outvote it.
+    plain = _sweep(shape, [_c("P", 10.1, 10.1), _c("Q", 10.3, 10.3), _c("R", 12.0, 12.0)])
+    assert tune.combine([tied, plain])[shape][0]["config"] == "Q"
