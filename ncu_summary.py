@@ -161,18 +161,22 @@ def launches_all(csv_path: str, bench_json: str) -> None:
     b = _bench()
     d = _bench_line(bench_json)
     by = read_ncu_csv(csv_path)
+    # Only the launches of the warm-up and timed steps, which come first and
+    # have the same calls: the end-to-end passes after them call each shape
+    # once, the large ones in row panels.
+    per_step = sum(d["timing"]["calls_per_step"].values())
+    keep = (d["warmup"] + d["steps"]) * per_step
+    launches = [v for _, v in sorted(by.items(), key=lambda kv: int(kv[0]))
+                if "wgemm_kernel" in v["kernel"]][:keep]
     agg = OrderedDict()
-    for v in by.values():
-        if "wgemm_kernel" not in v["kernel"]:
-            continue
+    for v in launches:
         a = agg.setdefault(_config_of_kernel(v["kernel"]), [0, 0.0])
         a[0] += 1
         a[1] += v["gpu__time_duration.sum"] / 1000.0
     total = sum(a[1] for a in agg.values())
-    # The list also holds the warm-up steps and the end-to-end passes (one
-    # call per shape each), which weigh the large shapes more than a timed
-    # step does; the weighted share puts each configuration's mean launch
-    # time on the bench's calls per step.
+    # The weighted share puts each configuration's mean launch time on the
+    # bench's calls per step (the same as the plain share when every launch
+    # kept belongs to a step).
     bench_ms, calls = OrderedDict(), OrderedDict()
     for s in d["shapes"]:
         bench_ms[s["config"]] = bench_ms.get(s["config"], 0.0) + s["us_median"] * s["calls"]
@@ -307,7 +311,7 @@ def _waves(config: str, M: int, N: int, grid: int, mode: str, splits: int) -> st
     a = _entry_args(config)
     if not a or grid <= 0:
         return "—"
-    cg, reps, bn, _, _, _, mc, _, _, _, mr = a
+    cg, reps, bn, _, _, _, mc, _, _, _, mr, _ = a
     tile_cols, tile_rows = 128 * reps * cg * mc, bn * mr
     tiles = -(-M // tile_rows) * -(-N // tile_cols)
     cluster = cg * mc * mr
