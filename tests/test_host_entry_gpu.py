@@ -146,3 +146,27 @@ def test_host_buffers_split_k_shape(lib):
     rc, hC, keep, s = host_call(A, B, M, N, K, K, K, N)
     finish(rc, s)
     check(hC, A, B, M, N, K, "int", "split-K shape through the host call")
+
+
+def test_host_buffers_pageable_and_with_pdl(lib):
+    # Pageable host memory (plain numpy arrays) works, only without overlap;
+    # programmatic dependent launch on does not change the result.
+    M, N, K = 1500, 900, 700
+    A, B = inputs.gemm_operands(M, N, K, seed=70, kind="int")
+    C = np.full((M, N), np.nan, dtype=np.float32)
+    na, nb, nc = wgemm.host_device_elems(M, N, K)
+    dA = torch.empty(na, dtype=torch.float16, device="cuda")
+    dB = torch.empty(nb, dtype=torch.float16, device="cuda")
+    dC = torch.empty(nc, dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream()
+    prev = wgemm.wgemm_set_pdl(True)
+    try:
+        assert lib.wgemm_debug_set_host_panels(3) >= 0
+        rc = wgemm.wgemm_f16f32_host(A.ctypes.data, B.ctypes.data, C.ctypes.data, M, N, K, K, K,
+                                     N, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(),
+                                     s.cuda_stream)
+        finish(rc, s)
+    finally:
+        lib.wgemm_debug_set_host_panels(0)
+        wgemm.wgemm_set_pdl(bool(prev))
+    check(torch.from_numpy(C), A, B, M, N, K, "int", "pageable host buffers, PDL on")
