@@ -103,9 +103,14 @@ def _bench_line(bench_json: str) -> dict:
 
 SHAPE_HEADER = ("| M×N×K | configuration | mode | grid (CTAs) | waves | bench µs (events, median) | "
                 "kernel µs (CUPTI, flushed) | kernel µs (CUPTI, warm) | bench TFLOP/s | tensor frac "
-                "(bench) | ncu µs | tensor pipe active % (ncu) | SM active % (ncu) | DRAM read MB | "
-                "DRAM write MB | DRAM read ÷ compulsory A+B |\n"
-                "|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
+                "(bench) | ncu µs | SM clock GHz (ncu) | tensor pipe active % (ncu) | SM active % "
+                "(ncu) | DRAM read MB | DRAM write MB | DRAM read ÷ compulsory A+B |\n"
+                "|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
+OLD_SHAPE_HEADER = ("| M×N×K | configuration | mode | grid (CTAs) | waves | bench µs (events, median) | "
+                    "kernel µs (CUPTI, flushed) | kernel µs (CUPTI, warm) | bench TFLOP/s | tensor "
+                    "frac (bench) | ncu µs | tensor pipe active % (ncu) | SM active % (ncu) | DRAM "
+                    "read MB | DRAM write MB | DRAM read ÷ compulsory A+B |\n"
+                    "|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
 
 
 def shapes(csv_dir: str, bench_json: str) -> None:
@@ -127,6 +132,7 @@ def shapes(csv_dir: str, bench_json: str) -> None:
             raise SystemExit(f"{s['shape']}: captured {cfg}, bench ran {s['config']}")
         t = v["gpu__time_duration.sum"] / 1000.0
         active = 100.0 * v["sm__cycles_active.avg"] / v["gpc__cycles_elapsed.max"]
+        ghz = v["gpc__cycles_elapsed.max"] / v["gpu__time_duration.sum"]  # cycles per ns
         grid = int(v.get("launch__grid_size", 0))
         rd, wr = v["dram__bytes_read.sum"], v["dram__bytes_write.sum"]
         ab = 2.0 * (M * K + N * K)
@@ -135,7 +141,7 @@ def shapes(csv_dir: str, bench_json: str) -> None:
             f"{_waves(cfg, M, N, grid, s['mode'], s.get('splits', 1))} | "
             f"{s['us_median']:.3f} | {s.get('us_kernel_median', float('nan')):.3f} | "
             f"{s.get('us_kernel_warm_median', float('nan')):.3f} | {s['tflops']} | "
-            f"{s['tensor_frac']} | {t:.1f} | "
+            f"{s['tensor_frac']} | {t:.1f} | {ghz:.2f} | "
             f"{v['sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed']:.1f} | "
             f"{active:.1f} | {rd / 1e6:.1f} | {wr / 1e6:.1f} | {rd / ab:.2f} |")
         traffic.append({"kernel_src": digest, "config": cfg, "shape": s["shape"],
@@ -147,6 +153,8 @@ def shapes(csv_dir: str, bench_json: str) -> None:
         json.dump(traffic, f, indent=1)
     p = os.path.join(PROFILES, "roofline_all_shapes.md")
     text = open(p).read()
+    if SHAPE_HEADER not in text:  # a table written before the clock column
+        text = text.replace(OLD_SHAPE_HEADER, SHAPE_HEADER)
     text = _set_digest(_replace_table(text, SHAPE_HEADER, rows), digest)
     open(p, "w").write(text)
     print("\n".join(rows))
