@@ -354,12 +354,13 @@ double predict_us(const KernelEntry& e, int M, int N, int K, bool aligned, int m
 }
 
 Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma_ok, int out,
-              int fuse = 0) {
+              int fuse = 0, bool dp_only = false) {
   // The table was measured with fp32 C, the plain epilogue and rows on
   // 32-byte sectors.
   const bool aligned = rows_on_sectors(lda, ldb);
   for (const TunedRow& r : kTuned) {
-    if (out == 0 && fuse == 0 && aligned && r.M == M && r.N == N && r.K == K) {
+    if (out == 0 && fuse == 0 && aligned && r.M == M && r.N == N && r.K == K &&
+        (!dp_only || r.mode == kDataParallel)) {
       const int id = find_config(r.config);
       const bool tma = std::strstr(r.config, "_tma") != nullptr;
       if (id >= 0 && (c_tma_ok || !tma)) return {id, r.mode, r.splits};
@@ -419,7 +420,7 @@ Choice choose(DeviceState& st, int M, int N, int K, int lda, int ldb, bool c_tma
     const int64_t tiles = (int64_t)((M + e.tile_rows - 1) / e.tile_rows) *
                           ((N + e.tile_cols - 1) / e.tile_cols);
     const int kblocks = (K + kBK - 1) / kBK;
-    if (ksplit && kblocks >= 32 && tiles < w) {
+    if (ksplit && !dp_only && kblocks >= 32 && tiles < w) {
       for (int sp = 2; sp <= 16 && sp <= kblocks / 8 && tiles * sp <= w; ++sp)
         consider(kSplitK, sp);
     }
@@ -566,6 +567,19 @@ int workspace(int dev, cudaStream_t stream, size_t words, Workspace** out) {
   return WGEMM_OK;
 }
 
+// True while `stream` is being captured into a CUDA graph. K-split plans
+// are not captured: their flags carry a per-call epoch that the kernel
+// parameters fix at capture, and a replayed graph would find the flags of
+// its previous replay already up.
+bool capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
+
 int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, int N, int K,
         int lda, int ldb, int ldc, int config_id, int mode, int splits, cudaStream_t stream,
         const EpiArgs& ep = EpiArgs()) {
@@ -602,8 +616,9 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
   }
   const auto& es = registry().entries;
   const bool c_ok = c_tma_ok(C, ldc, cb);
+  const bool in_graph = capturing(stream);
   if (config_id < 0) {
-    Choice c = choose(*st, M, N, K, lda, ldb, c_ok, out, fuse);
+    Choice c = choose(*st, M, N, K, lda, ldb, c_ok, out, fuse, in_graph);
     config_id = c.config;
     mode = c.mode;
     splits = c.splits;
@@ -613,11 +628,12 @@ int run(const void* A, const void* B, void* C, int ab_type, int c_type, int M, i
   if (e.out != out || !fuse_fits(e, fuse)) return WGEMM_ERR_CONFIG;
   if (e.epi == kEpiTma && !c_ok) return WGEMM_ERR_ALIGNMENT;
   if (mode < 0) {
-    Choice c = choose(*st, M, N, K, lda, ldb, c_ok, out, fuse);
+    Choice c = choose(*st, M, N, K, lda, ldb, c_ok, out, fuse, in_graph);
     mode = c.mode;
     splits = c.splits;
     if (mode != kDataParallel && e.epi != kEpiTma) mode = kDataParallel;
   }
+  if (in_graph && mode != kDataParallel) return WGEMM_ERR_CONFIG;
   // 16-bit C is rounded once from the full fp32 sum, and the fused epilogue
   // applies alpha, beta and bias to the full sum: no K split.
   if ((out != 0 || fuse) && mode != kDataParallel) return WGEMM_ERR_CONFIG;
@@ -1028,6 +1044,8 @@ int run_noalloc(const uint16_t* A, const uint16_t* B, float* C, int M, int N, in
   }
   const int config_id = find_config("g2_512x256_s4_a1_tma");
   if (config_id < 0) return WGEMM_ERR_CONFIG;
+  // Its flags carry a per-call epoch: not a call to capture in a graph.
+  if (capturing(stream)) return WGEMM_ERR_CONFIG;
   const KernelEntry& e = *registry().entries[config_id];
   const int mw = max_workers(*st, config_id);
   if (mw < 0) return mw;
@@ -1152,7 +1170,7 @@ int run_host(const wgemm_f16_t* A, const wgemm_f16_t* B, float* C, int M, int N,
     const int rc = device_state(&dev, &st);
     if (rc != WGEMM_OK) return rc;
     if (K > 0) {
-      const Choice c = choose(*st, M, N, K, (int)kd, (int)kd, true, 0, 0);
+      const Choice c = choose(*st, M, N, K, (int)kd, (int)kd, true, 0, 0, capturing(stream));
       config = c.config;
       mode = c.mode;
       splits = c.splits;

@@ -37,6 +37,14 @@
  * the GPU beside whatever else runs there, and then all are resident at once.
  * A K-split call beside a long-running kernel from another stream therefore
  * waits for room instead of running part of its grid.
+ *
+ * CUDA graphs. The calls may be captured into a CUDA graph (stream
+ * capture) after one call of the same shape outside the capture has set up
+ * the library's per-device state. While `stream` is capturing, the choice
+ * takes data-parallel plans only: a K-split plan's flags carry a per-call
+ * epoch fixed in the kernel parameters, which a replayed graph would repeat.
+ * A K-split mode forced during capture, and wgemm_f16f32_splitk_noalloc,
+ * return WGEMM_ERR_CONFIG there, with nothing enqueued.
  */
 #ifndef WGEMM_H
 #define WGEMM_H
