@@ -514,10 +514,13 @@ def run_ours(args):
     # End to end through the public API with host buffers: every step copies
     # every shape's A and B from pinned host memory to the device, computes,
     # and copies C back, all inside the timed region. For fp16 → fp32 C the
-    # library's host-buffer call does it (wgemm_f16f32_host: B up whole, A up
-    # in row panels whose GEMMs start as their rows land, C down panel by
-    # panel), the shapes alternating between two streams so that one shape's
-    # copies overlap another's GEMMs. The other element types and the fused
+    # library's host-buffer call does it (wgemm_f16f32_host: A up in row
+    # panels and B in blocks of its rows, each GEMM piece starting as its
+    # operands land, C down piece by piece), each shape on a stream of its
+    # own, as independent calls: one shape's copies overlap another's GEMMs.
+    # A call joins its caller's stream to its downloads, so a stream shared by
+    # two shapes would hold the second one's uploads behind the first one's
+    # downloads. The other element types and the fused
     # epilogue copy on two streams of their own around the device call,
     # pipelined across the step's shapes: shape i's upload overlaps shape
     # i-1's call and shape i-2's download.
@@ -536,7 +539,7 @@ def run_ours(args):
         # The host call's device layout: K rounded up to 8, N up to 4; the
         # bench's device buffers are dense, so every shape must have both.
         assert all(K % 8 == 0 and N % 4 == 0 for (M, N, K) in shapes)
-        call_streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+        call_streams = [torch.cuda.Stream(device=dev) for _ in shapes]
     for s in range(e2e_steps + 1 if host_entry else 0):
         flush.fill_(0.0)
         torch.cuda.synchronize()
@@ -547,7 +550,7 @@ def run_ours(args):
         for i, (M, N, K) in enumerate(shapes):
             hA, hB, hC, _ = pinned[i]
             _, _, dA, dB, C = data[i]
-            cs = call_streams[i % 2]
+            cs = call_streams[i]
             rc = wgemm.wgemm_f16f32_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K, K,
                                          K, N, dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
                                          cs.cuda_stream)
@@ -625,10 +628,10 @@ def run_ours(args):
                        "spin ahead of the start event hides host enqueue latency"),
             "kernel_time": ktime_note,
             "e2e": ("every step: each shape through wgemm_f16f32_host (A and B from pinned "
-                    "host memory, C back to pinned host memory; B up whole, A up in row "
-                    "panels whose GEMMs start as their rows land, C down panel by panel), "
-                    "shapes alternating between two streams; timed from the step's start "
-                    "to the last download" if host_entry else
+                    "host memory, C back to pinned host memory; A up in row panels and B "
+                    "in blocks of its rows, each GEMM piece starting as its operands "
+                    "land, C down piece by piece), each shape on a stream of its own; "
+                    "timed from the step's start to the last download" if host_entry else
                     "every step: A and B uploaded from pinned host memory, the call, C "
                     "downloaded; uploads and downloads on two copy streams, pipelined "
                     "across the step's shapes; timed from the first upload to the last "

@@ -69,6 +69,10 @@ def load():
         lib.wgemm_debug_set_host_panels.restype = i
         lib.wgemm_debug_host_panel_rows.argtypes = [i, i, i]
         lib.wgemm_debug_host_panel_rows.restype = i
+        lib.wgemm_debug_set_host_blocks.argtypes = [i]
+        lib.wgemm_debug_set_host_blocks.restype = i
+        lib.wgemm_debug_host_block_cols.argtypes = [i, i]
+        lib.wgemm_debug_host_block_cols.restype = i
         lib.wgemm_gemm.argtypes = [p, p, p, i, i, i, i, i, i, i, i, p]
         lib.wgemm_gemm.restype = i
         lib.wgemm_gemm_config.argtypes = [p, p, p, i, i, i, i, i, i, i, i, i, i, i, p]

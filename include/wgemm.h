@@ -333,12 +333,16 @@ int wgemm_f16f32_splitk_noalloc(const wgemm_f16_t* A, const wgemm_f16_t* B, floa
  * multiple of 4 (the pitches the call uses on the device). Their contents
  * on return are the device copies of A, B and C.
  *
- * How it runs: B goes up whole; A goes up in row panels (a multiple of 256
- * rows each; as many as min(A bytes, C bytes) holds 8 MiB, 1 to 8, and one
- * when the product splits K); each panel's GEMM runs on `stream` as soon as
- * its rows have landed, with the configuration chosen for the whole shape,
- * and each panel of C goes down as soon as it is computed. So the uploads and
- * downloads overlap the other panels' GEMMs. The copies run on two streams
+ * How it runs: A goes up in row panels (a multiple of 256 rows each; as
+ * many as min(A bytes, C bytes) holds 8 MiB, 1 to 8) and B in blocks of its
+ * rows, that is C's columns (a multiple of 256 rows each; as many as B's
+ * bytes hold 128 MiB, 1 to 4); a product that splits K has one panel and one
+ * block. The uploads run in the order the GEMMs need them: the first half of
+ * B's blocks, every panel of A, then B's other blocks. The GEMM of each
+ * (panel, block) runs on `stream` as soon as both have landed, with the
+ * configuration chosen for the whole shape, and each such block of C goes
+ * down as soon as it is computed. So the uploads and downloads overlap the
+ * other blocks' GEMMs. The copies run on two streams
  * the library creates per device (one per direction); they wait for
  * everything enqueued on `stream` before the call, and `stream` waits for
  * the last download, so work enqueued on `stream` after the call sees C in
@@ -422,6 +426,18 @@ int wgemm_debug_set_cooperative(int enable);
  */
 int wgemm_debug_set_host_panels(int panels);
 int wgemm_debug_host_panel_rows(int M, int N, int K);
+
+/*
+ * Test hook: blocks > 0 makes wgemm_f16f32_host split B's rows (C's columns)
+ * into that many blocks (before the rounding to 256 rows), whatever B's
+ * bytes; 0 (the default) restores the rule. Returns the previous setting, or
+ * WGEMM_ERR_INVALID_ARG for blocks outside 0..4.
+ * wgemm_debug_host_block_cols: B's rows (C's columns) per block that
+ * wgemm_f16f32_host uses for a data-parallel product with this N and K
+ * (host only), or WGEMM_ERR_INVALID_ARG.
+ */
+int wgemm_debug_set_host_blocks(int blocks);
+int wgemm_debug_host_block_cols(int N, int K);
 
 /*
  * Timeline tracing (a library built with WGEMM_TRACE=1 only; other builds

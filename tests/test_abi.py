@@ -295,3 +295,23 @@ def test_host_buffer_entry_without_launch(lib):
     finally:
         lib.wgemm_debug_set_host_panels(prev)
     assert lib.wgemm_debug_set_host_panels(9) == -1
+    # Blocks of B's rows (C's columns): B bytes / 128 MiB, 1 to 4, a multiple
+    # of 256 rows each.
+    cols = lib.wgemm_debug_host_block_cols
+    assert cols(16384, 16384) == 4096  # B is 512 MiB: four blocks
+    assert cols(8192, 8192) == 8192  # 128 MiB: one block
+    assert cols(8192, 32768) == 2048  # 512 MiB: four blocks
+    assert cols(2048, 65536) == 1024  # 256 MiB: two blocks
+    assert cols(1024, 65536) == 1024  # 128 MiB: one block
+    assert cols(777, 520) == 777
+    assert cols(0, 4) == -1 and cols(4, 0) == -1
+    prev = lib.wgemm_debug_set_host_blocks(2)
+    try:
+        assert cols(777, 520) == 512  # ceil(777 / 2) rounded up to 256
+        assert cols(200, 520) == 200  # one block of 256 covers it
+        lib.wgemm_debug_set_host_blocks(4)
+        assert cols(777, 520) == 256  # 256 + 256 + 256 + 9
+    finally:
+        lib.wgemm_debug_set_host_blocks(prev)
+    assert lib.wgemm_debug_set_host_blocks(5) == -1
+    assert lib.wgemm_debug_set_host_blocks(-1) == -1

@@ -86,6 +86,7 @@ def test_host_buffer_call_captured_in_a_graph(lib):
                                              K, K, K, N, dA.data_ptr(), dB.data_ptr(),
                                              dC.data_ptr(), h)
     assert lib.wgemm_debug_set_host_panels(3) >= 0
+    assert lib.wgemm_debug_set_host_blocks(4) >= 0
     try:
         s = torch.cuda.Stream()
         assert call(s.cuda_stream) == 0  # warm-up outside the capture
@@ -95,6 +96,7 @@ def test_host_buffer_call_captured_in_a_graph(lib):
             assert call(torch.cuda.current_stream().cuda_stream) == 0
     finally:
         lib.wgemm_debug_set_host_panels(0)
+        lib.wgemm_debug_set_host_blocks(0)
     for rep in range(2):
         hC.fill_(float("nan"))
         g.replay()

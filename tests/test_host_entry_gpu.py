@@ -1,5 +1,6 @@
 """GPU parity of wgemm_f16f32_host (A, B and C in host memory, uploads and
-downloads pipelined with row panels of the GEMM) against the CPU oracle:
+downloads pipelined with row panels of A and blocks of B's rows) against the
+CPU oracle:
 exact on integer inputs, |C − C_ref| ≤ 2e-3·(|A|·|B|ᵀ) + 1e-6 on uniform
 inputs ("SASS-Level Kernel Generation for Blackwell", section "The numbers",
 the setup paragraph: C = A·Bᵀ, fp16 in, fp32 accumulation and output)."""
@@ -24,6 +25,7 @@ def lib():
     lib = wgemm.load()
     yield lib
     lib.wgemm_debug_set_host_panels(0)
+    lib.wgemm_debug_set_host_blocks(0)
 
 
 def host_call(A, B, M, N, K, lda, ldb, ldc, stream=None, sentinel=np.nan):
@@ -61,32 +63,45 @@ def check(hC, A, B, M, N, K, kind, what):
         assert (err <= RTOL * ref_abs + ATOL).all(), f"{what}: outside tolerance"
 
 
-@pytest.mark.parametrize("panels", [0, 2, 4])
+@pytest.mark.parametrize("panels,blocks", [(0, 0), (2, 0), (4, 0), (0, 2), (3, 2), (3, 4)])
 @pytest.mark.parametrize("kind", ["int", "uniform"])
-def test_host_buffers_with_panels(lib, kind, panels):
+def test_host_buffers_with_panels(lib, kind, panels, blocks):
     # Host pitches above the row lengths; K not a multiple of 8 (device
     # pitch 528); N not a multiple of 4 (device pitch 780); with 4 panels the
-    # rows split 256 + 256 + 256 + 232.
+    # rows split 256 + 256 + 256 + 232, with 2 blocks the columns 512 + 265
+    # (the second block's C starts 512 floats into each device row), with 4
+    # blocks 256 + 256 + 256 + 9 (two before A, two after).
     M, N, K = 1000, 777, 521
     lda, ldb, ldc = K + 3, K + 11, N + 5
-    A, B = inputs.gemm_operands(M, N, K, seed=41 + panels, kind=kind, lda=lda, ldb=ldb)
+    A, B = inputs.gemm_operands(M, N, K, seed=41 + panels + 10 * blocks, kind=kind, lda=lda,
+                                ldb=ldb)
     assert lib.wgemm_debug_set_host_panels(panels) >= 0
+    assert lib.wgemm_debug_set_host_blocks(blocks) >= 0
     try:
         rc, hC, keep, s = host_call(A, B, M, N, K, lda, ldb, ldc)
         finish(rc, s)
     finally:
         lib.wgemm_debug_set_host_panels(0)
-    check(hC, A, B, M, N, K, kind, f"host buffers, {panels} panels")
+        lib.wgemm_debug_set_host_blocks(0)
+    check(hC, A, B, M, N, K, kind, f"host buffers, {panels} panels, {blocks} blocks")
     assert np.isnan(hC.numpy()[:, N:]).all(), "columns past N were written"
 
 
-def test_host_buffers_default_panels_at_8192(lib):
-    # The rule's own split: min(A, C) = 128 MiB gives eight panels of 1024 rows.
+@pytest.mark.parametrize("blocks", [0, 4])
+def test_host_buffers_default_panels_at_8192(lib, blocks):
+    # The rule's own split: min(A, C) = 128 MiB gives eight panels of 1024
+    # rows; B (128 MiB) stays one block unless the hook asks for four, the
+    # split the rule gives a B of 512 MiB (16384³).
     M = N = K = 8192
     assert lib.wgemm_debug_host_panel_rows(M, N, K) == 1024
-    A, B = inputs.gemm_operands(M, N, K, seed=43, kind="int")
-    rc, hC, keep, s = host_call(A, B, M, N, K, K, K, N)
-    finish(rc, s)
+    assert lib.wgemm_debug_host_block_cols(N, K) == 8192
+    A, B = inputs.gemm_operands(M, N, K, seed=43 + blocks, kind="int")
+    assert lib.wgemm_debug_set_host_blocks(blocks) >= 0
+    try:
+        rc, hC, keep, s = host_call(A, B, M, N, K, K, K, N)
+        finish(rc, s)
+    finally:
+        lib.wgemm_debug_set_host_blocks(0)
     rows = np.r_[0:32, 1008:1056, 4080:4112, 7152:7200, 8160:8192]  # seams between panels
     ref = oracle.gemm_f64(A[rows], B, K=K)
     got = hC.numpy()[rows].astype(np.float64)
@@ -139,12 +154,19 @@ def test_host_buffer_argument_errors(lib):
 
 def test_host_buffers_split_k_shape(lib):
     # The table runs 1024×1024×65536 as split-K 9: through the host call it
-    # stays one launch (one panel), with the K split, exact on integers.
+    # stays one launch (one panel, one block, even with the hooks asking for
+    # more), with the K split, exact on integers.
     M, N, K = 1024, 1024, 65536
     assert wgemm.wgemm_select(M, N, K)[1] == 1  # split-K
     A, B = inputs.gemm_operands(M, N, K, seed=44, kind="int")
-    rc, hC, keep, s = host_call(A, B, M, N, K, K, K, N)
-    finish(rc, s)
+    assert lib.wgemm_debug_set_host_panels(4) >= 0
+    assert lib.wgemm_debug_set_host_blocks(2) >= 0
+    try:
+        rc, hC, keep, s = host_call(A, B, M, N, K, K, K, N)
+        finish(rc, s)
+    finally:
+        lib.wgemm_debug_set_host_panels(0)
+        lib.wgemm_debug_set_host_blocks(0)
     check(hC, A, B, M, N, K, "int", "split-K shape through the host call")
 
 
