@@ -113,3 +113,12 @@ def test_compare_argument_errors(argv):
     r = subprocess.run([sys.executable, os.path.join(ROOT, "compare.py"), *argv],
                        cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert r.returncode == 2 and "error" in r.stderr
+
+
+@pytest.mark.parametrize("argv", [["--rounds", "0"], ["--steps", "0"],
+                                  ["--workload", "nosuch"]])
+def test_e2e_variants_argument_errors(argv):
+    """e2e_variants.py refuses bad options before it touches a GPU."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "e2e_variants.py"), *argv],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 2 and "error" in r.stderr
