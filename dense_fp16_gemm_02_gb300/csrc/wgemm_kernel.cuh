@@ -248,6 +248,10 @@ struct Cfg {
   static_assert(kBrows % 8 == 0, "operand rows in 8-row groups");
   static_assert(kAccCols * ACC <= 512, "TMEM capacity");
   static_assert(kSmemBytes <= 232448, "shared memory");
+  // The MMA thread offsets one descriptor per stage (16-byte units in a
+  // 14-bit field): shared-window addresses of the buffer, reserved space and
+  // alignment slack included, must stay below 256 KB.
+  static_assert(kSmemBytes + 4096 <= (1u << 18), "descriptor address field");
   static_assert(kKbBytes % 1024 == 0, "stage and k-block alignment");
   static_assert(KPS == 1 || KPS == 2, "KPS");
 };
@@ -685,17 +689,22 @@ struct Kernel {
         tcgen05_fence_after();
         // The stage's k-blocks (the same split as the producer's).
         const int32_t nk = min(K::KPS, u.kb_end - kb);
+        // One descriptor for the stage; every operand slice of it lies a
+        // constant number of 16-byte units further. The stage starts
+        // 1024-byte aligned and all of shared memory lies below 256 KB, so
+        // the descriptor's 14-bit address field never carries into the
+        // fields above it (host test: `wgemm_debug_smem_desc` offsets).
+        const uint64_t desc0 = umma_smem_desc_sw128(stage_a(base, s));
 #pragma unroll
         for (int32_t q = 0; q < K::KPS; ++q) {
           if (q >= nk) break;
-          const uint32_t sa = stage_a(base, s) + (uint32_t)q * K::kKbBytes, sb = sa + K::kAbytes;
 #pragma unroll
           for (int r = 0; r < K::REPS; ++r) {
 #pragma unroll
             for (int j = 0; j < kBK / 16; ++j) {
-              const uint64_t adesc = umma_smem_desc_sw128(sa + r * 128 * 128 + j * 32);
-              const uint64_t bdesc = umma_smem_desc_sw128(sb + j * 32);
-              umma_f16<K::CG>(d + r * K::BN, adesc, bdesc, idesc,
+              const uint32_t a_off = (uint32_t)q * K::kKbBytes + r * 128 * 128 + j * 32;
+              const uint32_t b_off = (uint32_t)q * K::kKbBytes + K::kAbytes + j * 32;
+              umma_f16<K::CG>(d + r * K::BN, desc0 + (a_off >> 4), desc0 + (b_off >> 4), idesc,
                               (kb + q > u.kb_begin || j > 0) ? 1u : 0u);
             }
           }

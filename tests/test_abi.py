@@ -60,6 +60,20 @@ def test_smem_descriptor_k_advance(lib):
         assert d1 - d0 == 2 * j
 
 
+def test_smem_descriptor_offsets_do_not_carry(lib):
+    # The MMA thread encodes one descriptor per stage and adds each operand
+    # slice's offset in 16-byte units. That equals encoding the slice's own
+    # address whenever the sum stays below 256 KB (shared memory per CTA is
+    # at most 227 KB): the 14-bit address field never carries.
+    for base in range(0, 232 * 1024, 8 * 1024):
+        d0 = lib.wgemm_debug_smem_desc(base)
+        for off in (16, 32, 96, 1024, 16384, 24 * 1024 + 32, 65536 + 96, 200 * 1024):
+            if base + off < 256 * 1024:
+                assert lib.wgemm_debug_smem_desc(base + off) == d0 + (off >> 4), (base, off)
+    # At 256 KB the field would wrap: the bound is real.
+    assert lib.wgemm_debug_smem_desc(256 * 1024) != lib.wgemm_debug_smem_desc(0) + (1 << 14)
+
+
 def test_sw128_layout_matches_address_bit_xor(lib):
     # TMA's 128-byte swizzle: within each 1024-byte block, byte address bits
     # [4:6] are XORed with bits [7:9]. Rebuild the image of a 128×64 fp16 tile
