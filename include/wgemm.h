@@ -38,6 +38,12 @@
  * A K-split call beside a long-running kernel from another stream therefore
  * waits for room instead of running part of its grid.
  *
+ * Host threads. The GEMM entry points may be called from several host threads
+ * at once; the library's state is guarded by its own locks (a call holds them
+ * while it chooses and enqueues, not while the GPU runs). The wgemm_debug_*
+ * hooks set process-wide values without a lock: set them while no call is in
+ * progress.
+ *
  * CUDA graphs. The calls may be captured into a CUDA graph (stream
  * capture) after one call of the same shape outside the capture has set up
  * the library's per-device state. While `stream` is capturing, the choice
